@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the paged sparse/sliding-window MQA decode path.
+
+A step is one full decode call over a batch: dsa_decode_run (gather +
+dequant + attention, one fused kernel) then dsa_decode_combine (split-KV
+merge). Default workload: 1024 decode tokens, 64 query heads, fp8 sliding
+window list of 128 over a 2^16-slot cache plus a 4096-wide NVFP4 list over a
+4M-slot (1.2 GB) cache, sink and RoPE on -- the bandwidth-stress
+configuration at its largest batch. All inputs are seeded synthetic data.
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle
+instead (the reference arm); ``--gpus N`` under torchrun runs N replicas.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from swa_paged_decode_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode tokens/s; gathered-KV HBM GB/s as % of GB300 peak (1 GPU)"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20        # > 2x the 126 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=5, help="workload 1..5")
+    ap.add_argument("--tokens", type=int, default=None, help="batch size (default: config's)")
+    ap.add_argument("--per-config", dest="per_config", action="store_true", default=True)
+    ap.add_argument("--quick", dest="per_config", action="store_false",
+                    help="skip the per-configuration table")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false", default=True)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU work for the oracle baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------ accounting
+
+def kept_rows(w: W.Workload) -> torch.Tensor:
+    """Per-token kept rows per list (bench-side accounting of the algorithmic
+    work: positions below clamp(len, 0, width) whose id is a cache slot)."""
+    cnt = []
+    for c, l in ((w.swa_cache, w.swa), (w.extra_cache, w.extra)):
+        if l is None:
+            continue
+        r = torch.arange(l.width, device=l.ids.device)[None, :]
+        lim = l.lens.clamp(0, l.width).to(torch.int64)[:, None]
+        ok = (r < lim) & (l.ids >= 0) & (l.ids.to(torch.int64) < c.num_slots)
+        cnt.append((ok.sum(1), c.record_bytes))
+    return cnt
+
+
+def algorithmic(w: W.Workload):
+    cnt = kept_rows(w)
+    rows = sum(int(k.sum()) for k, _ in cnt)
+    gathered = sum(int(k.sum()) * rb for k, rb in cnt)
+    flops = 2 * 2 * W.HEAD_DIM * w.H * rows      # QK^T and PV, 2 flops per MAC
+    ids_bytes = 4 * (w.swa.width + (0 if w.extra is None else w.extra.width)) * w.T
+    io_bytes = w.T * w.H * W.HEAD_DIM * 2 * 2 + w.T * w.H * 4   # q in, out, lse
+    return dict(rows=rows, gathered_bytes=gathered, flops=flops,
+                total_bytes=gathered + ids_bytes + io_bytes)
+
+
+# ------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock / throttle reasons while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.file is None or self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ GPU arm
+
+class Step:
+    def __init__(self, w: W.Workload, B):
+        self.w = w
+        self.B = B
+        self.dec = B.Decoder(w)
+        self.has_combine = self.dec.plan.ctas_per_group > 1
+
+    def __call__(self, ev_k0=None, ev_k1=None):
+        w, B, d = self.w, self.B, self.dec
+        if ev_k0 is not None:
+            ev_k0.record()
+        B.dsa_decode_run(d.plan, d.workspace, w.q, w.swa_cache, w.swa.ids, w.swa.lens,
+                         w.extra_cache, None if w.extra is None else w.extra.ids,
+                         None if w.extra is None else w.extra.lens, w.sink, w.positions,
+                         w.cos_sin, w.scale, d.out, d.lse)
+        if ev_k1 is not None:
+            ev_k1.record()
+        B.dsa_decode_combine(d.plan, d.workspace, w.sink, d.out, d.lse)
+
+
+def time_steps(step: Step, steps: int, warmup: int, flush: torch.Tensor, clocks=None):
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [(E(), E(), E(), E()) for _ in range(steps)]
+    ctx = clocks if clocks is not None else _Null()
+    with ctx:
+        for s0, k0, k1, s1 in evs:
+            flush.zero_()
+            s0.record()
+            step(k0, k1)
+            s1.record()
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, _, _, b in evs]
+    kern_ms = [a.elapsed_time(b) for _, a, b, _ in evs]
+    return sum(step_ms), step_ms, kern_ms
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def e2e_steps(w: W.Workload, B, steps: int, warmup: int, flush: torch.Tensor):
+    """Same step through the public API from pinned HOST buffers: per step the
+    per-token inputs (Q, slot lists, lengths, positions) go host->device and
+    out + lse come back device->host inside the timed region. The caches and
+    the sink (model state) stay resident."""
+    host = {}
+    names = ["q", "swa_ids", "swa_lens"] + (["extra_ids", "extra_lens"] if w.extra is not None else []) \
+        + (["positions"] if w.positions is not None else [])
+    src = {"q": w.q, "swa_ids": w.swa.ids, "swa_lens": w.swa.lens,
+           "extra_ids": None if w.extra is None else w.extra.ids,
+           "extra_lens": None if w.extra is None else w.extra.lens, "positions": w.positions}
+    dev = {}
+    for n in names:
+        host[n] = src[n].cpu().pin_memory()
+        dev[n] = torch.empty_like(src[n])
+    dec = B.Decoder(w)
+    out_h = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+    lse_h = torch.empty(dec.lse.shape, dtype=dec.lse.dtype).pin_memory()
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    def one():
+        for n in names:
+            dev[n].copy_(host[n], non_blocking=True)
+        B.dsa_decode_run(dec.plan, dec.workspace, dev["q"], w.swa_cache, dev["swa_ids"],
+                         dev["swa_lens"], w.extra_cache, dev.get("extra_ids"), dev.get("extra_lens"),
+                         w.sink, dev.get("positions"), w.cos_sin, w.scale, dec.out, dec.lse)
+        B.dsa_decode_combine(dec.plan, dec.workspace, w.sink, dec.out, dec.lse)
+        out_h.copy_(dec.out, non_blocking=True)
+        lse_h.copy_(dec.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        one()
+        b.record()
+        b.synchronize()
+        total += a.elapsed_time(b)
+    return total, h2d, d2h
+
+
+def roofline(w: W.Workload, alg, kern_ms_avg: float, peaks, peak_kind):
+    hbm = peaks["hbm_gbs"]
+    tf = peaks["bf16_tflops"]
+    intensity = alg["flops"] / max(alg["gathered_bytes"], 1)
+    ridge = tf * 1e12 / (hbm * 1e9)
+    s = kern_ms_avg * 1e-3
+    if intensity > ridge:
+        ach = alg["flops"] / s / 1e12
+        r = {"bound": "tensor", "achieved": ach, "peak": tf, "unit": "TFLOP/s",
+             "frac": ach / tf}
+    else:
+        ach = alg["gathered_bytes"] / s / 1e9
+        r = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
+    r["traffic"] = None
+    r["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+    r["intensity_flop_per_byte"] = intensity
+    r["kernel_ms"] = kern_ms_avg
+    return r
+
+
+def gpu_arm(args, rank, world, B, peaks, peak_kind):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    w = W.make_config(args.config, T=args.tokens, device=dev)
+    alg = algorithmic(w)
+    step = Step(w, B)
+    clocks = ClockSampler(dev.index)
+    total_ms, step_ms, kern_ms = time_steps(step, args.steps, args.warmup, flush, clocks)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = w.T * world / (ms_per_step * 1e-3)
+    kern_avg = sum(kern_ms) / len(kern_ms)
+    e2e_ms, h2d, d2h = e2e_steps(w, B, max(3, args.steps // 2), args.warmup, flush)
+    e2e_value = w.T * world / (e2e_ms / max(3, args.steps // 2) * 1e-3)
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if step.dec.plan.kernel == 1 else "fp32",
+        "data": "synthetic (seeded N(0,1) rows quantized to fp8/NVFP4 records, random slot lists)",
+        "config": {"workload": w.name, "T": w.T, "H": w.H,
+                   "swa": f"fp8_528 w{w.swa.width} page {w.swa_cache.page_size} "
+                          f"{w.swa_cache.num_slots} slots",
+                   "extra": None if w.extra is None else
+                   f"{['fp8_528', 'nvfp4_288'][w.extra_cache.fmt]} w{w.extra.width} page "
+                   f"{w.extra_cache.page_size} {w.extra_cache.num_slots} slots",
+                   "sink": w.sink is not None, "rope": w.cos_sin is not None,
+                   "global_batch": w.T * world, "l2": "flushed (256 MiB write before every step)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "kernel": ["simt", "tcgen05"][step.dec.plan.kernel]},
+        "gathered_hbm": {"bytes_per_step": alg["gathered_bytes"],
+                         "gbs": alg["gathered_bytes"] / (kern_avg * 1e-3) / 1e9,
+                         "frac_of_peak": alg["gathered_bytes"] / (kern_avg * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                         "gbs_step": alg["gathered_bytes"] / (ms_per_step * 1e-3) / 1e9},
+        "roofline": roofline(w, alg, kern_avg, peaks, peak_kind),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (1 + (1 if step.has_combine else 0)),
+        "clocks": clocks.summary(),
+    }
+    return res, w
+
+
+def per_config_table(B, peaks, peak_kind, steps=20, warmup=3):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    rows = []
+    for k, T in [(1, None), (2, None), (3, None), (4, None)] + [(5, t) for t in W.CONFIG5_BATCHES]:
+        w = W.make_config(k, T=T, device=dev)
+        alg = algorithmic(w)
+        step = Step(w, B)
+        total, step_ms, kern_ms = time_steps(step, steps, warmup, flush)
+        med = statistics.median(step_ms)
+        kmed = statistics.median(kern_ms)
+        rows.append({"workload": w.name, "tokens_per_s": w.T / (med * 1e-3),
+                     "ms_step_median": med, "ms_kernel_median": kmed,
+                     "gathered_gbs": alg["gathered_bytes"] / (kmed * 1e-3) / 1e9,
+                     "gathered_frac_hbm": alg["gathered_bytes"] / (kmed * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "tflops": alg["flops"] / (kmed * 1e-3) / 1e12,
+                     "tensor_frac": alg["flops"] / (kmed * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                     "splits": step.dec.plan.ctas_per_group})
+        del step, w
+        torch.cuda.empty_cache()
+    return rows
+
+
+# ------------------------------------------------------------ CPU (oracle) arm
+
+def oracle_timing(w: W.Workload, target_s: float, seed: int = 0):
+    """Time the fp64 oracle on a bounded token sample of workload w."""
+    import numpy as np
+
+    import oracle
+    a = W.oracle_args(w)
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(seed)
+    n = min(w.T, cores)
+    tok = np.sort(rng.choice(w.T, size=n, replace=False))
+    t0 = time.perf_counter()
+    oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
+                  positions=a["positions"], cos_sin=a["cos_sin"], tokens=tok, nthreads=cores)
+    dt = time.perf_counter() - t0
+    per_tok = dt / n
+    n2 = int(max(1, min(w.T, target_s / max(per_tok, 1e-9))))
+    if n2 > n:
+        tok = np.sort(rng.choice(w.T, size=n2, replace=False))
+        t0 = time.perf_counter()
+        oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
+                      positions=a["positions"], cos_sin=a["cos_sin"], tokens=tok, nthreads=cores)
+        dt = time.perf_counter() - t0
+        n = n2
+    return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens of {w.name} (fp64 C oracle, {cores} threads), {dt:.1f} s"}
+
+
+def reference_arm(args):
+    """The fp64 oracle as the reference arm: K steps, each a bounded token
+    sample of the same workload, on this host's cores."""
+    import numpy as np
+
+    import oracle
+    w = W.make_config(args.config, T=args.tokens, device="cpu")
+    a = W.oracle_args(w)
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    n = min(w.T, max(1, cores))
+    def one():
+        tok = np.sort(rng.choice(w.T, size=n, replace=False))
+        t0 = time.perf_counter()
+        oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
+                      positions=a["positions"], cos_sin=a["cos_sin"], tokens=tok, nthreads=cores)
+        return time.perf_counter() - t0
+    for _ in range(args.warmup):
+        one()
+    tot = sum(one() for _ in range(args.steps))
+    value = n * args.steps / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "T": w.T, "H": w.H,
+                                            "step": f"{n} sampled tokens"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{n} tokens per step of {w.name}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return line
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            # oracle runs on host cores only; the rendezvous is not needed
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+    from swa_paged_decode_gb300 import binding as B
+    from swa_paged_decode_gb300 import build as BLD
+    if rank == 0:
+        BLD.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        dist.barrier()
+    B.load()
+    peaks, peak_kind = load_peaks()
+    res, w = gpu_arm(args, rank, world, B, peaks, peak_kind)
+    if rank == 0 and world == 1:
+        if args.per_config:
+            res["per_config"] = per_config_table(B, peaks, peak_kind)
+        if args.cpu_baseline:
+            res["cpu_baseline"] = oracle_timing(w, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * dsa_decode.h -- C ABI of the GB300 (sm_103a) paged sparse/sliding-window
+ * MQA decode-attention library (libdsa_decode.so).
+ *
+ * The operation (one decode step of a DeepSeek-V4-style MQA layer): for each
+ * decode token t and query head h, gather the KV rows named by two slot
+ * lists -- a sliding-window list and an optional "extra" (compressed or
+ * top-k) list -- from paged, quantized caches; one 512-dim row serves as both
+ * key and value; compute
+ *     s_j  = scale * q[t,h] . k_j
+ *     lse  = log sum_j exp(s_j)                       (natural log, no sink)
+ *     out  = sum_j exp(s_j) k_j / (sum_j exp(s_j) + exp(sink[h]))
+ * Sources: the vLLM "swapab_decode_attn" page (SwapABDecodeKernel: __call__
+ * docstring for the argument meanings, stage_inputs for slot validity and
+ * paged addressing, the merge step for the sink) and FlashMLA's
+ * csrc/api/sparse_decode.h page (sparse_attn_decode_interface: MQA with one
+ * KV head, head dim 512, optional sink / extra cache / lengths, split-KV
+ * accumulators merged by a combine kernel).
+ *
+ * Conventions for every entry point:
+ *   - All device pointers are CUDA device (or managed) memory of the current
+ *     device. The caller owns every buffer, including the workspace; the
+ *     library never allocates device memory and never synchronizes, except
+ *     dsa_decode_read_status, which says so.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     dsa_decode_run then dsa_decode_combine must be issued in that order on
+ *     one stream, with the same plan and workspace.
+ *   - Argument errors are reported before anything is launched; launch
+ *     failures come back as DSA_ERR_CUDA. No entry point throws or aborts.
+ *   - Optional features are switched on by non-NULL pointers: the extra list,
+ *     the sink, RoPE (positions + cos_sin).
+ */
+#ifndef DSA_DECODE_H_
+#define DSA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *dsa_stream_t;
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = -1, /* NULL where required, bad shape, bad value     */
+  DSA_ERR_UNSUPPORTED = -2, /* head count / format / width not supported     */
+  DSA_ERR_ALIGNMENT = -3,   /* a pointer or stride breaks an alignment rule  */
+  DSA_ERR_WORKSPACE = -4,   /* workspace NULL, too small or misaligned       */
+  DSA_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed          */
+  DSA_ERR_TIMEOUT = -6,     /* device status: a bounded wait gave up         */
+  DSA_ERR_PLAN = -7         /* plan not made by dsa_decode_plan / mismatched */
+} dsa_status;
+
+/* KV record formats (one record = one slot = one 512-dim row).
+ * FP8_528  : 512 e4m3 codes, then 4 little-endian fp32 scales (one per 128
+ *            dims); value = code * scale.
+ * NVFP4_288: 256 bytes of e2m1 nibbles (element 2i in the low nibble of byte
+ *            i), then 32 e4m3 scales (one per 16 dims); value = code * scale.
+ * Source: the swapab page (record sizes 528 and 288, NVFP4 block of 16 with
+ * e4m3 scales) with the fp32-per-128 scale layout of FlashMLA's V3.2 record
+ * (sparse_decode.h, bytes_per_token = 512 + ... + (512/128)*4).            */
+enum { DSA_REC_FP8_528 = 0, DSA_REC_NVFP4_288 = 1 };
+
+/* A paged cache: base[num_pages][page_stride_bytes] bytes; the record of slot
+ * s lies at base + (s / page_size) * page_stride_bytes
+ *                + (s % page_size) * record_bytes.
+ * base: device pointer, 16-byte aligned. page_size: power of two (>= 1).
+ * page_stride_bytes: >= page_size * record_bytes and a multiple of 16 (pages
+ * may lie further apart than page_size * record_bytes). Slot ids outside
+ * [0, num_pages * page_size) are ignored, never dereferenced.            */
+typedef struct {
+  const void *base;
+  int64_t num_pages;
+  int64_t page_stride_bytes;
+  int32_t page_size;
+  int32_t format; /* DSA_REC_* */
+} dsa_cache_desc;
+
+/* Launch plan. Made by dsa_decode_plan on the host from shapes only (slot
+ * lengths are not read, so planning needs no device synchronization and a
+ * planned step can be captured in a CUDA graph). Plain data: copy it freely;
+ * callers must not edit the fields. */
+typedef struct {
+  int32_t magic;           /* identifies a plan made by this library         */
+  int32_t abi_version;
+  int32_t num_tokens;      /* T                                              */
+  int32_t num_heads;       /* H                                              */
+  int32_t swa_width;       /* columns of the sliding-window slot list        */
+  int32_t extra_width;     /* columns of the extra slot list (0 = none)      */
+  int32_t num_sms;         /* SM count the plan was made for                 */
+  int32_t head_groups;     /* CTAs that split the heads of one token         */
+  int32_t heads_per_group;
+  int32_t tiles_swa;       /* 128-row tiles per token in each list           */
+  int32_t tiles_extra;
+  int32_t tiles_per_token;
+  int32_t units_per_cta;   /* contiguous (token, tile) units per CTA         */
+  int32_t ctas_per_group;  /* CTAs per head group                            */
+  int32_t split_tokens;    /* upper bound on tokens split over CTAs          */
+  int32_t kernel;          /* internal kernel variant                        */
+  int64_t total_units;     /* T * tiles_per_token                            */
+  int64_t ws_sel_offset;   /* workspace byte offsets                         */
+  int64_t ws_part_lse_offset;
+  int64_t ws_part_sel_offset;
+  int64_t ws_part_o_offset;
+  int64_t workspace_bytes;
+  int64_t reserved[16];
+} dsa_decode_plan_t;
+
+/* Plan one decode call.
+ * num_tokens >= 0; num_heads in {16, 32, 48, 64, 96, 128}; swa_width >= 1;
+ * extra_width >= 0 (0 = no extra list). num_sms: SM count to spread the
+ * work over (0 = query the current device). On success fills *plan and
+ * *workspace_bytes (bytes of device scratch the caller must pass to run and
+ * combine; 256-byte aligned; 0 is possible only for num_tokens == 0).
+ * Host-only; launches nothing. */
+dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_width,
+                           int32_t extra_width, int32_t num_sms,
+                           dsa_decode_plan_t *plan, size_t *workspace_bytes);
+
+/* Run the fused gather + dequant + attention kernel (argument order after the
+ * plan and workspace follows the problem statement: q, sliding-window cache
+ * and list, extra cache and list, sink, positions, cos_sin, scale, out, lse).
+ *
+ * q          : bf16 [T, H, 512], element (t, h, d) at q + t*q_stride_t +
+ *              h*q_stride_h + d (strides in elements); 16-byte aligned rows.
+ * swa_cache  : required. swa_idx: int32 [T, swa_idx_stride >= swa_width]
+ *              slot ids (-1 = unused), 16-byte aligned, swa_idx_stride a
+ *              multiple of 4. swa_lens: int32 [T]; entries at positions >=
+ *              clamp(len, 0, width) are ignored.
+ * extra_*    : all NULL when plan->extra_width == 0, else all required, same
+ *              rules as the sliding-window list.
+ * sink       : fp32 [H] natural-log logits (not multiplied by scale), or NULL.
+ * positions  : int64 [T] in [0, cos_sin_rows), and cos_sin: fp32
+ *              [cos_sin_rows, 64] rows [cos(32) | sin(32)], 16-byte aligned;
+ *              both NULL = no RoPE. With RoPE, q dims 448..511 are rotated
+ *              NeoX style (dim 448+i pairs with 480+i) before the scores.
+ * scale      : softmax scale (e.g. 512^-0.5), finite.
+ * out        : bf16 [T, H, 512] contiguous, 16-byte aligned.
+ * lse        : fp32 [T, H] contiguous (natural-log LSE over the kept rows,
+ *              without the sink; -inf when no row is kept).
+ * Tokens whose work the plan splits over several CTAs get their out / lse
+ * from dsa_decode_combine, which must follow on the same stream. */
+dsa_status dsa_decode_run(const dsa_decode_plan_t *plan, void *workspace,
+                          size_t workspace_bytes, const void *q, int64_t q_stride_t,
+                          int64_t q_stride_h, const dsa_cache_desc *swa_cache,
+                          const int32_t *swa_idx, int64_t swa_idx_stride,
+                          const int32_t *swa_lens, const dsa_cache_desc *extra_cache,
+                          const int32_t *extra_idx, int64_t extra_idx_stride,
+                          const int32_t *extra_lens, const float *sink,
+                          const int64_t *positions, const float *cos_sin,
+                          int64_t cos_sin_rows, float scale, void *out, float *lse,
+                          dsa_stream_t stream);
+
+/* Merge the split-KV partials left in the workspace by dsa_decode_run:
+ * out = sum_i e^{lse_i} O_i / (sum_i e^{lse_i} + e^{sink}), lse = log sum_i
+ * e^{lse_i}, in a fixed split order (bitwise deterministic). `sink` must be
+ * the pointer given to run (or NULL). Launches nothing when the plan splits
+ * no token. */
+dsa_status dsa_decode_combine(const dsa_decode_plan_t *plan, void *workspace,
+                              size_t workspace_bytes, const float *sink, void *out,
+                              float *lse, dsa_stream_t stream);
+
+/* Row-selection record of the last run+combine on this workspace: per token
+ * the number of kept rows (kept[T], int32, device) and the sum mod 2^32 over
+ * kept rows of fmix32(id * 0x9E3779B1 + 2*position + list) (checksum[T],
+ * uint32, device; list 0 = sliding window, 1 = extra; fmix32 = MurmurHash3's
+ * 32-bit finalizer). Asynchronous copy on `stream`. */
+dsa_status dsa_decode_selection(const dsa_decode_plan_t *plan, const void *workspace,
+                                int32_t *kept, uint32_t *checksum, dsa_stream_t stream);
+
+/* Device status word of the workspace (DSA_OK, or DSA_ERR_TIMEOUT when a
+ * bounded device wait gave up). SYNCHRONIZES `stream` to read it. */
+dsa_status dsa_decode_read_status(const void *workspace, dsa_stream_t stream,
+                                  int32_t *device_status);
+
+/* Static description of a status code. */
+const char *dsa_decode_status_string(dsa_status s);
+
+/* ABI version of this header (bumped on any layout change). */
+int32_t dsa_decode_abi_version(void);
+
+#define DSA_DECODE_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_DECODE_H_ */

@@ -1,0 +1,188 @@
+"""ctypes binding of libdsa_decode.so (include/dsa_decode.h).
+
+Argument marshalling only: torch tensors become device pointers, strides and
+sizes; every step of the decode runs in the library's CUDA kernels. The
+functions keep the C names. Loading fails loudly when the library is missing
+(there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import workloads as W
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libdsa_decode.so")
+
+DSA_OK = 0
+STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED",
+                -3: "DSA_ERR_ALIGNMENT", -4: "DSA_ERR_WORKSPACE", -5: "DSA_ERR_CUDA",
+                -6: "DSA_ERR_TIMEOUT", -7: "DSA_ERR_PLAN"}
+EXPORTED = ("dsa_decode_plan", "dsa_decode_run", "dsa_decode_combine", "dsa_decode_selection",
+            "dsa_decode_read_status", "dsa_decode_status_string", "dsa_decode_abi_version")
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} -> {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("num_pages", ctypes.c_int64),
+                ("page_stride_bytes", ctypes.c_int64), ("page_size", ctypes.c_int32),
+                ("format", ctypes.c_int32)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "magic", "abi_version", "num_tokens", "num_heads", "swa_width", "extra_width",
+        "num_sms", "head_groups", "heads_per_group", "tiles_swa", "tiles_extra",
+        "tiles_per_token", "units_per_cta", "ctas_per_group", "split_tokens", "kernel")] + \
+        [(n, ctypes.c_int64) for n in (
+            "total_units", "ws_sel_offset", "ws_part_lse_offset", "ws_part_sel_offset",
+            "ws_part_o_offset", "workspace_bytes")] + [("reserved", ctypes.c_int64 * 16)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libdsa_decode.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m swa_paged_decode_gb300.build`"
+                           " (the CUDA library is required; there is no fallback)")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.dsa_decode_plan.restype = ctypes.c_int
+    lib.dsa_decode_plan.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(Plan),
+                                    ctypes.POINTER(ctypes.c_size_t)]
+    lib.dsa_decode_run.restype = ctypes.c_int
+    lib.dsa_decode_run.argtypes = [ctypes.POINTER(Plan), vp, ctypes.c_size_t, vp, i64, i64,
+                                   ctypes.POINTER(CacheDesc), vp, i64, vp,
+                                   ctypes.POINTER(CacheDesc), vp, i64, vp,
+                                   vp, vp, vp, i64, ctypes.c_float, vp, vp, vp]
+    lib.dsa_decode_combine.restype = ctypes.c_int
+    lib.dsa_decode_combine.argtypes = [ctypes.POINTER(Plan), vp, ctypes.c_size_t, vp, vp, vp, vp]
+    lib.dsa_decode_selection.restype = ctypes.c_int
+    lib.dsa_decode_selection.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp]
+    lib.dsa_decode_read_status.restype = ctypes.c_int
+    lib.dsa_decode_read_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.dsa_decode_status_string.restype = ctypes.c_char_p
+    lib.dsa_decode_status_string.argtypes = [ctypes.c_int]
+    lib.dsa_decode_abi_version.restype = ctypes.c_int32
+    lib.dsa_decode_abi_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, rc: int):
+    if rc != DSA_OK:
+        raise DsaError(fn, rc)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def cache_desc(c: Optional[W.PagedCache]) -> Optional[CacheDesc]:
+    if c is None:
+        return None
+    return CacheDesc(c.data.data_ptr(), c.num_pages, c.page_stride, c.page_size, c.fmt)
+
+
+def dsa_decode_plan(num_tokens: int, num_heads: int, swa_width: int, extra_width: int = 0,
+                    num_sms: int = 0):
+    """-> (Plan, workspace_bytes)."""
+    plan = Plan()
+    ws = ctypes.c_size_t(0)
+    _check("dsa_decode_plan", load().dsa_decode_plan(num_tokens, num_heads, swa_width,
+                                                     extra_width, num_sms, ctypes.byref(plan),
+                                                     ctypes.byref(ws)))
+    return plan, int(ws.value)
+
+
+def dsa_decode_run(plan: Plan, workspace: Optional[torch.Tensor], q: torch.Tensor,
+                   swa_cache: W.PagedCache, swa_idx: torch.Tensor, swa_lens: torch.Tensor,
+                   extra_cache: Optional[W.PagedCache], extra_idx: Optional[torch.Tensor],
+                   extra_lens: Optional[torch.Tensor], sink: Optional[torch.Tensor],
+                   positions: Optional[torch.Tensor], cos_sin: Optional[torch.Tensor],
+                   scale: float, out: torch.Tensor, lse: torch.Tensor, stream=None,
+                   check: bool = True) -> int:
+    sc, ec = cache_desc(swa_cache), cache_desc(extra_cache)
+    rc = load().dsa_decode_run(
+        ctypes.byref(plan), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        q.data_ptr(), q.stride(0), q.stride(1),
+        ctypes.byref(sc), swa_idx.data_ptr(), swa_idx.stride(0), swa_lens.data_ptr(),
+        None if ec is None else ctypes.byref(ec), _ptr(extra_idx),
+        0 if extra_idx is None else extra_idx.stride(0), _ptr(extra_lens),
+        _ptr(sink), _ptr(positions), _ptr(cos_sin),
+        0 if cos_sin is None else cos_sin.shape[0], float(scale),
+        out.data_ptr(), lse.data_ptr(), _stream(stream))
+    if check:
+        _check("dsa_decode_run", rc)
+    return rc
+
+
+def dsa_decode_combine(plan: Plan, workspace: Optional[torch.Tensor], sink: Optional[torch.Tensor],
+                       out: torch.Tensor, lse: torch.Tensor, stream=None, check: bool = True) -> int:
+    rc = load().dsa_decode_combine(ctypes.byref(plan), _ptr(workspace),
+                                   0 if workspace is None else workspace.numel(), _ptr(sink),
+                                   out.data_ptr(), lse.data_ptr(), _stream(stream))
+    if check:
+        _check("dsa_decode_combine", rc)
+    return rc
+
+
+def dsa_decode_selection(plan: Plan, workspace: torch.Tensor, kept: torch.Tensor,
+                         checksum: torch.Tensor, stream=None):
+    _check("dsa_decode_selection", load().dsa_decode_selection(
+        ctypes.byref(plan), workspace.data_ptr(), kept.data_ptr(), checksum.data_ptr(),
+        _stream(stream)))
+
+
+def dsa_decode_read_status(workspace: torch.Tensor, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check("dsa_decode_read_status", load().dsa_decode_read_status(
+        workspace.data_ptr(), _stream(stream), ctypes.byref(v)))
+    return int(v.value)
+
+
+class Decoder:
+    """Plan + workspace for one workload shape; ``__call__`` runs run+combine
+    on the current stream. Allocation uses torch; compute is the library's."""
+
+    def __init__(self, w: W.Workload, num_sms: int = 0):
+        self.plan, nbytes = dsa_decode_plan(w.T, w.H, w.swa.width,
+                                            0 if w.extra is None else w.extra.width, num_sms)
+        dev = w.q.device
+        self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((w.T, w.H, W.HEAD_DIM), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+
+    def __call__(self, w: W.Workload, stream=None):
+        dsa_decode_run(self.plan, self.workspace, w.q, w.swa_cache, w.swa.ids, w.swa.lens,
+                       w.extra_cache, None if w.extra is None else w.extra.ids,
+                       None if w.extra is None else w.extra.lens, w.sink, w.positions,
+                       w.cos_sin, w.scale, self.out, self.lse, stream)
+        dsa_decode_combine(self.plan, self.workspace, w.sink, self.out, self.lse, stream)
+        return self.out, self.lse
+
+    def selection(self, stream=None):
+        kept = torch.empty(self.plan.num_tokens, dtype=torch.int32, device=self.out.device)
+        chk = torch.empty(self.plan.num_tokens, dtype=torch.int32, device=self.out.device)
+        dsa_decode_selection(self.plan, self.workspace, kept, chk, stream)
+        return kept, chk

@@ -1,0 +1,273 @@
+// dsa_api.cu -- the C ABI (include/dsa_decode.h): planning, argument
+// validation and launches. Host code only; kernels live in the other
+// translation units.
+//
+// Validation mirrors the checks FlashMLA's sparse_attn_decode_interface
+// (csrc/api/sparse_decode.h page) makes before launching: MQA with head dim
+// 512, extra indices present iff an extra cache is present, record-sized
+// contiguous pages, dtype/shape of every optional input.
+#include <cmath>
+#include <cstring>
+
+#include "dsa_internal.cuh"
+
+using dsa::Params;
+
+namespace {
+
+constexpr int64_t kAlignWs = 256;
+constexpr int64_t kStatusBytes = 256;
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+int record_bytes(int32_t fmt) {
+  return fmt == DSA_REC_FP8_528 ? 528 : (fmt == DSA_REC_NVFP4_288 ? 288 : -1);
+}
+
+bool heads_supported(int32_t H) {
+  return H == 16 || H == 32 || H == 48 || H == 64 || H == 96 || H == 128;
+}
+
+dsa_status fill_list(const dsa_cache_desc *c, const int32_t *idx, int64_t stride,
+                     const int32_t *lens, int32_t width, dsa::ListArgs &L) {
+  if (!c || !idx || !lens || !c->base) return DSA_ERR_INVALID_ARG;
+  const int rb = record_bytes(c->format);
+  if (rb < 0) return DSA_ERR_UNSUPPORTED;
+  if (c->num_pages < 1 || !pow2(c->page_size)) return DSA_ERR_INVALID_ARG;
+  if (c->page_stride_bytes < (int64_t)c->page_size * rb) return DSA_ERR_INVALID_ARG;
+  if (c->num_pages * (int64_t)c->page_size > (int64_t)INT32_MAX + 1) return DSA_ERR_UNSUPPORTED;
+  if (stride < width) return DSA_ERR_INVALID_ARG;
+  if (!aligned(c->base, 16) || c->page_stride_bytes % 16 != 0) return DSA_ERR_ALIGNMENT;
+  if (!aligned(idx, 16) || stride % 4 != 0 || !aligned(lens, 4)) return DSA_ERR_ALIGNMENT;
+  L.base = static_cast<const uint8_t *>(c->base);
+  L.num_slots = c->num_pages * (int64_t)c->page_size;
+  L.page_stride = c->page_stride_bytes;
+  L.ids = idx;
+  L.lens = lens;
+  L.idx_stride = stride;
+  int sh = 0;
+  while ((1 << sh) < c->page_size) ++sh;
+  L.page_shift = sh;
+  L.page_mask = c->page_size - 1;
+  L.fmt = c->format;
+  L.rec = rb;
+  L.width = width;
+  L.tiles = (width + dsa::kTile - 1) / dsa::kTile;
+  return DSA_OK;
+}
+
+bool plan_ok(const dsa_decode_plan_t *plan) {
+  return plan && plan->magic == dsa::kPlanMagic && plan->abi_version == DSA_DECODE_ABI_VERSION;
+}
+
+void fill_schedule(const dsa_decode_plan_t *plan, void *ws, Params &p) {
+  p.T = plan->num_tokens;
+  p.H = plan->num_heads;
+  p.hpg = plan->heads_per_group;
+  p.HG = plan->head_groups;
+  p.tpt = plan->tiles_per_token;
+  p.upc = plan->units_per_cta;
+  p.C = plan->ctas_per_group;
+  p.U = plan->total_units;
+  char *w = static_cast<char *>(ws);
+  p.status = reinterpret_cast<int32_t *>(w);
+  p.sel = reinterpret_cast<int32_t *>(w + plan->ws_sel_offset);
+  p.part_lse = reinterpret_cast<float *>(w + plan->ws_part_lse_offset);
+  p.part_sel = reinterpret_cast<int32_t *>(w + plan->ws_part_sel_offset);
+  p.part_o = reinterpret_cast<float *>(w + plan->ws_part_o_offset);
+}
+
+dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t dsa_decode_abi_version(void) { return DSA_DECODE_ABI_VERSION; }
+
+const char *dsa_decode_status_string(dsa_status s) {
+  switch (s) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DSA_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case DSA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case DSA_ERR_CUDA: return "CUDA runtime error";
+    case DSA_ERR_TIMEOUT: return "device wait timed out";
+    case DSA_ERR_PLAN: return "invalid or mismatched plan";
+  }
+  return "unknown status";
+}
+
+dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_width,
+                           int32_t extra_width, int32_t num_sms, dsa_decode_plan_t *plan,
+                           size_t *workspace_bytes) {
+  if (!plan || !workspace_bytes) return DSA_ERR_INVALID_ARG;
+  if (num_tokens < 0 || swa_width < 1 || extra_width < 0 || num_sms < 0)
+    return DSA_ERR_INVALID_ARG;
+  if (!heads_supported(num_heads)) return DSA_ERR_UNSUPPORTED;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DSA_ERR_CUDA;
+  }
+  std::memset(plan, 0, sizeof(*plan));
+  plan->magic = dsa::kPlanMagic;
+  plan->abi_version = DSA_DECODE_ABI_VERSION;
+  plan->num_tokens = num_tokens;
+  plan->num_heads = num_heads;
+  plan->swa_width = swa_width;
+  plan->extra_width = extra_width;
+  plan->num_sms = num_sms;
+  plan->head_groups = num_heads <= 64 ? 1 : 2;
+  plan->heads_per_group = num_heads / plan->head_groups;
+  plan->tiles_swa = (swa_width + dsa::kTile - 1) / dsa::kTile;
+  plan->tiles_extra = (extra_width + dsa::kTile - 1) / dsa::kTile;
+  plan->tiles_per_token = plan->tiles_swa + plan->tiles_extra;
+  plan->total_units = (int64_t)num_tokens * plan->tiles_per_token;
+  plan->kernel = dsa::kKernelSimt;
+  // Balanced static split: every CTA of a head group gets the same number of
+  // consecutive units (FlashMLA's num_sm_parts idea, sparse_decode.h get_meta,
+  // with the units cut evenly instead of per request).
+  int64_t target = num_sms / plan->head_groups;
+  if (target < 1) target = 1;
+  int64_t U = plan->total_units;
+  int64_t ctas = U < target ? U : target;
+  int64_t upc = ctas > 0 ? (U + ctas - 1) / ctas : 1;
+  ctas = upc > 0 ? (U + upc - 1) / upc : 0;
+  if (upc > INT32_MAX || ctas > INT32_MAX / 2) return DSA_ERR_UNSUPPORTED;
+  plan->units_per_cta = (int32_t)upc;
+  plan->ctas_per_group = (int32_t)ctas;
+  plan->split_tokens = ctas > 1 ? (int32_t)(ctas - 1) : 0;
+  // Workspace: status | sel[T][2] | part_lse[HG][2C][hpg] | part_sel[2C][2] |
+  //            part_o[HG][2C][hpg][512]
+  const int64_t slots = 2 * ctas;
+  int64_t off = kStatusBytes;
+  plan->ws_sel_offset = off;
+  off = align_up(off + 8 * (int64_t)num_tokens, kAlignWs);
+  plan->ws_part_lse_offset = off;
+  off = align_up(off + 4 * plan->head_groups * slots * plan->heads_per_group, kAlignWs);
+  plan->ws_part_sel_offset = off;
+  off = align_up(off + 8 * slots, kAlignWs);
+  plan->ws_part_o_offset = off;
+  off = align_up(off + 4 * plan->head_groups * slots * plan->heads_per_group * (int64_t)dsa::kD,
+                 kAlignWs);
+  plan->workspace_bytes = num_tokens == 0 ? 0 : off;
+  *workspace_bytes = (size_t)plan->workspace_bytes;
+  return DSA_OK;
+}
+
+dsa_status dsa_decode_run(const dsa_decode_plan_t *plan, void *workspace,
+                          size_t workspace_bytes, const void *q, int64_t q_stride_t,
+                          int64_t q_stride_h, const dsa_cache_desc *swa_cache,
+                          const int32_t *swa_idx, int64_t swa_idx_stride,
+                          const int32_t *swa_lens, const dsa_cache_desc *extra_cache,
+                          const int32_t *extra_idx, int64_t extra_idx_stride,
+                          const int32_t *extra_lens, const float *sink,
+                          const int64_t *positions, const float *cos_sin,
+                          int64_t cos_sin_rows, float scale, void *out, float *lse,
+                          dsa_stream_t stream) {
+  if (!plan_ok(plan)) return DSA_ERR_PLAN;
+  if (plan->num_tokens == 0) return DSA_OK;
+  if (!q || !out || !lse) return DSA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return DSA_ERR_INVALID_ARG;
+  if (q_stride_h < dsa::kD || q_stride_t < (int64_t)plan->num_heads * q_stride_h)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || q_stride_t % 8 != 0 || q_stride_h % 8 != 0) return DSA_ERR_ALIGNMENT;
+  if (!aligned(out, 16) || !aligned(lse, 4)) return DSA_ERR_ALIGNMENT;
+  const bool has_extra = plan->extra_width > 0;
+  if (has_extra != (extra_cache != nullptr) || has_extra != (extra_idx != nullptr) ||
+      has_extra != (extra_lens != nullptr))
+    return DSA_ERR_INVALID_ARG;
+  if ((positions == nullptr) != (cos_sin == nullptr)) return DSA_ERR_INVALID_ARG;
+  if (cos_sin && (cos_sin_rows < 1 || !aligned(cos_sin, 16) || !aligned(positions, 8)))
+    return cos_sin_rows < 1 ? DSA_ERR_INVALID_ARG : DSA_ERR_ALIGNMENT;
+  if (sink && !aligned(sink, 4)) return DSA_ERR_ALIGNMENT;
+  if (!workspace || (int64_t)workspace_bytes < plan->workspace_bytes ||
+      !aligned(workspace, kAlignWs))
+    return DSA_ERR_WORKSPACE;
+
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  dsa_status s = fill_list(swa_cache, swa_idx, swa_idx_stride, swa_lens, plan->swa_width,
+                           p.list[0]);
+  if (s != DSA_OK) return s;
+  p.nlists = 1;
+  if (has_extra) {
+    s = fill_list(extra_cache, extra_idx, extra_idx_stride, extra_lens, plan->extra_width,
+                  p.list[1]);
+    if (s != DSA_OK) return s;
+    p.nlists = 2;
+  }
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.q_st = q_stride_t;
+  p.q_sh = q_stride_h;
+  p.sink = sink;
+  p.positions = positions;
+  p.cos_sin = cos_sin;
+  p.cs_rows = cos_sin_rows;
+  p.scale = scale;
+  p.scale_log2 = scale * dsa::kLog2e;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.lse = lse;
+  fill_schedule(plan, workspace, p);
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, st);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  return cuda_status(dsa_launch_simt(p, st));
+}
+
+dsa_status dsa_decode_combine(const dsa_decode_plan_t *plan, void *workspace,
+                              size_t workspace_bytes, const float *sink, void *out,
+                              float *lse, dsa_stream_t stream) {
+  if (!plan_ok(plan)) return DSA_ERR_PLAN;
+  if (plan->num_tokens == 0 || plan->ctas_per_group <= 1) return DSA_OK;
+  if (!out || !lse) return DSA_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(lse, 4) || (sink && !aligned(sink, 4)))
+    return DSA_ERR_ALIGNMENT;
+  if (!workspace || (int64_t)workspace_bytes < plan->workspace_bytes ||
+      !aligned(workspace, kAlignWs))
+    return DSA_ERR_WORKSPACE;
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  fill_schedule(plan, workspace, p);
+  p.list[0].tiles = plan->tiles_swa;
+  p.list[1].tiles = plan->tiles_extra;
+  p.sink = sink;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.lse = lse;
+  return cuda_status(dsa_launch_combine(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_decode_selection(const dsa_decode_plan_t *plan, const void *workspace,
+                                int32_t *kept, uint32_t *checksum, dsa_stream_t stream) {
+  if (!plan_ok(plan)) return DSA_ERR_PLAN;
+  if (plan->num_tokens == 0) return DSA_OK;
+  if (!workspace || !kept || !checksum) return DSA_ERR_INVALID_ARG;
+  const char *w = static_cast<const char *>(workspace) + plan->ws_sel_offset;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // sel is [T][2] (kept, checksum): two strided 2-D copies.
+  cudaError_t e = cudaMemcpy2DAsync(kept, 4, w, 8, 4, plan->num_tokens,
+                                    cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpy2DAsync(checksum, 4, w + 4, 8, 4, plan->num_tokens,
+                          cudaMemcpyDeviceToDevice, st);
+  return cuda_status(e);
+}
+
+dsa_status dsa_decode_read_status(const void *workspace, dsa_stream_t stream,
+                                  int32_t *device_status) {
+  if (!workspace || !device_status) return DSA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  *device_status = v;
+  return DSA_OK;
+}
+
+}  // extern "C"

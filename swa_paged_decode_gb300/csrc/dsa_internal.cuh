@@ -1,0 +1,173 @@
+// dsa_internal.cuh -- shared definitions of the CUDA library (not part of the
+// public ABI): the launch parameter block, the static work schedule, record
+// decoding and row selection.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsa_decode.h"
+
+namespace dsa {
+
+constexpr int kD = 512;          // head dim (K = V row)
+constexpr int kTile = 128;       // KV rows per work unit
+constexpr int kRopeStart = 448;  // RoPE acts on the last 64 dims
+constexpr int kRopeHalf = 32;
+constexpr int32_t kPlanMagic = 0x31415344;  // "DSA1"
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+enum KernelVariant : int32_t { kKernelSimt = 0, kKernelTc = 1 };
+
+// One slot list with the cache it points into.
+struct ListArgs {
+  const uint8_t *base;   // cache bytes
+  int64_t num_slots;     // num_pages * page_size
+  int64_t page_stride;   // bytes
+  const int32_t *ids;    // [T, idx_stride]
+  const int32_t *lens;   // [T]
+  int64_t idx_stride;
+  int32_t page_shift;    // log2(page_size)
+  int32_t page_mask;     // page_size - 1
+  int32_t fmt;           // DSA_REC_*
+  int32_t rec;           // record bytes
+  int32_t width;
+  int32_t tiles;         // ceil(width / kTile)
+};
+
+struct Params {
+  const __nv_bfloat16 *q;
+  int64_t q_st, q_sh;          // element strides
+  ListArgs list[2];
+  int32_t nlists;
+  const float *sink;           // [H] or null
+  const int64_t *positions;    // [T] or null
+  const float *cos_sin;        // [cs_rows, 64] or null
+  int64_t cs_rows;
+  float scale;
+  float scale_log2;            // scale * log2(e)
+  __nv_bfloat16 *out;          // [T, H, 512]
+  float *lse;                  // [T, H]
+  // schedule (copied from the plan)
+  int32_t T, H, hpg, HG, tpt, upc, C;
+  int64_t U;
+  // workspace
+  int32_t *status;             // device status word
+  int32_t *sel;                // [T][2]: kept rows, checksum
+  float *part_lse;             // [HG][2C][hpg]
+  int32_t *part_sel;           // [2C][2]
+  float *part_o;               // [HG][2C][hpg][512]
+};
+
+// ---------------------------------------------------------------- schedule
+// Units are (token, tile) pairs in token-major order; CTA c of a head group
+// owns units [c*upc, min(U, (c+1)*upc)). Inside a CTA, the first and last
+// tokens may be partial ("split"); their partial results go to slot 2c (the
+// first token) and 2c+1 (the last token, when different from the first).
+struct Segment {
+  int32_t t;        // token
+  int64_t u_begin;  // first unit
+  int64_t u_end;    // one past the last unit
+  bool whole;       // covers every unit of the token
+  int32_t slot;     // partial slot when !whole
+};
+
+__host__ __device__ inline int64_t cta_unit_begin(const Params &p, int32_t c) {
+  return (int64_t)c * p.upc;
+}
+__host__ __device__ inline int64_t cta_unit_end(const Params &p, int32_t c) {
+  int64_t e = (int64_t)(c + 1) * p.upc;
+  return e < p.U ? e : p.U;
+}
+
+__device__ inline Segment make_segment(const Params &p, int32_t c, int32_t t) {
+  int64_t u0 = cta_unit_begin(p, c), u1 = cta_unit_end(p, c);
+  int64_t ts = (int64_t)t * p.tpt, te = ts + p.tpt;
+  Segment s;
+  s.t = t;
+  s.u_begin = u0 > ts ? u0 : ts;
+  s.u_end = u1 < te ? u1 : te;
+  s.whole = (s.u_begin == ts) && (s.u_end == te);
+  int32_t tf = (int32_t)(u0 / p.tpt);
+  s.slot = 2 * c + (t == tf ? 0 : 1);
+  return s;
+}
+
+// Unit -> (list, first row).
+__device__ inline void unit_tile(const Params &p, int64_t u, int32_t &lid, int32_t &row0) {
+  int32_t k = (int32_t)(u % p.tpt);
+  if (k < p.list[0].tiles) {
+    lid = 0;
+    row0 = k * kTile;
+  } else {
+    lid = 1;
+    row0 = (k - p.list[0].tiles) * kTile;
+  }
+}
+
+// ---------------------------------------------------------------- selection
+// A list position r of token t names a row iff r < clamp(len, 0, width) and
+// 0 <= id < num_slots (vLLM swapab page, SwapABDecodeKernel.stage_inputs).
+__device__ inline int32_t list_limit(const ListArgs &L, int32_t t) {
+  int32_t len = __ldg(L.lens + t);
+  len = len < 0 ? 0 : len;
+  return len < L.width ? len : L.width;
+}
+
+__device__ inline bool slot_valid(const ListArgs &L, int32_t r, int32_t limit, int32_t sid) {
+  return r < limit && sid >= 0 && (int64_t)sid < L.num_slots;
+}
+
+// Record address: page = sid >> page_shift, offset = sid & page_mask.
+__device__ inline const uint8_t *record_ptr(const ListArgs &L, int32_t sid) {
+  int64_t blk = (int64_t)(sid >> L.page_shift);
+  int64_t off = (int64_t)(sid & L.page_mask);
+  return L.base + blk * L.page_stride + off * L.rec;
+}
+
+// MurmurHash3 32-bit finalizer; feeds the row-selection checksum.
+__device__ inline uint32_t fmix32(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85ebca6bu;
+  h ^= h >> 13;
+  h *= 0xc2b2ae35u;
+  h ^= h >> 16;
+  return h;
+}
+__device__ inline uint32_t row_hash(int32_t sid, int32_t r, int32_t lid) {
+  return fmix32((uint32_t)sid * 0x9E3779B1u + 2u * (uint32_t)r + (uint32_t)lid);
+}
+
+// ---------------------------------------------------------------- decoding
+// e4m3 (bias 7, subnormal below exponent field 1) -> fp32, exact: place the
+// 7 magnitude bits at the top of the fp32 exponent/mantissa fields, which
+// reads as 2^(e-127) * (1 + m/8) (or the fp32 subnormal m * 2^-129 when e is
+// 0), then multiply by 2^120. Needs denormals kept (no -ftz).
+__device__ inline float e4m3_to_f32(uint32_t code) {
+  float mag = __uint_as_float((code & 0x7Fu) << 20) * 1.329227995784916e36f;  // 2^120
+  return (code & 0x80u) ? -mag : mag;
+}
+
+// e2m1 (bias 1, subnormal at exponent field 0) -> fp32, exact, same trick
+// with 2^126.
+__device__ inline float e2m1_to_f32(uint32_t nib) {
+  float mag = __uint_as_float((nib & 0x7u) << 22) * 8.507059173023462e37f;  // 2^126
+  return (nib & 0x8u) ? -mag : mag;
+}
+
+__device__ inline float bf16_bits_to_f32(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// Status word: first failure wins.
+__device__ inline void report_status(int32_t *status, int32_t code) {
+  atomicCAS(status, 0, code);
+}
+
+}  // namespace dsa
+
+// Launchers (defined in the kernel translation units).
+cudaError_t dsa_launch_simt(const dsa::Params &p, cudaStream_t stream);
+cudaError_t dsa_launch_combine(const dsa::Params &p, cudaStream_t stream);
