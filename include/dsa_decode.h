@@ -128,13 +128,14 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
  * q          : bf16 [T, H, 512], element (t, h, d) at q + t*q_stride_t +
  *              h*q_stride_h + d (strides in elements); 16-byte aligned rows.
  * swa_cache  : required. swa_idx: int32 [T, swa_idx_stride >= swa_width]
- *              slot ids (-1 = unused), 16-byte aligned, swa_idx_stride a
- *              multiple of 4. swa_lens: int32 [T]; entries at positions >=
- *              clamp(len, 0, width) are ignored.
+ *              slot ids (-1 = unused). swa_lens: int32 [T]; entries at
+ *              positions >= clamp(len, 0, width) are ignored.
  * extra_*    : all NULL when plan->extra_width == 0, else all required, same
  *              rules as the sliding-window list.
  * sink       : fp32 [H] natural-log logits (not multiplied by scale), or NULL.
- * positions  : int64 [T] in [0, cos_sin_rows), and cos_sin: fp32
+ * positions  : int64 [T] in [0, cos_sin_rows) (a position outside the
+ *              table sets the device status to DSA_ERR_INVALID_ARG and uses
+ *              row 0), and cos_sin: fp32
  *              [cos_sin_rows, 64] rows [cos(32) | sin(32)], 16-byte aligned;
  *              both NULL = no RoPE. With RoPE, q dims 448..511 are rotated
  *              NeoX style (dim 448+i pairs with 480+i) before the scores.

@@ -7,6 +7,7 @@
 // 512, extra indices present iff an extra cache is present, record-sized
 // contiguous pages, dtype/shape of every optional input.
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "dsa_internal.cuh"
@@ -39,7 +40,7 @@ dsa_status fill_list(const dsa_cache_desc *c, const int32_t *idx, int64_t stride
   if (c->num_pages * (int64_t)c->page_size > (int64_t)INT32_MAX + 1) return DSA_ERR_UNSUPPORTED;
   if (stride < width) return DSA_ERR_INVALID_ARG;
   if (!aligned(c->base, 16) || c->page_stride_bytes % 16 != 0) return DSA_ERR_ALIGNMENT;
-  if (!aligned(idx, 16) || stride % 4 != 0 || !aligned(lens, 4)) return DSA_ERR_ALIGNMENT;
+  if (!aligned(idx, 4) || !aligned(lens, 4)) return DSA_ERR_ALIGNMENT;
   L.base = static_cast<const uint8_t *>(c->base);
   L.num_slots = c->num_pages * (int64_t)c->page_size;
   L.page_stride = c->page_stride_bytes;
@@ -127,7 +128,12 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   plan->tiles_extra = (extra_width + dsa::kTile - 1) / dsa::kTile;
   plan->tiles_per_token = plan->tiles_swa + plan->tiles_extra;
   plan->total_units = (int64_t)num_tokens * plan->tiles_per_token;
-  plan->kernel = dsa::kKernelSimt;
+  // Tensor-core kernel for 16/32/64 heads per group; the CUDA-core kernel
+  // takes 48/96 heads, or any shape when DSA_DECODE_KERNEL=simt is set (a
+  // cross-check switch read only here, at planning time).
+  plan->kernel = dsa_tc_supports(plan->heads_per_group) ? dsa::kKernelTc : dsa::kKernelSimt;
+  if (const char *k = std::getenv("DSA_DECODE_KERNEL"))
+    if (std::strcmp(k, "simt") == 0) plan->kernel = dsa::kKernelSimt;
   // Balanced static split: every CTA of a head group gets the same number of
   // consecutive units (FlashMLA's num_sm_parts idea, sparse_decode.h get_meta,
   // with the units cut evenly instead of per request).
@@ -217,7 +223,8 @@ dsa_status dsa_decode_run(const dsa_decode_plan_t *plan, void *workspace,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, st);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
-  return cuda_status(dsa_launch_simt(p, st));
+  return cuda_status(plan->kernel == dsa::kKernelTc ? dsa_launch_tc(p, st)
+                                                    : dsa_launch_simt(p, st));
 }
 
 dsa_status dsa_decode_combine(const dsa_decode_plan_t *plan, void *workspace,

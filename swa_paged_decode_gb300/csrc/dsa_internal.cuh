@@ -170,4 +170,6 @@ __device__ inline void report_status(int32_t *status, int32_t code) {
 
 // Launchers (defined in the kernel translation units).
 cudaError_t dsa_launch_simt(const dsa::Params &p, cudaStream_t stream);
+cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream);
+bool dsa_tc_supports(int heads_per_group);
 cudaError_t dsa_launch_combine(const dsa::Params &p, cudaStream_t stream);

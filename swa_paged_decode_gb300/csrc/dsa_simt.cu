@@ -103,6 +103,10 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) 
     const Segment seg = make_segment(p, c, t);
     // Q (fp32) with NeoX RoPE on dims 448..511.
     int64_t pos = p.positions ? __ldg(p.positions + t) : 0;
+    if (pos < 0 || (p.cos_sin && pos >= p.cs_rows)) {   // outside the table: flag, use row 0
+      if (tid == 0) report_status(p.status, DSA_ERR_INVALID_ARG);
+      pos = 0;
+    }
     for (int e = tid; e < HPG * kD; e += kSimtThreads) {
       const int h = e / kD, d = e % kD;
       const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)(h0 + h) * p.q_sh;

@@ -155,7 +155,7 @@ def test_run_rejects_bad_plan(lib):
     ("q", FAKE + 8, -3), ("q_st", 16 * 512 + 4, -3), ("out", FAKE + 4, -3), ("lse", FAKE + 2, -3),
     ("ws", None, -4), ("ws_bytes", 16, -4), ("ws", FAKE + 128, -4),
     ("swa_idx", None, -1), ("swa_lens", None, -1), ("swa_stride", 64, -1),
-    ("swa_idx", FAKE + 4, -3), ("swa_stride", 130, -3), ("swa_lens", FAKE + 2, -3),
+    ("swa_idx", FAKE + 2, -3), ("swa_lens", FAKE + 2, -3),
     ("pos", FAKE, -1), ("cs", FAKE, -1), ("sink", FAKE + 1, -3),
     ("extra_idx", FAKE, -1), ("extra_lens", FAKE, -1),
 ])

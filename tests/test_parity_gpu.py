@@ -173,3 +173,29 @@ def test_stream_and_workspace_reuse_across_shapes():
     s.synchronize()
     compare(o1, l1, k1, c1, oracle_ref(w1), what="stream w1")
     compare(o2, l2, k2, c2, oracle_ref(w2), what="stream w2")
+
+
+def test_default_kernel_is_tensor_core():
+    for H in (16, 32, 64, 128):
+        plan, _ = B.dsa_decode_plan(4, H, 128, 256, 0)
+        assert plan.kernel == 1, H
+    for H in (48, 96):
+        plan, _ = B.dsa_decode_plan(4, H, 128, 256, 0)
+        assert plan.kernel == 0, H
+
+
+@pytest.mark.parametrize("H", [16, 64, 128])
+def test_cuda_core_cross_check_kernel(monkeypatch, H):
+    monkeypatch.setenv("DSA_DECODE_KERNEL", "simt")
+    w = small(200 + H, H=H, T=4)
+    dec, out, lse, kept, chk = run_gpu(w, num_sms=5)
+    assert dec.plan.kernel == 0
+    compare(out, lse, kept, chk, oracle_ref(w), what=f"simt H={H}")
+
+
+def test_position_outside_table_sets_status():
+    w = small(300, T=2)
+    w.positions[1] = W.ROPE_TABLE_ROWS + 5
+    dec = B.Decoder(w)
+    dec(w)
+    assert B.dsa_decode_read_status(dec.workspace) == -1
