@@ -11,7 +11,9 @@
 //            NVFP4: e2m1 * e4m3 scale (exact in f16);
 //            fp8:   e4m3 * s_hi, where s_hi is the fp32 block scale rounded to
 //            7 significant bits (product exact in f16); the remaining factor
-//            rho = s / s_hi (fp32) is applied to the scores, so Q.K is exact;
+//            rho = s / s_hi (fp32, per row and 128-dim block) is applied to
+//            the block scores and, for PV, to P of the matching 128-dim M
+//            block, so both products see the exact dequantized row;
 //   QK^T     swap-AB: S[128 rows, H] = K[128, 512] . Q[H, 512]^T with
 //            tcgen05.mma kind::f16 into TMEM (fp8 tiles: one accumulator per
 //            128-dim scale block, scaled by rho in fp32 afterwards);
@@ -44,25 +46,28 @@ template <int HPG>
 struct TcCfg {
   static constexpr int kHalf = HPG / 2;                  // heads per thread
   static constexpr int kPRow = HPG * 2;                  // bytes per P row
+  static constexpr int kPBufs = HPG == 64 ? 2 : 4;       // P' buffers (fp8 tiles: one per M block)
+  static constexpr uint32_t kPBytes = 128 * kPRow;       // one P tile
   static constexpr uint32_t kKV = 0;                     // 128 x 512 f16 = 128 KiB
   static constexpr uint32_t kQ = 131072;                 // HPG x 512 f16
-  static constexpr uint32_t kP = kQ + HPG * 1024;        // 128 x HPG f16
-  static constexpr uint32_t kRho = kP + 128 * kPRow;     // [128][4] f32
-  static constexpr uint32_t kValid = kRho + 2048;        // [128] i32
-  static constexpr uint32_t kHeadF = kValid + 512;       // [64] f32 per-head score factor
+  static constexpr uint32_t kP = kQ + HPG * 1024;        // kPBufs x [128 x HPG] f16
+  static constexpr uint32_t kHeadF = kP + kPBufs * kPBytes;  // [64] f32 per-head score factor
   static constexpr uint32_t kM = kHeadF + 256;           // [64] running max (log2)
   static constexpr uint32_t kAlpha = kM + 256;           // [64]
   static constexpr uint32_t kInv = kAlpha + 256;         // [64]
   static constexpr uint32_t kRed = kInv + 256;           // [4][64] f32
   static constexpr uint32_t kMisc = kRed + 1024;         // flags, mbarriers, tmem base
   static constexpr uint32_t kBytes = kMisc + 64;
-  static constexpr uint32_t kSmem = kBytes + 1024;       // + alignment slack
+  // Dynamic shared memory requested: the tiles plus slack for aligning the
+  // base to 1024 bytes, capped at the 227 KiB a CTA may use.
+  static constexpr uint32_t kSmem = kBytes + 1024 > 232448u ? 232448u : kBytes + 1024;
   static constexpr uint32_t kCols = HPG == 16 ? 128 : (HPG == 32 ? 256 : 512);
   static constexpr uint32_t kColS = 0;                   // S block b at b*HPG
   static constexpr uint32_t kColO = 4 * HPG;             // O block mb at (4+mb)*HPG
   static constexpr uint32_t kPSwz = HPG == 64 ? tc::kSwz128 : (HPG == 32 ? tc::kSwz64 : tc::kSwz32);
   static constexpr uint32_t kIdQK = tc::idesc_f16(128, HPG, false, false);
   static constexpr uint32_t kIdPV = tc::idesc_f16(128, HPG, true, true);
+  static_assert(kBytes <= 232448u, "shared memory layout exceeds 227 KiB");
 };
 
 // Byte offset of the 16-byte chunk holding f16 elements [8*ci, 8*ci+8) of
@@ -85,9 +90,12 @@ __device__ __forceinline__ uint32_t p_off(int r, int ci) {
            (uint32_t)((ci ^ ((r & 7) >> 2)) << 4);
 }
 
-// Per-thread prefetch registers for one tile (this thread's half of one row).
+// Per-thread prefetch registers for one tile. Thread (warp w, lane l) owns
+// row 32*(w%4) + l -- the TMEM lane its softmax reads -- and half j = w/4 of
+// the record's 16-byte chunks: c = 4m + 2j + e (e in {0,1}), i.e. whole
+// 32-byte sectors.
 struct Gather {
-  uint4 d[16];   // fp8: 16 chunks (c = 2k + j); NVFP4: 8 chunks
+  uint4 d[16];   // fp8: 16 chunks; NVFP4: 8 chunks
   uint4 s[2];    // fp8: s[0] = 4 fp32 scales; NVFP4: 32 e4m3 scales
   int32_t sid;
   int32_t r;
@@ -104,7 +112,7 @@ __device__ __forceinline__ void prefetch(const Params &p, int64_t u, Gather &g) 
   int32_t t, lid, row0;
   unit_info(p, u, t, lid, row0);
   const ListArgs &L = p.list[lid];
-  const int row = threadIdx.x >> 1, j = threadIdx.x & 1;
+  const int row = 32 * ((threadIdx.x >> 5) & 3) + (threadIdx.x & 31), j = threadIdx.x >> 7;
   g.r = row0 + row;
   g.sid = -1;
   if (g.r < L.width) g.sid = __ldg(L.ids + (int64_t)t * L.idx_stride + g.r);
@@ -115,7 +123,7 @@ __device__ __forceinline__ void prefetch(const Params &p, int64_t u, Gather &g) 
     if (g.ok) {
       const uint8_t *rec = record_ptr(L, g.sid);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) g.d[k] = tc::ldg_nc_v4(rec + 16 * (2 * k + j));
+      for (int k = 0; k < 16; ++k) g.d[k] = tc::ldg_nc_v4(rec + 16 * (4 * (k >> 1) + 2 * j + (k & 1)));
       g.s[0] = tc::ldg_nc_v4(rec + 512);
     } else {
 #pragma unroll
@@ -126,7 +134,7 @@ __device__ __forceinline__ void prefetch(const Params &p, int64_t u, Gather &g) 
     if (g.ok) {
       const uint8_t *rec = record_ptr(L, g.sid);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) g.d[k] = tc::ldg_nc_v4(rec + 16 * (2 * k + j));
+      for (int k = 0; k < 8; ++k) g.d[k] = tc::ldg_nc_v4(rec + 16 * (4 * (k >> 1) + 2 * j + (k & 1)));
       g.s[0] = tc::ldg_nc_v4(rec + 256);
       g.s[1] = tc::ldg_nc_v4(rec + 272);
     } else {
@@ -149,23 +157,21 @@ __device__ __forceinline__ void split_scale(float s, uint32_t &shi2, float &rho)
   shi2 = hb | (hb << 16);
 }
 
-// Registers -> f16 tile in shared memory (+ rho, valid). Returns this
-// thread's row validity.
-__device__ __forceinline__ void dequant(const Params &p, int32_t lid, uint8_t *smem,
-                                        const Gather &g, uint32_t kv_base, float *rho_s,
-                                        int32_t *valid_s) {
+// Registers -> f16 tile in shared memory. fp8 records also return the four
+// per-block factors rho = s / s_hi of this thread's row.
+__device__ __forceinline__ void dequant(const Params &p, int32_t lid, const Gather &g,
+                                        uint32_t kv_base, float (&rho)[4]) {
   const ListArgs &L = p.list[lid];
-  const int row = threadIdx.x >> 1, j = threadIdx.x & 1;
+  const int row = 32 * ((threadIdx.x >> 5) & 3) + (threadIdx.x & 31), j = threadIdx.x >> 7;
   if (L.fmt == DSA_REC_FP8_528) {
     uint32_t shi2[4];
-    float rho[4];
     split_scale(__uint_as_float(g.s[0].x), shi2[0], rho[0]);
     split_scale(__uint_as_float(g.s[0].y), shi2[1], rho[1]);
     split_scale(__uint_as_float(g.s[0].z), shi2[2], rho[2]);
     split_scale(__uint_as_float(g.s[0].w), shi2[3], rho[3]);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      const int c = 2 * k + j;  // dims [16c, 16c+16), scale block c/8
+      const int c = 4 * (k >> 1) + 2 * j + (k & 1);  // dims [16c, 16c+16), scale block c/8
       const uint32_t sc = shi2[c >> 3];
       const uint32_t w[4] = {g.d[k].x, g.d[k].y, g.d[k].z, g.d[k].w};
       uint32_t f[8];
@@ -179,16 +185,13 @@ __device__ __forceinline__ void dequant(const Params &p, int32_t lid, uint8_t *s
       tc::st_shared_v4(kv_base + sw128_off(row, kb, ci, 16384), f[0], f[1], f[2], f[3]);
       tc::st_shared_v4(kv_base + sw128_off(row, kb, ci + 1, 16384), f[4], f[5], f[6], f[7]);
     }
-    if (j == 0) {
-      reinterpret_cast<float4 *>(rho_s)[row] = make_float4(rho[0], rho[1], rho[2], rho[3]);
-      valid_s[row] = g.ok ? 1 : 0;
-    }
   } else {
+    rho[0] = rho[1] = rho[2] = rho[3] = 1.f;
     const uint32_t sw[8] = {g.s[0].x, g.s[0].y, g.s[0].z, g.s[0].w,
                             g.s[1].x, g.s[1].y, g.s[1].z, g.s[1].w};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int c = 2 * k + j;  // dims [32c, 32c+32), scales 2c (first 16) and 2c+1
+      const int c = 4 * (k >> 1) + 2 * j + (k & 1);  // dims [32c, 32c+32), scales 2c, 2c+1
       const uint32_t pair = (sw[c >> 1] >> (16 * (c & 1))) & 0xFFFFu;
       const uint32_t s2 = tc::e4m3x2_to_f16x2(pair);
       const uint32_t sa = __byte_perm(s2, s2, 0x1010), sb = __byte_perm(s2, s2, 0x3232);
@@ -204,7 +207,6 @@ __device__ __forceinline__ void dequant(const Params &p, int32_t lid, uint8_t *s
         tc::st_shared_v4(kv_base + sw128_off(row, kb, ci, 16384), f[0], f[1], f[2], f[3]);
       }
     }
-    if (j == 0) valid_s[row] = g.ok ? 1 : 0;
   }
 }
 
@@ -213,14 +215,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   using Cfg = TcCfg<HPG>;
   constexpr int NH = Cfg::kHalf;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = tc::smem_u32(smem);
+  // Swizzled tiles need a 1024-byte aligned base (the swizzle acts on
+  // address bits); the layout is checked to fit after aligning.
+  const uint32_t raw_base = tc::smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
+  if (pad + Cfg::kBytes > Cfg::kSmem) {
+    if (threadIdx.x == 0) report_status(p.status, DSA_ERR_UNSUPPORTED);
+    return;
+  }
+  uint8_t *smem = smem_raw + pad;
+  const uint32_t sbase = raw_base + pad;
   const uint32_t kv_base = sbase + Cfg::kKV;
   const uint32_t q_base = sbase + Cfg::kQ;
   const uint32_t p_base = sbase + Cfg::kP;
-  float *rho_s = reinterpret_cast<float *>(smem + Cfg::kRho);
-  int32_t *valid_s = reinterpret_cast<int32_t *>(smem + Cfg::kValid);
   float *headf_s = reinterpret_cast<float *>(smem + Cfg::kHeadF);
   float *m_s = reinterpret_cast<float *>(smem + Cfg::kM);
   float *alpha_s = reinterpret_cast<float *>(smem + Cfg::kAlpha);
@@ -231,7 +238,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   uint32_t *red_u = reinterpret_cast<uint32_t *>(flag_s + 2);   // [2] selection reduction
   uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + Cfg::kMisc + 16);
   uint64_t *bar_o = bar_s + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kMisc + 32);
+  uint64_t *bar_p = bar_s + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kMisc + 48);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, half = warp >> 2;
@@ -249,6 +257,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   if (tid == 0) {
     tc::mbar_init(bar_s, 1);
     tc::mbar_init(bar_o, 1);
+    tc::mbar_init(bar_p, 1);
     tc::fence_mbar_init();
     *flag_s = 0;
     *err_s = 0;
@@ -259,7 +268,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   const uint32_t tmem = *tmem_slot;
   const uint32_t tl_lane = tmem + ((uint32_t)(32 * q4) << 16);   // this warp's TMEM lanes
 
-  uint32_t ph_s = 0, ph_o = 0;
+  uint32_t ph_s = 0, ph_o = 0, ph_p = 0;
   bool o_pending = false;
   bool failed = false;
   float m_reg[NH], l_reg[NH];
@@ -430,14 +439,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     }
     wait_o();
     const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
-    dequant(p, lid, smem, g, kv_base, rho_s, valid_s);
-    if ((threadIdx.x & 1) == 0 && g.ok) {
+    float rho[4];
+    dequant(p, lid, g, kv_base, rho);
+    const bool row_ok = g.ok;
+    if (half == 0 && g.ok) {
       kept += 1;
       chk += row_hash(g.sid, g.r, lid);
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
-    const int st = __syncthreads_or((g.ok ? 1 : 0) | (failed ? 2 : 0));
+    const int st = __syncthreads_or((row_ok ? 1 : 0) | (failed ? 2 : 0));
     tc::tc_fence_after();
     if (st & 2) {
       failed = true;
@@ -468,10 +479,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     // ---- softmax on this thread's row and NH heads
     float x[NH];
     {
-      const bool rv = valid_s[prow] != 0;
+      const bool rv = row_ok;
       if (fp8) {
-        const float4 rh = reinterpret_cast<const float4 *>(rho_s)[prow];
-        const float rr[4] = {rh.x, rh.y, rh.z, rh.w};
 #pragma unroll
         for (int j = 0; j < NH; ++j) x[j] = 0.f;
 #pragma unroll
@@ -479,7 +488,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           float sv[NH];
           tc::tmem_ld<NH>(tl_lane + Cfg::kColS + b * HPG + half * NH, sv);
 #pragma unroll
-          for (int j = 0; j < NH; ++j) x[j] = fmaf(rr[b], sv[j], x[j]);
+          for (int j = 0; j < NH; ++j) x[j] = fmaf(rho[b], sv[j], x[j]);
         }
       } else {
         tc::tmem_ld<NH>(tl_lane + Cfg::kColS + half * NH, x);
@@ -533,45 +542,64 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         }
       }
     }
-    // P = 2^(x - m) (<= 2^8), f16, MN-major [128 rows, HPG]
-    {
-      uint32_t pw[NH / 2];
+    // P = 2^(x - m) (<= 2^8); f16, MN-major [128 rows, HPG].
 #pragma unroll
-      for (int j = 0; j < NH; j += 2) {
-        const float p0 = (x[j] == -INFINITY) ? 0.f : tc::ex2(x[j] - m_reg[j]);
-        const float p1 = (x[j + 1] == -INFINITY) ? 0.f : tc::ex2(x[j + 1] - m_reg[j + 1]);
-        l_reg[j] += p0;
-        l_reg[j + 1] += p1;
-        pw[j / 2] = tc::pack_f16x2(p0, p1);
-      }
-#pragma unroll
-      for (int k = 0; k < NH / 8; ++k) {
-        const int ci = half * (NH / 8) + k;
-        tc::st_shared_v4(p_base + p_off<HPG>(prow, ci), pw[4 * k], pw[4 * k + 1], pw[4 * k + 2],
-                         pw[4 * k + 3]);
-      }
+    for (int j = 0; j < NH; ++j) {
+      x[j] = (x[j] == -INFINITY) ? 0.f : tc::ex2(x[j] - m_reg[j]);
+      l_reg[j] += x[j];
     }
-    tc::fence_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    // ---- O^T += K^T . P
-    if (tid == 0) {
-      *flag_s = 0;
-      tc::tc_fence_after();
-#pragma unroll 1
-      for (int mb = 0; mb < 4; ++mb) {
+    // NVFP4 tiles: one P for all four M blocks. fp8 tiles: P'_mb = P * rho_mb
+    // for M block mb, written kPBufs at a time.
+    const int nbatch = fp8 ? 4 / Cfg::kPBufs : 1;
+    bool late = false;
+    for (int batch = 0; batch < nbatch; ++batch) {
+      if (batch > 0) {   // the previous batch's MMAs must be done reading P'
+        late |= !tc::mbar_wait(bar_p, ph_p, kWaitIters);
+        ph_p ^= 1;
+        tc::tc_fence_after();
+      }
+      const int nb = fp8 ? Cfg::kPBufs : 1;
+      for (int i = 0; i < nb; ++i) {
+        const float f = fp8 ? rho[batch * nb + i] : 1.f;
+        uint32_t pw[NH / 2];
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t ad =
-              tc::sdesc(kv_base + 2 * mb * 16384 + ks * 2048, 16384, 1024, tc::kSwz128);
-          const uint64_t bd = tc::sdesc(p_base + ks * 16 * Cfg::kPRow, 128 * Cfg::kPRow,
-                                        8 * Cfg::kPRow, Cfg::kPSwz);
-          tc::mma_f16(tmem + Cfg::kColO + mb * HPG, ad, bd, Cfg::kIdPV,
-                      (first_pv && ks == 0) ? 0u : 1u);
+        for (int j = 0; j < NH; j += 2) pw[j / 2] = tc::pack_f16x2(x[j] * f, x[j + 1] * f);
+#pragma unroll
+        for (int k = 0; k < NH / 8; ++k) {
+          const int ci = half * (NH / 8) + k;
+          tc::st_shared_v4(p_base + i * Cfg::kPBytes + p_off<HPG>(prow, ci), pw[4 * k],
+                           pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
         }
       }
-      tc::mma_commit(bar_o);
+      tc::fence_async_smem();
+      tc::tc_fence_before();
+      if (__syncthreads_or(late ? 1 : 0)) {
+        failed = true;
+        break;
+      }
+      // ---- O^T += K^T . P
+      if (tid == 0) {
+        *flag_s = 0;
+        tc::tc_fence_after();
+        const int mb0 = fp8 ? batch * Cfg::kPBufs : 0;
+        const int mb1 = fp8 ? mb0 + Cfg::kPBufs : 4;
+#pragma unroll 1
+        for (int mb = mb0; mb < mb1; ++mb) {
+          const uint32_t pb = p_base + (fp8 ? (uint32_t)(mb - mb0) * Cfg::kPBytes : 0u);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t ad =
+                tc::sdesc(kv_base + 2 * mb * 16384 + ks * 2048, 16384, 1024, tc::kSwz128);
+            const uint64_t bd = tc::sdesc(pb + ks * 16 * Cfg::kPRow, Cfg::kPBytes,
+                                          8 * Cfg::kPRow, Cfg::kPSwz);
+            tc::mma_f16(tmem + Cfg::kColO + mb * HPG, ad, bd, Cfg::kIdPV,
+                        (first_pv && ks == 0) ? 0u : 1u);
+          }
+        }
+        tc::mma_commit(batch + 1 < nbatch ? bar_p : bar_o);
+      }
     }
+    if (failed) break;
     o_pending = true;
     first_pv = false;
   }
