@@ -1,32 +1,40 @@
 // dsa_tc.cu -- fused gather + dequant + attention on sm_103a tensor cores.
 //
-// One persistent CTA (256 threads, one per SM: its shared memory forbids a
-// second) walks a contiguous range of (token, 128-row tile) units. Per tile:
+// One persistent CTA per SM walks a contiguous range of (token, 128-row tile)
+// units with three warp-specialised roles joined by mbarriers:
 //
-//   gather   predicated 16-byte loads of the tile's 128 records (2 threads
-//            per row), issued one tile ahead so they are in flight while the
-//            previous tile computes;
-//   dequant  records -> f16 K-major tile in shared memory, 128-byte swizzle
-//            (16-byte chunk c of row r stored at chunk c ^ (r % 8));
-//            NVFP4: e2m1 * e4m3 scale (exact in f16);
-//            fp8:   e4m3 * s_hi, where s_hi is the fp32 block scale rounded to
-//            7 significant bits (product exact in f16); the remaining factor
-//            rho = s / s_hi (fp32, per row and 128-dim block) is applied to
-//            the block scores and, for PV, to P of the matching 128-dim M
-//            block, so both products see the exact dequantized row;
-//   QK^T     swap-AB: S[128 rows, H] = K[128, 512] . Q[H, 512]^T with
-//            tcgen05.mma kind::f16 into TMEM (fp8 tiles: one accumulator per
-//            128-dim scale block, scaled by rho in fp32 afterwards);
-//   softmax  one TMEM lane (= one KV row) per thread pair, base-2, with a
-//            running per-head max that is only raised when a score exceeds
-//            it by more than 2^8 (then O in TMEM and the partial sums are
-//            rescaled) -- the common tile needs no cross-row max at all;
-//   PV       O^T[512, H] += K^T[512, 128] . P[128, H], four 128-dim M blocks,
-//            A read MN-major from the same shared tile, accumulated in TMEM.
+//   producers (warps 8-15)  gather: predicated 16-byte loads of the tile's
+//            128 records, one tile ahead, held in registers (thread = one row
+//            and one half of its 32-byte sectors); dequant: records -> f16
+//            K-major tile in shared memory, 128-byte swizzle (16-byte chunk c
+//            of row r at chunk c ^ (r % 8)), written one 128-dim block at a
+//            time as soon as the PV MMAs of the previous tile release it.
+//            NVFP4: e2m1 * e4m3 scale (exact in f16). fp8: e4m3 * s_hi with
+//            s_hi = the fp32 block scale rounded to 7 significant bits (the
+//            product is exact in f16); rho = s / s_hi goes to the softmax.
+//   MMA issue (one thread of warp 0)  swap-AB tcgen05.mma kind::f16:
+//            S[128 rows, H] = K[128, 512] . Q[H, 512]^T into TMEM (fp8 tiles:
+//            one accumulator per 128-dim scale block), issued block by block
+//            as the producers land them; then O^T[512, H] += K^T . P in four
+//            128-dim M blocks, A read MN-major from the same tile. Commits
+//            release tile blocks (to the producers) and S / O (to softmax).
+//   softmax (warps 0-7)     one TMEM lane (= one KV row) and half of the heads
+//            per thread; scores x = (sum_b rho_b S_b) * scale * log2e;
+//            base-2 running max per head that moves only when a score passes
+//            it by 2^8 (then O in TMEM and the partial sums are rescaled);
+//            P = 2^(x - m) as f16 (fp8 tiles: P'_mb = P * rho_mb per M block,
+//            so PV sees the exact row as well). Also stages Q (NeoX RoPE,
+//            per-head power-of-two prescale into f16) and, per token,
+//            reduces the sums, folds the sink into the denominator and writes
+//            out (bf16) and lse (fp32) -- or an fp32 partial for a token split
+//            over CTAs, merged later by the combine kernel.
 //
-// At the end of a token: per-head sums reduced over rows, sink folded into
-// the denominator, bf16 out and fp32 lse written (or an fp32 partial for a
-// token split over CTAs, merged later by the combine kernel).
+// Tiles whose first row lies past min(len, width) are skipped by every role
+// (each evaluates the same predicate from the lengths), so all roles walk the
+// same sequence of tiles and tokens. Every mbarrier wait is bounded; when one
+// gives up the CTA records DSA_ERR_TIMEOUT, later waits return at once and no
+// further MMA is issued, while every role still walks its loops to the end
+// (named barriers keep matching).
 //
 // Design sources (prior art, re-derived for this GPU): the vLLM
 // "swapab_decode_attn" page (SwapABDecodeKernel: swap-AB tcgen05 tiles of 128
@@ -38,28 +46,27 @@
 
 namespace dsa {
 
-constexpr int kTcThreads = 256;
-constexpr long long kWaitIters = 4000000000ll;  // wait budget in SM cycles (~2 s)
-constexpr float kRescaleSlack = 8.0f;       // log2 headroom before the running max moves
+constexpr int kSmWarps = 8;                    // softmax / epilogue / MMA issue
+constexpr int kPrWarps = 8;                    // producers
+constexpr int kTcThreads = 32 * (kSmWarps + kPrWarps);
+constexpr long long kWaitBudget = 4000000000ll;  // SM cycles (~2 s) per wait
+constexpr float kRescaleSlack = 8.0f;            // log2 headroom of the running max
 
 template <int HPG>
 struct TcCfg {
-  static constexpr int kHalf = HPG / 2;                  // heads per thread
+  static constexpr int kHalf = HPG / 2;                  // heads per softmax thread
   static constexpr int kPRow = HPG * 2;                  // bytes per P row
-  static constexpr int kPBufs = HPG == 64 ? 2 : 4;       // P' buffers (fp8 tiles: one per M block)
-  static constexpr uint32_t kPBytes = 128 * kPRow;       // one P tile
+  static constexpr int kPBufs = HPG == 64 ? 2 : 4;       // P' buffers (fp8: one per M block)
+  static constexpr uint32_t kPBytes = 128 * kPRow;
   static constexpr uint32_t kKV = 0;                     // 128 x 512 f16 = 128 KiB
   static constexpr uint32_t kQ = 131072;                 // HPG x 512 f16
   static constexpr uint32_t kP = kQ + HPG * 1024;        // kPBufs x [128 x HPG] f16
-  static constexpr uint32_t kHeadF = kP + kPBufs * kPBytes;  // [64] f32 per-head score factor
+  static constexpr uint32_t kRho = kP + kPBufs * kPBytes;  // [128][4] f16: rho - 1 (-2: row not kept)
+  static constexpr uint32_t kHeadF = kRho + 1024;        // [64] f32 per-head score factor
   static constexpr uint32_t kM = kHeadF + 256;           // [64] running max (log2)
-  static constexpr uint32_t kAlpha = kM + 256;           // [64]
-  static constexpr uint32_t kInv = kAlpha + 256;         // [64]
-  static constexpr uint32_t kRed = kInv + 256;           // [4][64] f32
-  static constexpr uint32_t kMisc = kRed + 1024;         // flags, mbarriers, tmem base
-  static constexpr uint32_t kBytes = kMisc + 64;
-  // Dynamic shared memory requested: the tiles plus slack for aligning the
-  // base to 1024 bytes, capped at the 227 KiB a CTA may use.
+  static constexpr uint32_t kRed = kM + 256;             // [4][64] f32
+  static constexpr uint32_t kMisc = kRed + 1024;         // mbarriers, counters, tmem base
+  static constexpr uint32_t kBytes = kMisc + 256;   // bars 120 B, abort, tmem, counters
   static constexpr uint32_t kSmem = kBytes + 1024 > 232448u ? 232448u : kBytes + 1024;
   static constexpr uint32_t kCols = HPG == 16 ? 128 : (HPG == 32 ? 256 : 512);
   static constexpr uint32_t kColS = 0;                   // S block b at b*HPG
@@ -70,14 +77,27 @@ struct TcCfg {
   static_assert(kBytes <= 232448u, "shared memory layout exceeds 227 KiB");
 };
 
-// Byte offset of the 16-byte chunk holding f16 elements [8*ci, 8*ci+8) of
-// row r in a K-major 128B-swizzled tile whose k-blocks are `kb_bytes` apart.
+// mbarrier slots in the misc area
+enum Bar : int {
+  kBarKvFull = 0,   // [4] producers -> softmax: 128-dim block of the tile written
+  kBarKvFree = 4,   // [4] MMA commit -> producers: block no longer read
+  kBarSFull = 8,    // MMA commit -> softmax: S ready (and every earlier MMA done)
+  kBarPFree = 9,    // MMA commit -> softmax: first P' batch consumed
+  kBarOFinal = 10,  // MMA commit -> softmax: last PV of a token done
+  kNumBars = 11
+};
+constexpr uint32_t kMiscAbort = 8 * kNumBars;        // int32
+constexpr uint32_t kMiscTmem = kMiscAbort + 4;       // uint32
+constexpr uint32_t kMiscCnt = kMiscAbort + 8;        // [4][2] uint32: kept rows / checksum
+// Kept-row records ride in 4 slots indexed by the ordinal of the token among
+// the tokens with work: producers can be at most two such tokens ahead of the
+// softmax warps that read (and clear) a slot.
+
 __device__ __forceinline__ uint32_t sw128_off(int r, int kb, int ci, uint32_t kb_bytes) {
   return (uint32_t)kb * kb_bytes + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u +
          (uint32_t)((ci ^ (r & 7)) << 4);
 }
 
-// P tile (MN-major: row r holds HPG f16 heads), swizzle matching its row width.
 template <int HPG>
 __device__ __forceinline__ uint32_t p_off(int r, int ci) {
   if constexpr (HPG == 64)
@@ -90,40 +110,61 @@ __device__ __forceinline__ uint32_t p_off(int r, int ci) {
            (uint32_t)((ci ^ ((r & 7) >> 2)) << 4);
 }
 
-// Per-thread prefetch registers for one tile. Thread (warp w, lane l) owns
-// row 32*(w%4) + l -- the TMEM lane its softmax reads -- and half j = w/4 of
-// the record's 16-byte chunks: c = 4m + 2j + e (e in {0,1}), i.e. whole
-// 32-byte sectors.
-struct Gather {
-  uint4 d[16];   // fp8: 16 chunks; NVFP4: 8 chunks
-  uint4 s[2];    // fp8: s[0] = 4 fp32 scales; NVFP4: 32 e4m3 scales
-  int32_t sid;
-  int32_t r;
-  bool ok;
-};
-
 __device__ __forceinline__ void unit_info(const Params &p, int64_t u, int32_t &t, int32_t &lid,
                                           int32_t &row0) {
   t = (int32_t)(u / p.tpt);
   unit_tile(p, u, lid, row0);
 }
 
-__device__ __forceinline__ void prefetch(const Params &p, int64_t u, Gather &g) {
+// A tile is worked on iff its first row lies below min(len, width).
+__device__ __forceinline__ bool unit_live(const Params &p, int64_t u) {
+  int32_t t, lid, row0;
+  unit_info(p, u, t, lid, row0);
+  return row0 < list_limit(p.list[lid], t);
+}
+
+__device__ __forceinline__ int64_t next_live(const Params &p, int64_t u, int64_t u1) {
+  while (u < u1 && !unit_live(p, u)) ++u;
+  return u;
+}
+
+// fp32 block scale -> (f16 s_hi with 7 significant bits, rho = s / s_hi).
+__device__ __forceinline__ void split_scale(float s, uint32_t &shi2, float &rho) {
+  uint32_t u = __float_as_uint(s);
+  u = (u + 0x10000u) & 0xFFFE0000u;
+  const __half h = __float2half_rn(__uint_as_float(u));
+  const float hf = __half2float(h);
+  rho = (hf != 0.f) ? s / hf : 0.f;
+  const uint32_t hb = (uint32_t)__half_as_ushort(h);
+  shi2 = hb | (hb << 16);
+}
+
+// ---------------------------------------------------------------- producer
+// Thread (producer warp pw, lane l): row 32*(pw%4) + l, half j = pw/4 of the
+// record's 16-byte chunks: c = 4m + 2j + e (e in {0,1}) -- whole sectors.
+struct Gather {
+  uint4 d[16];   // fp8: 16 chunks; NVFP4: 8 chunks
+  uint4 s[2];    // fp8: 4 fp32 scales; NVFP4: 32 e4m3 scales
+  int32_t sid;
+  int32_t r;
+  bool ok;
+};
+
+__device__ __forceinline__ void issue_loads(const Params &p, int64_t u, int32_t sid, int row,
+                                            int j, Gather &g) {
   int32_t t, lid, row0;
   unit_info(p, u, t, lid, row0);
   const ListArgs &L = p.list[lid];
-  const int row = 32 * ((threadIdx.x >> 5) & 3) + (threadIdx.x & 31), j = threadIdx.x >> 7;
   g.r = row0 + row;
-  g.sid = -1;
-  if (g.r < L.width) g.sid = __ldg(L.ids + (int64_t)t * L.idx_stride + g.r);
-  const int32_t limit = list_limit(L, t);
-  g.ok = slot_valid(L, g.r, limit, g.sid);
+  g.sid = sid;
+  g.ok = slot_valid(L, g.r, list_limit(L, t), sid);
   const uint4 z = make_uint4(0, 0, 0, 0);
   if (L.fmt == DSA_REC_FP8_528) {
     if (g.ok) {
-      const uint8_t *rec = record_ptr(L, g.sid);
+      const uint8_t *rec = record_ptr(L, sid);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) g.d[k] = tc::ldg_nc_v4(rec + 16 * (4 * (k >> 1) + 2 * j + (k & 1)));
+      for (int k = 0; k < 16; ++k)
+        g.d[k] = tc::ldg_nc_v4(rec + 16 * (4 * (k >> 1) + 2 * j + (k & 1)));
       g.s[0] = tc::ldg_nc_v4(rec + 512);
     } else {
 #pragma unroll
@@ -132,9 +173,10 @@ __device__ __forceinline__ void prefetch(const Params &p, int64_t u, Gather &g) 
     }
   } else {
     if (g.ok) {
-      const uint8_t *rec = record_ptr(L, g.sid);
+      const uint8_t *rec = record_ptr(L, sid);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) g.d[k] = tc::ldg_nc_v4(rec + 16 * (4 * (k >> 1) + 2 * j + (k & 1)));
+      for (int k = 0; k < 8; ++k)
+        g.d[k] = tc::ldg_nc_v4(rec + 16 * (4 * (k >> 1) + 2 * j + (k & 1)));
       g.s[0] = tc::ldg_nc_v4(rec + 256);
       g.s[1] = tc::ldg_nc_v4(rec + 272);
     } else {
@@ -146,63 +188,60 @@ __device__ __forceinline__ void prefetch(const Params &p, int64_t u, Gather &g) 
   }
 }
 
-// fp32 block scale -> (f16 s_hi with 7 significant bits, rho = s / s_hi).
-__device__ __forceinline__ void split_scale(float s, uint32_t &shi2, float &rho) {
-  uint32_t u = __float_as_uint(s);
-  u = (u + 0x10000u) & 0xFFFE0000u;        // round to 6 explicit mantissa bits
-  const __half h = __float2half_rn(__uint_as_float(u));
-  const float hf = __half2float(h);
-  rho = (hf != 0.f) ? s / hf : 0.f;
-  const uint32_t hb = (uint32_t)__half_as_ushort(h);
-  shi2 = hb | (hb << 16);
+__device__ __forceinline__ int32_t load_sid(const Params &p, int64_t u, int row) {
+  int32_t t, lid, row0;
+  unit_info(p, u, t, lid, row0);
+  const ListArgs &L = p.list[lid];
+  const int32_t r = row0 + row;
+  return r < L.width ? __ldg(L.ids + (int64_t)t * L.idx_stride + r) : -1;
 }
 
-// Registers -> f16 tile in shared memory. fp8 records also return the four
-// per-block factors rho = s / s_hi of this thread's row.
-__device__ __forceinline__ void dequant(const Params &p, int32_t lid, const Gather &g,
-                                        uint32_t kv_base, float (&rho)[4]) {
-  const ListArgs &L = p.list[lid];
-  const int row = 32 * ((threadIdx.x >> 5) & 3) + (threadIdx.x & 31), j = threadIdx.x >> 7;
-  if (L.fmt == DSA_REC_FP8_528) {
-    uint32_t shi2[4];
-    split_scale(__uint_as_float(g.s[0].x), shi2[0], rho[0]);
-    split_scale(__uint_as_float(g.s[0].y), shi2[1], rho[1]);
-    split_scale(__uint_as_float(g.s[0].z), shi2[2], rho[2]);
-    split_scale(__uint_as_float(g.s[0].w), shi2[3], rho[3]);
+// Dequantize the two 64-dim k-blocks of M block mb for this thread's row.
+__device__ __forceinline__ void dequant_block(bool fp8, const Gather &g, const uint32_t (&shi2)[4],
+                                              int mb, int row, int j, uint32_t kv_base) {
+  if (fp8) {
+    // chunks c = 4m + 2j + e of k-block m; M block mb = k-blocks {2mb, 2mb+1}
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int c = 4 * (k >> 1) + 2 * j + (k & 1);  // dims [16c, 16c+16), scale block c/8
-      const uint32_t sc = shi2[c >> 3];
-      const uint32_t w[4] = {g.d[k].x, g.d[k].y, g.d[k].z, g.d[k].w};
-      uint32_t f[8];
+    for (int mm = 0; mm < 2; ++mm) {
+      const int m = 2 * mb + mm;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        tc::e4m3x4_to_f16x4(w[i], f[2 * i], f[2 * i + 1]);
-        f[2 * i] = tc::hmul2(f[2 * i], sc);
-        f[2 * i + 1] = tc::hmul2(f[2 * i + 1], sc);
+      for (int e = 0; e < 2; ++e) {
+        const int k = 2 * m + e;
+        const int c = 4 * m + 2 * j + e;   // dims [16c, 16c+16), scale block mb
+        const uint32_t sc = shi2[mb];
+        const uint32_t w[4] = {g.d[k].x, g.d[k].y, g.d[k].z, g.d[k].w};
+        uint32_t f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          tc::e4m3x4_to_f16x4(w[i], f[2 * i], f[2 * i + 1]);
+          f[2 * i] = tc::hmul2(f[2 * i], sc);
+          f[2 * i + 1] = tc::hmul2(f[2 * i + 1], sc);
+        }
+        const int ci = (2 * c) & 7;
+        tc::st_shared_v4(kv_base + sw128_off(row, m, ci, 16384), f[0], f[1], f[2], f[3]);
+        tc::st_shared_v4(kv_base + sw128_off(row, m, ci + 1, 16384), f[4], f[5], f[6], f[7]);
       }
-      const int kb = c >> 2, ci = (2 * c) & 7;
-      tc::st_shared_v4(kv_base + sw128_off(row, kb, ci, 16384), f[0], f[1], f[2], f[3]);
-      tc::st_shared_v4(kv_base + sw128_off(row, kb, ci + 1, 16384), f[4], f[5], f[6], f[7]);
     }
   } else {
-    rho[0] = rho[1] = rho[2] = rho[3] = 1.f;
+    // chunk c = 4m + 2j + e holds dims [32c, 32c+32) of k-block 2m + j;
+    // M block mb is m = mb, e in {0, 1}
     const uint32_t sw[8] = {g.s[0].x, g.s[0].y, g.s[0].z, g.s[0].w,
                             g.s[1].x, g.s[1].y, g.s[1].z, g.s[1].w};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int c = 4 * (k >> 1) + 2 * j + (k & 1);  // dims [32c, 32c+32), scales 2c, 2c+1
+    for (int e = 0; e < 2; ++e) {
+      const int k = 2 * mb + e;
+      const int c = 4 * mb + 2 * j + e;
       const uint32_t pair = (sw[c >> 1] >> (16 * (c & 1))) & 0xFFFFu;
       const uint32_t s2 = tc::e4m3x2_to_f16x2(pair);
       const uint32_t sa = __byte_perm(s2, s2, 0x1010), sb = __byte_perm(s2, s2, 0x3232);
       const uint32_t w[4] = {g.d[k].x, g.d[k].y, g.d[k].z, g.d[k].w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {  // word i = dims [32c + 8i, 32c + 8i + 8)
+      for (int i = 0; i < 4; ++i) {  // word i = dims [32c + 8i, +8)
         uint32_t f[4];
         tc::e2m1x8_to_f16x8(w[i], f);
         const uint32_t sc = i < 2 ? sa : sb;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) f[e] = tc::hmul2(f[e], sc);
+        for (int q = 0; q < 4; ++q) f[q] = tc::hmul2(f[q], sc);
         const int kb = c >> 1, ci = (4 * c + i) & 7;
         tc::st_shared_v4(kv_base + sw128_off(row, kb, ci, 16384), f[0], f[1], f[2], f[3]);
       }
@@ -210,16 +249,34 @@ __device__ __forceinline__ void dequant(const Params &p, int32_t lid, const Gath
   }
 }
 
+// Named barrier 1 among the 256 softmax threads (optionally OR-reducing).
+__device__ __forceinline__ int sm_bar_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, 1, 256, p;\n\t"
+      "selp.b32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred)
+      : "memory");
+  return r;
+}
+__device__ __forceinline__ void sm_bar() { asm volatile("barrier.cta.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar))
+               : "memory");
+}
+
 template <int HPG>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   using Cfg = TcCfg<HPG>;
   constexpr int NH = Cfg::kHalf;
   extern __shared__ uint8_t smem_raw[];
-  // Swizzled tiles need a 1024-byte aligned base (the swizzle acts on
-  // address bits); the layout is checked to fit after aligning.
   const uint32_t raw_base = tc::smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
-  if (pad + Cfg::kBytes > Cfg::kSmem) {
+  if (pad + Cfg::kBytes > Cfg::kSmem) {   // swizzled tiles need a 1024-byte aligned base
     if (threadIdx.x == 0) report_status(p.status, DSA_ERR_UNSUPPORTED);
     return;
   }
@@ -228,22 +285,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   const uint32_t kv_base = sbase + Cfg::kKV;
   const uint32_t q_base = sbase + Cfg::kQ;
   const uint32_t p_base = sbase + Cfg::kP;
+  __half *rho_s = reinterpret_cast<__half *>(smem + Cfg::kRho);
   float *headf_s = reinterpret_cast<float *>(smem + Cfg::kHeadF);
   float *m_s = reinterpret_cast<float *>(smem + Cfg::kM);
-  float *alpha_s = reinterpret_cast<float *>(smem + Cfg::kAlpha);
-  float *inv_s = reinterpret_cast<float *>(smem + Cfg::kInv);
   float *red_s = reinterpret_cast<float *>(smem + Cfg::kRed);
-  int32_t *flag_s = reinterpret_cast<int32_t *>(smem + Cfg::kMisc);
-  int32_t *err_s = flag_s + 1;
-  uint32_t *red_u = reinterpret_cast<uint32_t *>(flag_s + 2);   // [2] selection reduction
-  uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + Cfg::kMisc + 16);
-  uint64_t *bar_o = bar_s + 1;
-  uint64_t *bar_p = bar_s + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kMisc + 48);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kMisc);
+  volatile int32_t *abort_s = reinterpret_cast<volatile int32_t *>(smem + Cfg::kMisc + kMiscAbort);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kMisc + kMiscTmem);
+  uint32_t *cnt_s = reinterpret_cast<uint32_t *>(smem + Cfg::kMisc + kMiscCnt);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q4 = warp & 3, half = warp >> 2;
-  const int prow = 32 * q4 + lane;   // TMEM lane = KV row handled in the softmax
   const int hg = blockIdx.x % p.HG;
   const int cta = blockIdx.x / p.HG;
   const int h0 = hg * HPG;
@@ -255,240 +306,309 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(bar_s, 1);
-    tc::mbar_init(bar_o, 1);
-    tc::mbar_init(bar_p, 1);
+    for (int b = 0; b < kNumBars; ++b)
+      tc::mbar_init(&bars[b], (b >= kBarKvFull && b < kBarKvFull + 4) ? kPrWarps : 1u);
     tc::fence_mbar_init();
-    *flag_s = 0;
-    *err_s = 0;
+    *abort_s = 0;
+    for (int i = 0; i < 8; ++i) cnt_s[i] = 0;
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tl_lane = tmem + ((uint32_t)(32 * q4) << 16);   // this warp's TMEM lanes
 
-  uint32_t ph_s = 0, ph_o = 0, ph_p = 0;
-  bool o_pending = false;
-  bool failed = false;
-  float m_reg[NH], l_reg[NH];
-  bool first_pv = true;
-  uint32_t kept = 0, chk = 0;
-  Segment seg;
-  seg.t = -1;
-
-  Gather g;
-  prefetch(p, u0, g);
-
-  // Wait for the last PV (O and the shared tiles are free afterwards).
-  auto wait_o = [&]() {
-    if (o_pending) {
-      if (!tc::mbar_wait(bar_o, ph_o, kWaitIters)) failed = true;
-      ph_o ^= 1;
-      o_pending = false;
-      tc::tc_fence_after();
+  // Bounded wait on a barrier phase. After any timeout (here or in another
+  // warp) it returns at once; callers keep their control flow unchanged.
+  auto wait = [&](int b, uint32_t &phase) {
+    if (!*abort_s) {
+      const bool done = tc::mbar_wait(&bars[b], phase, kWaitBudget);
+      if (!done && !*abort_s) {
+        *abort_s = 1;
+        report_status(p.status, DSA_ERR_TIMEOUT);
+      }
     }
+    phase ^= 1u;
   };
 
-  // Returns false (CTA-uniformly) when a bounded wait gave up.
-  auto finalize = [&]() -> bool {
-    wait_o();
-    // Row selection record.
-    uint32_t k2 = kept, c2 = chk;
+  if (warp >= kSmWarps) {
+    // ======================================================== producers
+    const int pw = warp - kSmWarps;
+    const int row = 32 * (pw & 3) + lane, j = pw >> 2;
+    uint32_t ph_free[4] = {0, 0, 0, 0};
+    bool first = true;
+    uint32_t kept = 0, chk = 0, pord = 0;
+    int64_t u = next_live(p, u0, u1);
+    Gather g;
+    if (u < u1) issue_loads(p, u, load_sid(p, u, row), row, j, g);
+    while (u < u1) {
+      int32_t t, lid, row0;
+      unit_info(p, u, t, lid, row0);
+      const int64_t un = next_live(p, u + 1, u1);
+      const int32_t sid_next = un < u1 ? load_sid(p, un, row) : -1;
+      const bool last_of_token = un >= u1 || (int32_t)(un / p.tpt) != t;
+      const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
+      uint32_t shi2[4] = {0, 0, 0, 0};
+      float rho[4] = {1.f, 1.f, 1.f, 1.f};
+      if (fp8) {
+        split_scale(__uint_as_float(g.s[0].x), shi2[0], rho[0]);
+        split_scale(__uint_as_float(g.s[0].y), shi2[1], rho[1]);
+        split_scale(__uint_as_float(g.s[0].z), shi2[2], rho[2]);
+        split_scale(__uint_as_float(g.s[0].w), shi2[3], rho[3]);
+      }
+      if (j == 0 && g.ok) {
+        kept += 1;
+        chk += row_hash(g.sid, g.r, lid);
+      }
+      if (last_of_token) {   // add this warp's kept-row record of token t to its slot
+        uint32_t k2 = kept, c2 = chk;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      k2 += __shfl_xor_sync(0xffffffffu, k2, off);
-      c2 += __shfl_xor_sync(0xffffffffu, c2, off);
-    }
-    // Per-head sums over rows: butterfly within the warp, then 4 quadrants.
-#pragma unroll
-    for (int j = 0; j < NH; ++j) {
-      float v = l_reg[j];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0) red_s[q4 * 64 + half * NH + j] = v;
-    }
-    if (tid == 0) {
-      red_u[0] = 0;
-      red_u[1] = 0;
-    }
-    if (__syncthreads_or(failed ? 1 : 0)) {
-      failed = true;
-      return false;
-    }
-    if (lane == 0) {
-      atomicAdd(&red_u[0], k2);
-      atomicAdd(&red_u[1], c2);
-    }
-    if (tid < HPG) {
-      const int h = tid;
-      const float l = red_s[h] + red_s[64 + h] + red_s[128 + h] + red_s[192 + h];
-      const float m = m_s[h];
-      const float lse = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
-      float inv = 0.f;
-      if (l > 0.f) {
-        float den = l;
-        if (seg.whole && p.sink) {
-          const float sk = __ldg(p.sink + h0 + h);
-          den = (sk == INFINITY) ? INFINITY : l + tc::ex2(sk * kLog2e - m);
+        for (int off = 16; off > 0; off >>= 1) {
+          k2 += __shfl_xor_sync(0xffffffffu, k2, off);
+          c2 += __shfl_xor_sync(0xffffffffu, c2, off);
         }
-        inv = 1.f / den;
+        if (lane == 0) {
+          atomicAdd(&cnt_s[(pord & 3) * 2], k2);
+          atomicAdd(&cnt_s[(pord & 3) * 2 + 1], c2);
+        }
+        kept = 0;
+        chk = 0;
+        ++pord;
       }
-      inv_s[h] = inv;
-      if (seg.whole)
-        p.lse[(int64_t)seg.t * p.H + h0 + h] = lse;
-      else
-        p.part_lse[((int64_t)hg * 2 * p.C + seg.slot) * HPG + h] = lse;
-    }
-    __syncthreads();
-    if (hg == 0 && tid == 0) {
-      int32_t *dst = seg.whole ? (p.sel + 2 * (int64_t)seg.t) : (p.part_sel + 2 * (int64_t)seg.slot);
-      dst[0] = (int32_t)red_u[0];
-      dst[1] = (int32_t)red_u[1];
-    }
-    // O^T[d, h] from TMEM: thread holds d = 128*mb + prow for its NH heads.
-#pragma unroll 1
-    for (int mb = 0; mb < 4; ++mb) {
-      float o[NH];
-      if (!first_pv) {
-        tc::tmem_ld<NH>(tl_lane + Cfg::kColO + mb * HPG + half * NH, o);
+      for (int mb = 0; mb < 4; ++mb) {
+        if (!first) wait(kBarKvFree + mb, ph_free[mb]);
+        if (mb == 0 && j == 0) {
+          // rho - 1 as f16 (|rho - 1| <= 2^-8); -2 marks a row that is not kept
+          const float v0 = g.ok ? rho[0] - 1.f : -2.f, v1 = g.ok ? rho[1] - 1.f : -2.f;
+          const float v2 = g.ok ? rho[2] - 1.f : -2.f, v3 = g.ok ? rho[3] - 1.f : -2.f;
+          __half2 a = __floats2half2_rn(v0, v1), b = __floats2half2_rn(v2, v3);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t *>(&a);
+          pk.y = *reinterpret_cast<uint32_t *>(&b);
+          reinterpret_cast<uint2 *>(rho_s)[row] = pk;
+        }
+        dequant_block(fp8, g, shi2, mb, row, j, kv_base);
+        tc::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarKvFull + mb]);
       }
-      const int d = 128 * mb + prow;
+      first = false;
+      u = un;
+      if (u < u1) issue_loads(p, u, sid_next, row, j, g);
+    }
+  } else {
+    // ======================================================== softmax / epilogue / MMA
+    const int q4 = warp & 3, half = warp >> 2;
+    const int prow = 32 * q4 + lane;
+    const uint32_t tl_lane = tmem + ((uint32_t)(32 * q4) << 16);
+    const bool issuer = tid == 0;   // issues every tcgen05.mma and commit
+    uint32_t ph_s = 0, ph_kv[4] = {0, 0, 0, 0}, ph_pf = 0, ph_of = 0, sord = 0;
+    float l_reg[NH];
+    int32_t cur_t = -1;
+    bool seg_worked = false, first_pv = true;
+
+    auto stage_q = [&](int32_t t) {
+      int64_t pos = p.positions ? __ldg(p.positions + t) : 0;
+      if (pos < 0 || (p.cos_sin && pos >= p.cs_rows)) {   // outside the table: flag, row 0
+        if (tid == 0) report_status(p.status, DSA_ERR_INVALID_ARG);
+        pos = 0;
+      }
+      for (int h = warp; h < HPG; h += kSmWarps) {
+        const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)(h0 + h) * p.q_sh;
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane);
+        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane + 1);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+          v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+        }
+        if (p.cos_sin) {   // NeoX: dim 448+i pairs with 480+i; lanes 28..31 hold 448..511
+          const float *cs = p.cos_sin + pos * 64;
+          const bool rope = lane >= 28;
+          const bool firsth = lane < 30;
+          const int i0 = (lane & 1) * 16;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[k], 2);
+            if (rope) {
+              const float c = __ldg(cs + i0 + k), s = __ldg(cs + kRopeHalf + i0 + k);
+              v[k] = firsth ? (v[k] * c - other * s) : (v[k] * c + other * s);
+            }
+          }
+        }
+        float mx = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(v[k]));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        // Per-head power-of-two prescale: f16 Q with max |q| in [1, 2).
+        int e = (mx > 0.f) ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+        e = e < -126 ? -126 : (e > 126 ? 126 : e);
+        const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+        const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+        if (lane == 0) headf_s[h] = p.scale_log2 * up;
+        uint32_t f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = tc::pack_f16x2(v[2 * i] * down, v[2 * i + 1] * down);
+        const int kb = lane >> 2, ci = (lane & 3) * 2;
+        tc::st_shared_v4(q_base + sw128_off(h, kb, ci, HPG * 128), f[0], f[1], f[2], f[3]);
+        tc::st_shared_v4(q_base + sw128_off(h, kb, ci + 1, HPG * 128), f[4], f[5], f[6], f[7]);
+      }
+      if (tid < HPG) m_s[tid] = -INFINITY;
+      tc::fence_async_smem();
+      sm_bar();   // Q (async proxy), headf_s and m_s visible to the group
+    };
+
+    // Token finished: sums over rows, sink, out / lse (or partial), selection.
+    auto finalize = [&](const Segment &seg) {
+      if (seg_worked) wait(kBarOFinal, ph_of);
+      tc::tc_fence_after();
 #pragma unroll
       for (int j = 0; j < NH; ++j) {
-        const int h = half * NH + j;
-        const float inv = inv_s[h];
-        const float v = (first_pv || inv == 0.f) ? 0.f : o[j] * inv;
+        float v = seg_worked ? l_reg[j] : 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) red_s[q4 * 64 + half * NH + j] = v;
+      }
+      sm_bar();
+      if (tid < HPG) {   // 1 / denominator of head tid, lse
+        const int h = tid;
+        const float l = red_s[h] + red_s[64 + h] + red_s[128 + h] + red_s[192 + h];
+        const float m = seg_worked ? m_s[h] : -INFINITY;
+        float iv = 0.f;
+        if (l > 0.f) {
+          float den = l;
+          if (seg.whole && p.sink) {
+            const float sk = __ldg(p.sink + h0 + h);
+            den = (sk == INFINITY) ? INFINITY : l + tc::ex2(sk * kLog2e - m);
+          }
+          iv = 1.f / den;
+        }
+        const float lse = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
         if (seg.whole)
-          p.out[((int64_t)seg.t * p.H + h0 + h) * kD + d] = __float2bfloat16_rn(v);
+          p.lse[(int64_t)seg.t * p.H + h0 + h] = lse;
         else
-          p.part_o[(((int64_t)hg * 2 * p.C + seg.slot) * HPG + h) * kD + d] = v;
+          p.part_lse[((int64_t)hg * 2 * p.C + seg.slot) * HPG + h] = lse;
+        red_s[256 - 64 + h] = iv;   // read below; sums of row 3 were consumed above
       }
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    return true;
-  };
-
-  auto stage_q = [&](int32_t t) {
-    int64_t pos = p.positions ? __ldg(p.positions + t) : 0;
-    if (pos < 0 || (p.cos_sin && pos >= p.cs_rows)) {   // outside the table: flag, use row 0
-      if (tid == 0) report_status(p.status, DSA_ERR_INVALID_ARG);
-      pos = 0;
-    }
-    for (int h = warp; h < HPG; h += kTcThreads / 32) {
-      const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)(h0 + h) * p.q_sh;
-      const uint4 a = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane);
-      const uint4 b = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane + 1);
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      float v[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-        v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+      if (tid == 0) {   // kept rows / checksum of the token, then clear the slot
+        uint32_t k2 = 0, c2 = 0;
+        if (seg_worked) {
+          k2 = cnt_s[(sord & 3) * 2];
+          c2 = cnt_s[(sord & 3) * 2 + 1];
+          cnt_s[(sord & 3) * 2] = 0;
+          cnt_s[(sord & 3) * 2 + 1] = 0;
+        }
+        if (hg == 0) {
+          int32_t *dst =
+              seg.whole ? (p.sel + 2 * (int64_t)seg.t) : (p.part_sel + 2 * (int64_t)seg.slot);
+          dst[0] = (int32_t)k2;
+          dst[1] = (int32_t)c2;
+        }
       }
-      if (p.cos_sin) {   // NeoX: dim 448+i pairs with 480+i; lanes 28..31 hold 448..511
-        const float *cs = p.cos_sin + pos * 64;
-        const bool rope = lane >= 28;
-        const bool first = lane < 30;
-        const int i0 = (lane & 1) * 16;
+      if (seg_worked) ++sord;
+      sm_bar();
+#pragma unroll 1
+      for (int mb = 0; mb < 4; ++mb) {
+        const int d = 128 * mb + prow;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float other = __shfl_xor_sync(0xffffffffu, v[k], 2);
-          if (rope) {
-            const float c = __ldg(cs + i0 + k), s = __ldg(cs + kRopeHalf + i0 + k);
-            v[k] = first ? (v[k] * c - other * s) : (v[k] * c + other * s);
+        for (int g8 = 0; g8 < NH / 8; ++g8) {
+          float o[8];
+          if (seg_worked) tc::tmem_ld<8>(tl_lane + Cfg::kColO + mb * HPG + half * NH + 8 * g8, o);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int h = half * NH + 8 * g8 + i;
+            const float iv = red_s[256 - 64 + h];
+            const float v = (!seg_worked || iv == 0.f) ? 0.f : o[i] * iv;
+            if (seg.whole)
+              p.out[((int64_t)seg.t * p.H + h0 + h) * kD + d] = __float2bfloat16_rn(v);
+            else
+              p.part_o[(((int64_t)hg * 2 * p.C + seg.slot) * HPG + h) * kD + d] = v;
           }
         }
       }
-      float mx = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(v[k]));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      int e = (mx > 0.f) ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
-      e = e < -126 ? -126 : (e > 126 ? 126 : e);
-      const float down = __uint_as_float((uint32_t)(127 - e) << 23);
-      const float up = __uint_as_float((uint32_t)(127 + e) << 23);
-      if (lane == 0) headf_s[h] = p.scale_log2 * up;
-      uint32_t f[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) f[i] = tc::pack_f16x2(v[2 * i] * down, v[2 * i + 1] * down);
-      const int kb = lane >> 2, ci = (lane & 3) * 2;
-      tc::st_shared_v4(q_base + sw128_off(h, kb, ci, HPG * 128), f[0], f[1], f[2], f[3]);
-      tc::st_shared_v4(q_base + sw128_off(h, kb, ci + 1, HPG * 128), f[4], f[5], f[6], f[7]);
-    }
-    if (tid < HPG) m_s[tid] = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < NH; ++j) {
-      m_reg[j] = -INFINITY;
-      l_reg[j] = 0.f;
-    }
-    first_pv = true;
-    kept = 0;
-    chk = 0;
-  };
+      tc::tc_fence_before();
+      sm_bar();   // O read out (next PV may overwrite it); red_s free again
+    };
 
-  for (int64_t u = u0; u < u1 && !failed; ++u) {
-    int32_t t, lid, row0;
-    unit_info(p, u, t, lid, row0);
-    if (t != seg.t) {
-      if (seg.t >= 0 && !finalize()) break;
-      seg = make_segment(p, cta, t);
-      stage_q(t);
-    }
-    wait_o();
-    const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
-    float rho[4];
-    dequant(p, lid, g, kv_base, rho);
-    const bool row_ok = g.ok;
-    if (half == 0 && g.ok) {
-      kept += 1;
-      chk += row_hash(g.sid, g.r, lid);
-    }
-    tc::fence_async_smem();
-    tc::tc_fence_before();
-    const int st = __syncthreads_or((row_ok ? 1 : 0) | (failed ? 2 : 0));
-    tc::tc_fence_after();
-    if (st & 2) {
-      failed = true;
-      break;
-    }
-    if (u + 1 < u1) prefetch(p, u + 1, g);
-    if (!(st & 1)) continue;
-
-    // ---- S = K . Q^T
-    if (tid == 0) {
-#pragma unroll 1
-      for (int kb = 0; kb < 8; ++kb) {
-        const uint32_t d_tmem = tmem + Cfg::kColS + (fp8 ? (uint32_t)(kb >> 1) * HPG : 0u);
+    Segment seg;
+    seg.t = -1;
+    for (int64_t u = u0; u < u1; ++u) {
+      int32_t t, lid, row0;
+      unit_info(p, u, t, lid, row0);
+      if (t != cur_t) {
+        if (cur_t >= 0) finalize(seg);
+        cur_t = t;
+        seg = make_segment(p, cta, t);
+        seg_worked = false;
+        first_pv = true;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = tc::sdesc(kv_base + kb * 16384 + ks * 32, 16, 1024, tc::kSwz128);
-          const uint64_t bd = tc::sdesc(q_base + kb * HPG * 128 + ks * 32, 16, 1024, tc::kSwz128);
-          const uint32_t acc = fp8 ? ((kb & 1) | ks) : (kb | ks);
-          tc::mma_f16(d_tmem, ad, bd, Cfg::kIdQK, acc);
-        }
+        for (int j = 0; j < NH; ++j) l_reg[j] = 0.f;
+        // Q is staged only for tokens with a live tile in this range.
+        bool any = false;
+        for (int64_t v = seg.u_begin; v < seg.u_end && !any; ++v) any = unit_live(p, v);
+        if (any) stage_q(t);
       }
-      tc::mma_commit(bar_s);
-    }
-    const bool s_late = !tc::mbar_wait(bar_s, ph_s, kWaitIters);
-    ph_s ^= 1;
-    tc::tc_fence_after();
-
-    // ---- softmax on this thread's row and NH heads
-    float x[NH];
-    {
-      const bool rv = row_ok;
+      if (!unit_live(p, u)) continue;
+      seg_worked = true;
+      const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
+      // ---- S = K . Q^T, one 128-dim block at a time as the producers land it
+      if (warp == 0) {
+        for (int mb = 0; mb < 4; ++mb) {
+          wait(kBarKvFull + mb, ph_kv[mb]);
+          tc::tc_fence_after();
+          if (issuer && !*abort_s) {
+            const uint32_t d_tmem = tmem + Cfg::kColS + (fp8 ? (uint32_t)mb * HPG : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              const int kb = 2 * mb + kk;
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t ad =
+                    tc::sdesc(kv_base + kb * 16384 + ks * 32, 16, 1024, tc::kSwz128);
+                const uint64_t bd =
+                    tc::sdesc(q_base + kb * HPG * 128 + ks * 32, 16, 1024, tc::kSwz128);
+                tc::mma_f16(d_tmem, ad, bd, Cfg::kIdQK, fp8 ? (kk | ks) : (kb | ks));
+              }
+            }
+          }
+          __syncwarp();
+        }
+        if (issuer && !*abort_s) tc::mma_commit(&bars[kBarSFull]);
+        __syncwarp();
+      } else {
+        // rho / row validity are written with block 0 of the tile
+        wait(kBarKvFull, ph_kv[0]);
+      }
+      float rho[4];
+      {
+        const uint2 pk = reinterpret_cast<const uint2 *>(rho_s)[prow];
+        const __half2 a = *reinterpret_cast<const __half2 *>(&pk.x);
+        const __half2 b = *reinterpret_cast<const __half2 *>(&pk.y);
+        rho[0] = __low2float(a) + 1.f;
+        rho[1] = __high2float(a) + 1.f;
+        rho[2] = __low2float(b) + 1.f;
+        rho[3] = __high2float(b) + 1.f;
+      }
+      const bool rv = rho[0] >= 0.f;   // -2 + 1 marks a row that is not kept
+      wait(kBarSFull, ph_s);
+      tc::tc_fence_after();
+      float x[NH];
       if (fp8) {
 #pragma unroll
-        for (int j = 0; j < NH; ++j) x[j] = 0.f;
+        for (int g8 = 0; g8 < NH / 8; ++g8) {
+          float sv[8];
+          tc::tmem_ld<8>(tl_lane + Cfg::kColS + half * NH + 8 * g8, sv);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          float sv[NH];
-          tc::tmem_ld<NH>(tl_lane + Cfg::kColS + b * HPG + half * NH, sv);
+          for (int i = 0; i < 8; ++i) x[8 * g8 + i] = rho[0] * sv[i];
 #pragma unroll
-          for (int j = 0; j < NH; ++j) x[j] = fmaf(rho[b], sv[j], x[j]);
+          for (int b = 1; b < 4; ++b) {
+            tc::tmem_ld<8>(tl_lane + Cfg::kColS + b * HPG + half * NH + 8 * g8, sv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[8 * g8 + i] = fmaf(rho[b], sv[i], x[8 * g8 + i]);
+          }
         }
       } else {
         tc::tmem_ld<NH>(tl_lane + Cfg::kColS + half * NH, x);
@@ -496,119 +616,102 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       bool need = false;
 #pragma unroll
       for (int j = 0; j < NH; ++j) {
-        x[j] = rv ? x[j] * headf_s[half * NH + j] : -INFINITY;
-        need |= x[j] > m_reg[j] + kRescaleSlack;
+        const int h = half * NH + j;
+        x[j] = rv ? x[j] * headf_s[h] : -INFINITY;
+        need |= x[j] > m_s[h] + kRescaleSlack;
       }
-      if (__any_sync(0xffffffffu, need) && lane == 0) *flag_s = 1;
-    }
-    if (__syncthreads_or(s_late ? 1 : 0)) {
-      failed = true;
-      break;
-    }
-    if (*flag_s) {
-      // Raise the running max to the tile max; rescale partial sums and O.
+      if (sm_bar_or(need ? 1 : 0)) {
+        // Raise the running max to the tile max; rescale sums and O.
 #pragma unroll
-      for (int j = 0; j < NH; ++j) {
-        float v = x[j];
+        for (int j = 0; j < NH; ++j) {
+          float v = x[j];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0) red_s[q4 * 64 + half * NH + j] = v;
-      }
-      __syncthreads();
-      if (tid < HPG) {
-        const float tm = fmaxf(fmaxf(red_s[tid], red_s[64 + tid]), fmaxf(red_s[128 + tid], red_s[192 + tid]));
-        const float mo = m_s[tid];
-        const float mn = fmaxf(mo, tm);
-        alpha_s[tid] = (mn == -INFINITY) ? 1.f : (mo == -INFINITY ? 0.f : tc::ex2(mo - mn));
-        m_s[tid] = mn;
-      }
-      __syncthreads();
-      float al[NH];
-#pragma unroll
-      for (int j = 0; j < NH; ++j) {
-        al[j] = alpha_s[half * NH + j];
-        m_reg[j] = m_s[half * NH + j];
-        l_reg[j] *= al[j];
-      }
-      if (!first_pv) {
-#pragma unroll 1
-        for (int mb = 0; mb < 4; ++mb) {
-          float o[NH];
-          const uint32_t ta = tl_lane + Cfg::kColO + mb * HPG + half * NH;
-          tc::tmem_ld<NH>(ta, o);
-#pragma unroll
-          for (int j = 0; j < NH; ++j) o[j] *= al[j];
-          tc::tmem_st<NH>(ta, o);
+          for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+          if (lane == 0) red_s[q4 * 64 + half * NH + j] = v;
         }
-      }
-    }
-    // P = 2^(x - m) (<= 2^8); f16, MN-major [128 rows, HPG].
-#pragma unroll
-    for (int j = 0; j < NH; ++j) {
-      x[j] = (x[j] == -INFINITY) ? 0.f : tc::ex2(x[j] - m_reg[j]);
-      l_reg[j] += x[j];
-    }
-    // NVFP4 tiles: one P for all four M blocks. fp8 tiles: P'_mb = P * rho_mb
-    // for M block mb, written kPBufs at a time.
-    const int nbatch = fp8 ? 4 / Cfg::kPBufs : 1;
-    bool late = false;
-    for (int batch = 0; batch < nbatch; ++batch) {
-      if (batch > 0) {   // the previous batch's MMAs must be done reading P'
-        late |= !tc::mbar_wait(bar_p, ph_p, kWaitIters);
-        ph_p ^= 1;
-        tc::tc_fence_after();
-      }
-      const int nb = fp8 ? Cfg::kPBufs : 1;
-      for (int i = 0; i < nb; ++i) {
-        const float f = fp8 ? rho[batch * nb + i] : 1.f;
-        uint32_t pw[NH / 2];
-#pragma unroll
-        for (int j = 0; j < NH; j += 2) pw[j / 2] = tc::pack_f16x2(x[j] * f, x[j + 1] * f);
-#pragma unroll
-        for (int k = 0; k < NH / 8; ++k) {
-          const int ci = half * (NH / 8) + k;
-          tc::st_shared_v4(p_base + i * Cfg::kPBytes + p_off<HPG>(prow, ci), pw[4 * k],
-                           pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
+        sm_bar();
+        if (tid < HPG) {   // new max and rescale factor of head tid (factor -> red_s[tid])
+          const float tm = fmaxf(fmaxf(red_s[tid], red_s[64 + tid]), fmaxf(red_s[128 + tid], red_s[192 + tid]));
+          const float mo = m_s[tid];
+          const float mn = fmaxf(mo, tm);
+          red_s[tid] = (mn == -INFINITY) ? 1.f : (mo == -INFINITY ? 0.f : tc::ex2(mo - mn));
+          m_s[tid] = mn;
         }
-      }
-      tc::fence_async_smem();
-      tc::tc_fence_before();
-      if (__syncthreads_or(late ? 1 : 0)) {
-        failed = true;
-        break;
-      }
-      // ---- O^T += K^T . P
-      if (tid == 0) {
-        *flag_s = 0;
-        tc::tc_fence_after();
-        const int mb0 = fp8 ? batch * Cfg::kPBufs : 0;
-        const int mb1 = fp8 ? mb0 + Cfg::kPBufs : 4;
-#pragma unroll 1
-        for (int mb = mb0; mb < mb1; ++mb) {
-          const uint32_t pb = p_base + (fp8 ? (uint32_t)(mb - mb0) * Cfg::kPBytes : 0u);
+        sm_bar();
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t ad =
-                tc::sdesc(kv_base + 2 * mb * 16384 + ks * 2048, 16384, 1024, tc::kSwz128);
-            const uint64_t bd = tc::sdesc(pb + ks * 16 * Cfg::kPRow, Cfg::kPBytes,
-                                          8 * Cfg::kPRow, Cfg::kPSwz);
-            tc::mma_f16(tmem + Cfg::kColO + mb * HPG, ad, bd, Cfg::kIdPV,
-                        (first_pv && ks == 0) ? 0u : 1u);
+        for (int j = 0; j < NH; ++j) l_reg[j] *= red_s[half * NH + j];
+        if (!first_pv) {
+#pragma unroll 1
+          for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+            for (int g8 = 0; g8 < NH / 8; ++g8) {
+              float o[8];
+              const uint32_t ta = tl_lane + Cfg::kColO + mb * HPG + half * NH + 8 * g8;
+              tc::tmem_ld<8>(ta, o);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o[i] *= red_s[half * NH + 8 * g8 + i];
+              tc::tmem_st<8>(ta, o);
+            }
           }
         }
-        tc::mma_commit(batch + 1 < nbatch ? bar_p : bar_o);
+        sm_bar();   // red_s free again before the next use
       }
+      // P = 2^(x - m) (<= 2^8) as f16, MN-major [128 rows, HPG]
+#pragma unroll
+      for (int j = 0; j < NH; ++j) {
+        const float mh = m_s[half * NH + j];
+        x[j] = (x[j] == -INFINITY) ? 0.f : tc::ex2(x[j] - mh);
+        l_reg[j] += x[j];
+      }
+      const int nbatch = fp8 ? 4 / Cfg::kPBufs : 1;
+      for (int batch = 0; batch < nbatch; ++batch) {
+        if (batch > 0) wait(kBarPFree, ph_pf);
+        const int nb = fp8 ? Cfg::kPBufs : 1;
+        for (int i = 0; i < nb; ++i) {
+          const float f = fp8 ? rho[batch * nb + i] : 1.f;
+#pragma unroll
+          for (int k = 0; k < NH / 8; ++k) {
+            uint32_t pw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              pw[e] = tc::pack_f16x2(x[8 * k + 2 * e] * f, x[8 * k + 2 * e + 1] * f);
+            const int ci = half * (NH / 8) + k;
+            tc::st_shared_v4(p_base + i * Cfg::kPBytes + p_off<HPG>(prow, ci), pw[0], pw[1],
+                             pw[2], pw[3]);
+          }
+        }
+        tc::fence_async_smem();
+        tc::tc_fence_before();
+        sm_bar();   // P' of this batch written by the whole group
+        // ---- O^T += K^T . P
+        if (issuer && !*abort_s) {
+          tc::tc_fence_after();
+          const int mb0 = fp8 ? batch * Cfg::kPBufs : 0;
+          const int mb1 = fp8 ? mb0 + Cfg::kPBufs : 4;
+          for (int mb = mb0; mb < mb1; ++mb) {
+            const uint32_t pb = p_base + (fp8 ? (uint32_t)(mb - mb0) * Cfg::kPBytes : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t ad =
+                  tc::sdesc(kv_base + 2 * mb * 16384 + ks * 2048, 16384, 1024, tc::kSwz128);
+              const uint64_t bd = tc::sdesc(pb + ks * 16 * Cfg::kPRow, Cfg::kPBytes,
+                                            8 * Cfg::kPRow, Cfg::kPSwz);
+              tc::mma_f16(tmem + Cfg::kColO + mb * HPG, ad, bd, Cfg::kIdPV,
+                          (first_pv && ks == 0) ? 0u : 1u);
+            }
+            tc::mma_commit(&bars[kBarKvFree + mb]);
+          }
+          if (batch + 1 < nbatch) tc::mma_commit(&bars[kBarPFree]);
+          else if (u + 1 >= seg.u_end || next_live(p, u + 1, seg.u_end) >= seg.u_end)
+            tc::mma_commit(&bars[kBarOFinal]);   // last PV of this token
+        }
+        __syncwarp();
+      }
+      first_pv = false;
     }
-    if (failed) break;
-    o_pending = true;
-    first_pv = false;
+    if (cur_t >= 0) finalize(seg);
   }
-  if (!failed && seg.t >= 0) finalize();
-  if (failed) {
-    report_status(p.status, DSA_ERR_TIMEOUT);
-    // Give outstanding tensor-core work a bounded chance to drain.
-    if (o_pending) tc::mbar_wait(bar_o, ph_o, kWaitIters);
-  }
+
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
