@@ -35,6 +35,8 @@ struct ListArgs {
   int32_t rec;           // record bytes
   int32_t width;
   int32_t tiles;         // ceil(width / kTile)
+  int32_t aligned32;     // every record starts on a 32-byte boundary
+  int32_t pad_;
 };
 
 struct Params {

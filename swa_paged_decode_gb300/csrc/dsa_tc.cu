@@ -172,7 +172,12 @@ __device__ __forceinline__ void issue_loads(const Params &p, int64_t u, int32_t 
       g.s[0] = z;
     }
   } else {
-    if (g.ok) {
+    if (g.ok && L.aligned32) {   // whole 32-byte sectors per request
+      const uint8_t *rec = record_ptr(L, sid);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) tc::ldg_nc_v8(rec + 64 * m + 32 * j, g.d[2 * m], g.d[2 * m + 1]);
+      tc::ldg_nc_v8(rec + 256, g.s[0], g.s[1]);
+    } else if (g.ok) {
       const uint8_t *rec = record_ptr(L, sid);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -337,14 +342,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     uint32_t ph_free[4] = {0, 0, 0, 0};
     bool first = true;
     uint32_t kept = 0, chk = 0, pord = 0;
+    // Tile records are prefetched into L2 (bulk, one thread per row) two
+    // tiles ahead and loaded into registers one tile ahead.
+    auto prefetch = [&](int64_t uu, int32_t sid) {
+      if (j != 0 || uu >= u1) return;
+      int32_t t2, lid2, row02;
+      unit_info(p, uu, t2, lid2, row02);
+      const ListArgs &L = p.list[lid2];
+      if (slot_valid(L, row02 + row, list_limit(L, t2), sid))
+        tc::prefetch_l2_bulk(record_ptr(L, sid), (uint32_t)L.rec);
+    };
     int64_t u = next_live(p, u0, u1);
+    int64_t un = u < u1 ? next_live(p, u + 1, u1) : u1;
+    int32_t sid_n1 = un < u1 ? load_sid(p, un, row) : -1;   // sid of the next tile
     Gather g;
-    if (u < u1) issue_loads(p, u, load_sid(p, u, row), row, j, g);
+    if (u < u1) {
+      const int32_t sid0 = load_sid(p, u, row);
+      prefetch(u, sid0);
+      prefetch(un, sid_n1);
+      issue_loads(p, u, sid0, row, j, g);
+    }
     while (u < u1) {
       int32_t t, lid, row0;
       unit_info(p, u, t, lid, row0);
-      const int64_t un = next_live(p, u + 1, u1);
-      const int32_t sid_next = un < u1 ? load_sid(p, un, row) : -1;
+      const int64_t un2 = un < u1 ? next_live(p, un + 1, u1) : u1;
+      const int32_t sid_n2 = un2 < u1 ? load_sid(p, un2, row) : -1;
+      const int32_t sid_next = sid_n1;
       const bool last_of_token = un >= u1 || (int32_t)(un / p.tpt) != t;
       const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
       uint32_t shi2[4] = {0, 0, 0, 0};
@@ -392,7 +415,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         if (lane == 0) mbar_arrive(&bars[kBarKvFull + mb]);
       }
       first = false;
+      prefetch(un2, sid_n2);
       u = un;
+      un = un2;
+      sid_n1 = sid_n2;
       if (u < u1) issue_loads(p, u, sid_next, row, j, g);
     }
   } else {
