@@ -49,6 +49,13 @@ namespace dsa {
 constexpr int kSmWarps = 8;                    // softmax / epilogue / MMA issue
 constexpr int kPrWarps = 8;                    // producers
 constexpr int kTcThreads = 32 * (kSmWarps + kPrWarps);
+// Register split (per thread): the kernel is launched with 128, softmax
+// warpgroups raise theirs to 144 and producer warpgroups drop to 112, which
+// sums to exactly the launch allocation (2*128*144 + 2*128*112 = 512*128).
+constexpr int kLaunchRegs = 128;
+constexpr int kSmRegs = 144;
+constexpr int kPrRegs = 112;
+static_assert(kSmRegs + kPrRegs == 2 * kLaunchRegs, "register split must match the launch");
 constexpr long long kWaitBudget = 4000000000ll;  // SM cycles (~2 s) per wait
 constexpr float kRescaleSlack = 8.0f;            // log2 headroom of the running max
 
@@ -337,6 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 
   if (warp >= kSmWarps) {
     // ======================================================== producers
+    tc::setmaxnreg_dec<kPrRegs>();
     const int pw = warp - kSmWarps;
     const int row = 32 * (pw & 3) + lane, j = pw >> 2;
     uint32_t ph_free[4] = {0, 0, 0, 0};
@@ -423,6 +431,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     }
   } else {
     // ======================================================== softmax / epilogue / MMA
+    tc::setmaxnreg_inc<kSmRegs>();
     const int q4 = warp & 3, half = warp >> 2;
     const int prow = 32 * q4 + lane;
     const uint32_t tl_lane = tmem + ((uint32_t)(32 * q4) << 16);
@@ -622,18 +631,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       wait(kBarSFull, ph_s);
       tc::tc_fence_after();
       float x[NH];
-      if (fp8) {
+      if (fp8) {   // x = sum_b rho_b S_b, two blocks per TMEM wait
 #pragma unroll
-        for (int g8 = 0; g8 < NH / 8; ++g8) {
-          float sv[8];
-          tc::tmem_ld<8>(tl_lane + Cfg::kColS + half * NH + 8 * g8, sv);
+        for (int g16 = 0; g16 < NH / 16; ++g16) {
+          const uint32_t c = tl_lane + Cfg::kColS + half * NH + 16 * g16;
+          uint32_t a[16], b[16];
+          tc::tmem_ld16x2(c, c + HPG, a, b);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) x[8 * g8 + i] = rho[0] * sv[i];
+          for (int i = 0; i < 16; ++i)
+            x[16 * g16 + i] = fmaf(rho[1], __uint_as_float(b[i]), rho[0] * __uint_as_float(a[i]));
+          tc::tmem_ld16x2(c + 2 * HPG, c + 3 * HPG, a, b);
 #pragma unroll
-          for (int b = 1; b < 4; ++b) {
-            tc::tmem_ld<8>(tl_lane + Cfg::kColS + b * HPG + half * NH + 8 * g8, sv);
+          for (int i = 0; i < 16; ++i)
+            x[16 * g16 + i] = fmaf(rho[3], __uint_as_float(b[i]),
+                                   fmaf(rho[2], __uint_as_float(a[i]), x[16 * g16 + i]));
+        }
+        if constexpr (NH % 16 != 0) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[8 * g8 + i] = fmaf(rho[b], sv[i], x[8 * g8 + i]);
+          for (int g8 = (NH / 16) * 2; g8 < NH / 8; ++g8) {
+            float sv[8];
+            tc::tmem_ld<8>(tl_lane + Cfg::kColS + half * NH + 8 * g8, sv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[8 * g8 + i] = rho[0] * sv[i];
+#pragma unroll
+            for (int b = 1; b < 4; ++b) {
+              tc::tmem_ld<8>(tl_lane + Cfg::kColS + b * HPG + half * NH + 8 * g8, sv);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[8 * g8 + i] = fmaf(rho[b], sv[i], x[8 * g8 + i]);
+            }
+          }
+        }
+      } else if constexpr (NH % 32 == 0) {
+#pragma unroll
+        for (int g32 = 0; g32 < NH / 32; ++g32) {
+          const uint32_t c = tl_lane + Cfg::kColS + half * NH + 32 * g32;
+          uint32_t a[16], b[16];
+          tc::tmem_ld16x2(c, c + 16, a, b);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            x[32 * g32 + i] = __uint_as_float(a[i]);
+            x[32 * g32 + 16 + i] = __uint_as_float(b[i]);
           }
         }
       } else {
@@ -758,6 +795,11 @@ cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
 #define DSA_TC_CASE(N)                                                                   \
   case N: {                                                                              \
     const int smem = (int)TcCfg<N>::kSmem;                                               \
+    cudaFuncAttributes fa;                                                               \
+    err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N>);                               \
+    if (err != cudaSuccess) return err;                                                  \
+    /* the warpgroup register split assumes exactly kLaunchRegs per thread */           \
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;                 \
     err = cudaFuncSetAttribute(tc_decode_kernel<N>,                                      \
                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
     if (err != cudaSuccess) return err;                                                  \

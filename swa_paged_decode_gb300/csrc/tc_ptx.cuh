@@ -85,6 +85,50 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]) \
       : "memory")
 
+// x16 load without the wait; pair with tmem_wait16 on the same registers
+// (the wait names them, so no use can move above it).
+#define DSA_TMEM_LD16_NOWAIT(taddr, r)                                                    \
+  asm volatile(                                                                           \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "                                           \
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"                   \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),           \
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),         \
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])                                \
+      : "r"(taddr)                                                                        \
+      : "memory")
+
+// Waits for every outstanding tcgen05.ld of the warp; the 32 registers are
+// tied to the wait so their uses stay below it.
+#define DSA_TMEM_WAIT32(a, b)                                                             \
+  asm volatile("tcgen05.wait::ld.sync.aligned;"                                           \
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),  \
+                 "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), \
+                 "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(b[0]),          \
+                 "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]),  \
+                 "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]),            \
+                 "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])                       \
+               :                                                                          \
+               : "memory")
+
+// Two x16 loads (columns c0.. and c1..) under one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, uint32_t (&a)[16],
+                                            uint32_t (&b)[16]) {
+  DSA_TMEM_LD16_NOWAIT(ta, a);
+  DSA_TMEM_LD16_NOWAIT(tb, b);
+  DSA_TMEM_WAIT32(a, b);
+}
+
+// Register budget of a warpgroup (multiple of 8); the four warps of the
+// warpgroup execute it together.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // N columns in groups of 8.
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float *v) {
