@@ -436,6 +436,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     const int prow = 32 * q4 + lane;
     const uint32_t tl_lane = tmem + ((uint32_t)(32 * q4) << 16);
     const bool issuer = tid == 0;   // issues every tcgen05.mma and commit
+    // Descriptor bases; an offset of `o` bytes adds o >> 4 to the start
+    // address field (no carry: shared addresses stay below 256 KiB).
+    const uint64_t dA_qk = tc::sdesc(kv_base, 16, 1024, tc::kSwz128);
+    const uint64_t dB_qk = tc::sdesc(q_base, 16, 1024, tc::kSwz128);
+    const uint64_t dA_pv = tc::sdesc(kv_base, 16384, 1024, tc::kSwz128);
+    const uint64_t dB_pv = tc::sdesc(p_base, Cfg::kPBytes, 8 * Cfg::kPRow, Cfg::kPSwz);
     uint32_t ph_s = 0, ph_kv[4] = {0, 0, 0, 0}, ph_pf = 0, ph_of = 0, sord = 0;
     float l_reg[NH];
     int32_t cur_t = -1;
@@ -601,10 +607,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
               const int kb = 2 * mb + kk;
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ad =
-                    tc::sdesc(kv_base + kb * 16384 + ks * 32, 16, 1024, tc::kSwz128);
-                const uint64_t bd =
-                    tc::sdesc(q_base + kb * HPG * 128 + ks * 32, 16, 1024, tc::kSwz128);
+                const uint64_t ad = dA_qk + (uint64_t)((kb * 16384 + ks * 32) >> 4);
+                const uint64_t bd = dB_qk + (uint64_t)((kb * HPG * 128 + ks * 32) >> 4);
                 tc::mma_f16(d_tmem, ad, bd, Cfg::kIdQK, fp8 ? (kk | ks) : (kb | ks));
               }
             }
@@ -752,16 +756,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           const int mb0 = fp8 ? batch * Cfg::kPBufs : 0;
           const int mb1 = fp8 ? mb0 + Cfg::kPBufs : 4;
           for (int mb = mb0; mb < mb1; ++mb) {
-            const uint32_t pb = p_base + (fp8 ? (uint32_t)(mb - mb0) * Cfg::kPBytes : 0u);
+            const uint64_t pb = dB_pv + (fp8 ? (uint64_t)(((mb - mb0) * Cfg::kPBytes) >> 4) : 0ull);
+            const uint64_t ab = dA_pv + (uint64_t)((2 * mb * 16384) >> 4);
+            const uint32_t dt = tmem + Cfg::kColO + mb * HPG;
+            tc::mma_f16(dt, ab, pb, Cfg::kIdPV, first_pv ? 0u : 1u);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t ad =
-                  tc::sdesc(kv_base + 2 * mb * 16384 + ks * 2048, 16384, 1024, tc::kSwz128);
-              const uint64_t bd = tc::sdesc(pb + ks * 16 * Cfg::kPRow, Cfg::kPBytes,
-                                            8 * Cfg::kPRow, Cfg::kPSwz);
-              tc::mma_f16(tmem + Cfg::kColO + mb * HPG, ad, bd, Cfg::kIdPV,
-                          (first_pv && ks == 0) ? 0u : 1u);
-            }
+            for (int ks = 1; ks < 8; ++ks)
+              tc::mma_f16(dt, ab + (uint64_t)((ks * 2048) >> 4),
+                          pb + (uint64_t)((ks * 16 * Cfg::kPRow) >> 4), Cfg::kIdPV, 1u);
             tc::mma_commit(&bars[kBarKvFree + mb]);
           }
           if (batch + 1 < nbatch) tc::mma_commit(&bars[kBarPFree]);
