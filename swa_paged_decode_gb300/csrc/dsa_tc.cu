@@ -117,22 +117,61 @@ __device__ __forceinline__ uint32_t p_off(int r, int ci) {
            (uint32_t)((ci ^ ((r & 7) >> 2)) << 4);
 }
 
-__device__ __forceinline__ void unit_info(const Params &p, int64_t u, int32_t &t, int32_t &lid,
-                                          int32_t &row0) {
-  t = (int32_t)(u / p.tpt);
-  unit_tile(p, u, lid, row0);
+// Position in the CTA's unit range, stepped without 64-bit divisions; keeps
+// min(len, width) of both lists for the current token.
+struct Cursor {
+  int64_t u;
+  int32_t t, k;        // token, tile index within the token
+  int32_t lim0, lim1;  // row limits of the two lists for token t
+};
+__device__ __forceinline__ void cursor_limits(const Params &p, Cursor &c) {
+  if (c.t < p.T) {
+    c.lim0 = list_limit(p.list[0], c.t);
+    c.lim1 = p.nlists > 1 ? list_limit(p.list[1], c.t) : 0;
+  } else {
+    c.lim0 = c.lim1 = 0;
+  }
 }
-
+__device__ __forceinline__ Cursor cursor_at(const Params &p, int64_t u) {
+  Cursor c;
+  c.u = u;
+  c.t = (int32_t)(u / p.tpt);
+  c.k = (int32_t)(u - (int64_t)c.t * p.tpt);
+  cursor_limits(p, c);
+  return c;
+}
+__device__ __forceinline__ void cursor_step(const Params &p, Cursor &c) {
+  ++c.u;
+  if (++c.k == p.tpt) {
+    c.k = 0;
+    ++c.t;
+    cursor_limits(p, c);
+  }
+}
+__device__ __forceinline__ void cursor_tile(const Params &p, const Cursor &c, int32_t &lid,
+                                            int32_t &row0) {
+  if (c.k < p.list[0].tiles) {
+    lid = 0;
+    row0 = c.k * kTile;
+  } else {
+    lid = 1;
+    row0 = (c.k - p.list[0].tiles) * kTile;
+  }
+}
 // A tile is worked on iff its first row lies below min(len, width).
-__device__ __forceinline__ bool unit_live(const Params &p, int64_t u) {
-  int32_t t, lid, row0;
-  unit_info(p, u, t, lid, row0);
-  return row0 < list_limit(p.list[lid], t);
+__device__ __forceinline__ bool cursor_live(const Params &p, const Cursor &c) {
+  int32_t lid, row0;
+  cursor_tile(p, c, lid, row0);
+  return row0 < (lid == 0 ? c.lim0 : c.lim1);
 }
-
-__device__ __forceinline__ int64_t next_live(const Params &p, int64_t u, int64_t u1) {
-  while (u < u1 && !unit_live(p, u)) ++u;
-  return u;
+// Advance to the next live unit below u1 (or to u1).
+__device__ __forceinline__ void cursor_next_live(const Params &p, Cursor &c, int64_t u1) {
+  do {
+    cursor_step(p, c);
+  } while (c.u < u1 && !cursor_live(p, c));
+}
+__device__ __forceinline__ void cursor_first_live(const Params &p, Cursor &c, int64_t u1) {
+  if (c.u < u1 && !cursor_live(p, c)) cursor_next_live(p, c, u1);
 }
 
 // fp32 block scale -> (f16 s_hi with 7 significant bits, rho = s / s_hi).
@@ -157,14 +196,14 @@ struct Gather {
   bool ok;
 };
 
-__device__ __forceinline__ void issue_loads(const Params &p, int64_t u, int32_t sid, int row,
+__device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, int32_t sid, int row,
                                             int j, Gather &g) {
-  int32_t t, lid, row0;
-  unit_info(p, u, t, lid, row0);
+  int32_t lid, row0;
+  cursor_tile(p, c, lid, row0);
   const ListArgs &L = p.list[lid];
   g.r = row0 + row;
   g.sid = sid;
-  g.ok = slot_valid(L, g.r, list_limit(L, t), sid);
+  g.ok = slot_valid(L, g.r, lid == 0 ? c.lim0 : c.lim1, sid);
   const uint4 z = make_uint4(0, 0, 0, 0);
   if (L.fmt == DSA_REC_FP8_528) {
     if (g.ok) {
@@ -200,12 +239,12 @@ __device__ __forceinline__ void issue_loads(const Params &p, int64_t u, int32_t 
   }
 }
 
-__device__ __forceinline__ int32_t load_sid(const Params &p, int64_t u, int row) {
-  int32_t t, lid, row0;
-  unit_info(p, u, t, lid, row0);
+__device__ __forceinline__ int32_t load_sid(const Params &p, const Cursor &c, int row) {
+  int32_t lid, row0;
+  cursor_tile(p, c, lid, row0);
   const ListArgs &L = p.list[lid];
   const int32_t r = row0 + row;
-  return r < L.width ? __ldg(L.ids + (int64_t)t * L.idx_stride + r) : -1;
+  return r < L.width ? __ldg(L.ids + (int64_t)c.t * L.idx_stride + r) : -1;
 }
 
 // Dequantize the two 64-dim k-blocks of M block mb for this thread's row.
@@ -298,7 +337,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   const uint32_t q_base = sbase + Cfg::kQ;
   const uint32_t p_base = sbase + Cfg::kP;
   __half *rho_s = reinterpret_cast<__half *>(smem + Cfg::kRho);
-  float *headf_s = reinterpret_cast<float *>(smem + Cfg::kHeadF);
   float *m_s = reinterpret_cast<float *>(smem + Cfg::kM);
   float *red_s = reinterpret_cast<float *>(smem + Cfg::kRed);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kMisc);
@@ -331,9 +369,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 
   // Bounded wait on a barrier phase. After any timeout (here or in another
   // warp) it returns at once; callers keep their control flow unchanged.
+  // Waits off the MMA-issue path sleep between polls; the issuing warp spins.
   auto wait = [&](int b, uint32_t &phase) {
     if (!*abort_s) {
-      const bool done = tc::mbar_wait(&bars[b], phase, kWaitBudget);
+      const bool done = tc::mbar_wait(&bars[b], phase, kWaitBudget, warp == 0 ? 0u : 2000u);
       if (!done && !*abort_s) {
         *abort_s = 1;
         report_status(p.status, DSA_ERR_TIMEOUT);
@@ -352,31 +391,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     uint32_t kept = 0, chk = 0, pord = 0;
     // Tile records are prefetched into L2 (bulk, one thread per row) two
     // tiles ahead and loaded into registers one tile ahead.
-    auto prefetch = [&](int64_t uu, int32_t sid) {
-      if (j != 0 || uu >= u1) return;
-      int32_t t2, lid2, row02;
-      unit_info(p, uu, t2, lid2, row02);
+    auto prefetch = [&](const Cursor &c, int32_t sid) {
+      if (j != 0 || c.u >= u1) return;
+      int32_t lid2, row02;
+      cursor_tile(p, c, lid2, row02);
       const ListArgs &L = p.list[lid2];
-      if (slot_valid(L, row02 + row, list_limit(L, t2), sid))
+      if (slot_valid(L, row02 + row, lid2 == 0 ? c.lim0 : c.lim1, sid))
         tc::prefetch_l2_bulk(record_ptr(L, sid), (uint32_t)L.rec);
     };
-    int64_t u = next_live(p, u0, u1);
-    int64_t un = u < u1 ? next_live(p, u + 1, u1) : u1;
-    int32_t sid_n1 = un < u1 ? load_sid(p, un, row) : -1;   // sid of the next tile
+    Cursor cu = cursor_at(p, u0);       // tile being dequantized
+    cursor_first_live(p, cu, u1);
+    Cursor cn = cu;                     // next live tile
+    if (cn.u < u1) cursor_next_live(p, cn, u1);
+    int32_t sid_n1 = cn.u < u1 ? load_sid(p, cn, row) : -1;   // sid of the next tile
     Gather g;
-    if (u < u1) {
-      const int32_t sid0 = load_sid(p, u, row);
-      prefetch(u, sid0);
-      prefetch(un, sid_n1);
-      issue_loads(p, u, sid0, row, j, g);
+    if (cu.u < u1) {
+      const int32_t sid0 = load_sid(p, cu, row);
+      prefetch(cu, sid0);
+      prefetch(cn, sid_n1);
+      issue_loads(p, cu, sid0, row, j, g);
     }
-    while (u < u1) {
-      int32_t t, lid, row0;
-      unit_info(p, u, t, lid, row0);
-      const int64_t un2 = un < u1 ? next_live(p, un + 1, u1) : u1;
-      const int32_t sid_n2 = un2 < u1 ? load_sid(p, un2, row) : -1;
+    while (cu.u < u1) {
+      const int32_t t = cu.t;
+      int32_t lid, row0;
+      cursor_tile(p, cu, lid, row0);
+      Cursor cn2 = cn;
+      if (cn2.u < u1) cursor_next_live(p, cn2, u1);
+      const int32_t sid_n2 = cn2.u < u1 ? load_sid(p, cn2, row) : -1;
       const int32_t sid_next = sid_n1;
-      const bool last_of_token = un >= u1 || (int32_t)(un / p.tpt) != t;
+      const bool last_of_token = cn.u >= u1 || cn.t != t;
       const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
       uint32_t shi2[4] = {0, 0, 0, 0};
       float rho[4] = {1.f, 1.f, 1.f, 1.f};
@@ -423,11 +466,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         if (lane == 0) mbar_arrive(&bars[kBarKvFull + mb]);
       }
       first = false;
-      prefetch(un2, sid_n2);
-      u = un;
-      un = un2;
+      prefetch(cn2, sid_n2);
+      cu = cn;
+      cn = cn2;
       sid_n1 = sid_n2;
-      if (u < u1) issue_loads(p, u, sid_next, row, j, g);
+      if (cu.u < u1) issue_loads(p, cu, sid_next, row, j, g);
     }
   } else {
     // ======================================================== softmax / epilogue / MMA
@@ -443,10 +486,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     const uint64_t dA_pv = tc::sdesc(kv_base, 16384, 1024, tc::kSwz128);
     const uint64_t dB_pv = tc::sdesc(p_base, Cfg::kPBytes, 8 * Cfg::kPRow, Cfg::kPSwz);
     uint32_t ph_s = 0, ph_kv[4] = {0, 0, 0, 0}, ph_pf = 0, ph_of = 0, sord = 0;
-    float l_reg[NH];
+    float l_reg[NH];              // per-head partial sums of this row
+    const float4 *m_s4 = reinterpret_cast<const float4 *>(m_s) + half * (NH / 4);
+    float headf = 0.f;            // scale * log2(e) * 2^e of the token's Q prescale
     int32_t cur_t = -1;
     bool seg_worked = false, first_pv = true;
 
+    // Q of token t -> f16 K-major SW128 tile. RoPE (NeoX) in fp32, then one
+    // power-of-two prescale for the whole token so max |q| lies in [1, 2):
+    // exact for bf16 inputs whose exponents fit f16's range after scaling.
+    auto load_q = [&](int32_t t, int h, int64_t pos, float (&v)[16]) {
+      const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)(h0 + h) * p.q_sh;
+      const uint4 a = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane);
+      const uint4 b = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane + 1);
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+        v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+      }
+      if (p.cos_sin) {   // NeoX: dim 448+i pairs with 480+i; lanes 28..31 hold 448..511
+        const float *cs = p.cos_sin + pos * 64;
+        const bool rope = lane >= 28;
+        const bool firsth = lane < 30;
+        const int i0 = (lane & 1) * 16;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float other = __shfl_xor_sync(0xffffffffu, v[k], 2);
+          if (rope) {
+            const float c = __ldg(cs + i0 + k), s = __ldg(cs + kRopeHalf + i0 + k);
+            v[k] = firsth ? (v[k] * c - other * s) : (v[k] * c + other * s);
+          }
+        }
+      }
+    };
     auto stage_q = [&](int32_t t) {
       int64_t pos = p.positions ? __ldg(p.positions + t) : 0;
       if (pos < 0 || (p.cos_sin && pos >= p.cs_rows)) {   // outside the table: flag, row 0
@@ -454,42 +527,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         pos = 0;
       }
       for (int h = warp; h < HPG; h += kSmWarps) {
-        const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)(h0 + h) * p.q_sh;
-        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane);
-        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane + 1);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         float v[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-          v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-        }
-        if (p.cos_sin) {   // NeoX: dim 448+i pairs with 480+i; lanes 28..31 hold 448..511
-          const float *cs = p.cos_sin + pos * 64;
-          const bool rope = lane >= 28;
-          const bool firsth = lane < 30;
-          const int i0 = (lane & 1) * 16;
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[k], 2);
-            if (rope) {
-              const float c = __ldg(cs + i0 + k), s = __ldg(cs + kRopeHalf + i0 + k);
-              v[k] = firsth ? (v[k] * c - other * s) : (v[k] * c + other * s);
-            }
-          }
-        }
+        load_q(t, h, pos, v);
         float mx = 0.f;
 #pragma unroll
         for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(v[k]));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        // Per-head power-of-two prescale: f16 Q with max |q| in [1, 2).
-        int e = (mx > 0.f) ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
-        e = e < -126 ? -126 : (e > 126 ? 126 : e);
-        const float down = __uint_as_float((uint32_t)(127 - e) << 23);
-        const float up = __uint_as_float((uint32_t)(127 + e) << 23);
-        if (lane == 0) headf_s[h] = p.scale_log2 * up;
+        if (lane == 0) red_s[h] = mx;
+      }
+      sm_bar();
+      float mx = 0.f;
+      for (int h = 0; h < HPG; ++h) mx = fmaxf(mx, red_s[h]);
+      int e = (mx > 0.f) ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+      e = e < -126 ? -126 : (e > 126 ? 126 : e);
+      const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+      headf = p.scale_log2 * __uint_as_float((uint32_t)(127 + e) << 23);
+      for (int h = warp; h < HPG; h += kSmWarps) {
+        float v[16];
+        load_q(t, h, pos, v);
         uint32_t f[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) f[i] = tc::pack_f16x2(v[2 * i] * down, v[2 * i + 1] * down);
@@ -499,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       }
       if (tid < HPG) m_s[tid] = -INFINITY;
       tc::fence_async_smem();
-      sm_bar();   // Q (async proxy), headf_s and m_s visible to the group
+      sm_bar();   // Q (async proxy) and m_s visible; red_s free again
     };
 
     // Token finished: sums over rows, sink, out / lse (or partial), selection.
@@ -576,9 +633,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 
     Segment seg;
     seg.t = -1;
-    for (int64_t u = u0; u < u1; ++u) {
-      int32_t t, lid, row0;
-      unit_info(p, u, t, lid, row0);
+    for (Cursor cu = cursor_at(p, u0); cu.u < u1; cursor_step(p, cu)) {
+      const int32_t t = cu.t;
+      int32_t lid, row0;
+      cursor_tile(p, cu, lid, row0);
       if (t != cur_t) {
         if (cur_t >= 0) finalize(seg);
         cur_t = t;
@@ -588,11 +646,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 #pragma unroll
         for (int j = 0; j < NH; ++j) l_reg[j] = 0.f;
         // Q is staged only for tokens with a live tile in this range.
-        bool any = false;
-        for (int64_t v = seg.u_begin; v < seg.u_end && !any; ++v) any = unit_live(p, v);
-        if (any) stage_q(t);
+        Cursor cv = cu;
+        cursor_first_live(p, cv, seg.u_end);
+        if (cv.u < seg.u_end) stage_q(t);
       }
-      if (!unit_live(p, u)) continue;
+      if (!cursor_live(p, cu)) continue;
       seg_worked = true;
       const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
       // ---- S = K . Q^T, one 128-dim block at a time as the producers land it
@@ -682,10 +740,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       }
       bool need = false;
 #pragma unroll
-      for (int j = 0; j < NH; ++j) {
-        const int h = half * NH + j;
-        x[j] = rv ? x[j] * headf_s[h] : -INFINITY;
-        need |= x[j] > m_s[h] + kRescaleSlack;
+      for (int g4 = 0; g4 < NH / 4; ++g4) {
+        const float4 m4 = m_s4[g4];
+        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float &xv = x[4 * g4 + i];
+          xv = rv ? xv * headf : -INFINITY;
+          need |= xv > mm[i] + kRescaleSlack;
+        }
       }
       if (sm_bar_or(need ? 1 : 0)) {
         // Raise the running max to the tile max; rescale sums and O.
@@ -725,10 +788,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       }
       // P = 2^(x - m) (<= 2^8) as f16, MN-major [128 rows, HPG]
 #pragma unroll
-      for (int j = 0; j < NH; ++j) {
-        const float mh = m_s[half * NH + j];
-        x[j] = (x[j] == -INFINITY) ? 0.f : tc::ex2(x[j] - mh);
-        l_reg[j] += x[j];
+      for (int g4 = 0; g4 < NH / 4; ++g4) {
+        const float4 m4 = m_s4[g4];
+        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float &xv = x[4 * g4 + i];
+          xv = (xv == -INFINITY) ? 0.f : tc::ex2(xv - mm[i]);
+          l_reg[4 * g4 + i] += xv;
+        }
       }
       const int nbatch = fp8 ? 4 / Cfg::kPBufs : 1;
       for (int batch = 0; batch < nbatch; ++batch) {
@@ -767,8 +835,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
             tc::mma_commit(&bars[kBarKvFree + mb]);
           }
           if (batch + 1 < nbatch) tc::mma_commit(&bars[kBarPFree]);
-          else if (u + 1 >= seg.u_end || next_live(p, u + 1, seg.u_end) >= seg.u_end)
-            tc::mma_commit(&bars[kBarOFinal]);   // last PV of this token
+          else {
+            Cursor cv = cu;
+            cursor_next_live(p, cv, seg.u_end);
+            if (cv.u >= seg.u_end) tc::mma_commit(&bars[kBarOFinal]);   // last PV of this token
+          }
         }
         __syncwarp();
       }

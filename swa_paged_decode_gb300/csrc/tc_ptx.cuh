@@ -45,11 +45,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
   return ok != 0;
 }
 // Bounded wait on a phase: gives up (returns false) after `budget` SM
-// clock cycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long budget) {
+// clock cycles. With `sleep_ns` > 0 the thread sleeps between polls (woken
+// early when the phase completes), leaving issue slots to busy warps.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long budget,
+                                          uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait_sleep(bar, parity, 20000u))
+  while (!(sleep_ns ? mbar_try_wait_sleep(bar, parity, sleep_ns) : mbar_try_wait(bar, parity)))
     if (clock64() - t0 > budget) return false;
   return true;
 }
@@ -180,14 +182,17 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// No "memory" clobber: the MMA touches shared memory and TMEM only through
+// the async proxy, ordered by the fences and barriers around it (all volatile
+// asm, which the compiler keeps in program order); a clobber here would force
+// reloads of spilled values before every MMA.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 // Arrive on `bar` once every tcgen05 op this thread issued so far completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
