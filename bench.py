@@ -36,11 +36,25 @@ UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20        # > 2x the 126 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM traffic of tc_decode_kernel<64> from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum, one launch of the
+# bandwidth-stress workload at 256 tokens), per gathered KV row; valid only
+# while the kernel sources hash to `sources`. The capture is summarised under
+# profiles/ with the command that made it.
+NCU_TRAFFIC = {
+    "sources": "0deadecde8d77038",
+    "workload": "config5_T256_H64",
+    "bytes_per_launch": 444004608 + 29087744,
+    "rows_per_launch": 256 * (128 + 4096),
+}
+KERNEL_SOURCES = ("swa_paged_decode_gb300/csrc/dsa_tc.cu", "swa_paged_decode_gb300/csrc/tc_ptx.cuh",
+                  "swa_paged_decode_gb300/csrc/dsa_internal.cuh")
+
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, help="workload 1..5")
@@ -109,10 +123,18 @@ class ClockSampler:
             self.file = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return self
+        # start timing only once the sampler is producing lines
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            self.file.flush()
+            if os.path.getsize(f"/proc/self/fd/{self.file.fileno()}") > 0:
+                break
+            time.sleep(0.02)
         return self
 
     def __exit__(self, *exc):
@@ -257,11 +279,29 @@ def roofline(w: W.Workload, alg, kern_ms_avg: float, peaks, peak_kind):
     else:
         ach = alg["gathered_bytes"] / s / 1e9
         r = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
-    r["traffic"] = None
+    r["traffic"] = ncu_traffic(alg["rows"])
     r["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
     r["intensity_flop_per_byte"] = intensity
     r["kernel_ms"] = kern_ms_avg
     return r
+
+
+def sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(rows: int):
+    """Captured DRAM bytes per launch scaled to `rows` gathered rows (the
+    traffic grows with the rows: same per-token lists, more tokens); None
+    once the kernel sources differ from the captured ones."""
+    if sources_hash() != NCU_TRAFFIC["sources"]:
+        return None
+    return int(NCU_TRAFFIC["bytes_per_launch"] * rows / NCU_TRAFFIC["rows_per_launch"])
 
 
 def gpu_arm(args, rank, world, B, peaks, peak_kind):
