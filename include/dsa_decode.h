@@ -178,6 +178,44 @@ dsa_status dsa_decode_selection(const dsa_decode_plan_t *plan, const void *works
 dsa_status dsa_decode_read_status(const void *workspace, dsa_stream_t stream,
                                   int32_t *device_status);
 
+/* Bytes of the library's own device scratch used by dsa_decode_run_noalloc
+ * (one array per device, 48 MiB). A plan for up to 152 SMs needs about
+ * 40 MB plus 8 bytes per token, so every plan of up to ~1M tokens on a
+ * GB300 fits. */
+#define DSA_NOALLOC_MAX_WORKSPACE (48u * 1024u * 1024u)
+
+/* dsa_decode_run followed by dsa_decode_combine, with the library's own
+ * file-scope device array (DSA_NOALLOC_MAX_WORKSPACE bytes) as the
+ * workspace. The pages that define the method have no counterpart of this
+ * call. It serves callers that cannot provide a workspace: a plain C host
+ * program without a device allocator of its own, or a runtime that has given
+ * all free device memory to its KV-cache pool. A cudaMalloc inside the call
+ * would also synchronize the device. The call allocates nothing.
+ *   plan: from dsa_decode_plan; a plan whose workspace_bytes exceeds
+ *         DSA_NOALLOC_MAX_WORKSPACE is refused with DSA_ERR_WORKSPACE
+ *         before any CUDA call.
+ *   q ... lse, stream: as for dsa_decode_run; out and lse receive the final
+ *         (combined) result.
+ *   device_status: optional int32 device pointer (4-byte aligned). When
+ *         non-NULL, it receives an asynchronous copy of the device status
+ *         word (DSA_OK, or what the kernels recorded, as
+ *         dsa_decode_read_status reports it).
+ * Set-up: the first call on each device, with that device current, looks
+ * the array up (cudaGetSymbolAddress, which may load the module); make that
+ * first call before any stream capture. The array is shared: calls that
+ * overlap in time on one device (other streams or host threads) race on it
+ * and must be serialized by the caller. */
+dsa_status dsa_decode_run_noalloc(const dsa_decode_plan_t *plan, const void *q,
+                                  int64_t q_stride_t, int64_t q_stride_h,
+                                  const dsa_cache_desc *swa_cache, const int32_t *swa_idx,
+                                  int64_t swa_idx_stride, const int32_t *swa_lens,
+                                  const dsa_cache_desc *extra_cache, const int32_t *extra_idx,
+                                  int64_t extra_idx_stride, const int32_t *extra_lens,
+                                  const float *sink, const int64_t *positions,
+                                  const float *cos_sin, int64_t cos_sin_rows, float scale,
+                                  void *out, float *lse, int32_t *device_status,
+                                  dsa_stream_t stream);
+
 /* Static description of a status code. */
 const char *dsa_decode_status_string(dsa_status s);
 

@@ -75,6 +75,11 @@ def load(path: str = LIB_PATH):
     lib.dsa_decode_selection.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp]
     lib.dsa_decode_read_status.restype = ctypes.c_int
     lib.dsa_decode_read_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.dsa_decode_run_noalloc.restype = ctypes.c_int
+    lib.dsa_decode_run_noalloc.argtypes = [ctypes.POINTER(Plan), vp, i64, i64,
+                                           ctypes.POINTER(CacheDesc), vp, i64, vp,
+                                           ctypes.POINTER(CacheDesc), vp, i64, vp,
+                                           vp, vp, vp, i64, ctypes.c_float, vp, vp, vp, vp]
     lib.dsa_decode_status_string.restype = ctypes.c_char_p
     lib.dsa_decode_status_string.argtypes = [ctypes.c_int]
     lib.dsa_decode_abi_version.restype = ctypes.c_int32
@@ -159,6 +164,29 @@ def dsa_decode_read_status(workspace: torch.Tensor, stream=None) -> int:
     _check("dsa_decode_read_status", load().dsa_decode_read_status(
         workspace.data_ptr(), _stream(stream), ctypes.byref(v)))
     return int(v.value)
+
+
+def dsa_decode_run_noalloc(plan: Plan, q: torch.Tensor, swa_cache: W.PagedCache,
+                           swa_idx: torch.Tensor, swa_lens: torch.Tensor,
+                           extra_cache: Optional[W.PagedCache], extra_idx: Optional[torch.Tensor],
+                           extra_lens: Optional[torch.Tensor], sink: Optional[torch.Tensor],
+                           positions: Optional[torch.Tensor], cos_sin: Optional[torch.Tensor],
+                           scale: float, out: torch.Tensor, lse: torch.Tensor,
+                           device_status: Optional[torch.Tensor] = None, stream=None,
+                           check: bool = True) -> int:
+    """run + combine on the library's own device scratch (no workspace)."""
+    sc, ec = cache_desc(swa_cache), cache_desc(extra_cache)
+    rc = load().dsa_decode_run_noalloc(
+        ctypes.byref(plan), q.data_ptr(), q.stride(0), q.stride(1),
+        ctypes.byref(sc), swa_idx.data_ptr(), swa_idx.stride(0), swa_lens.data_ptr(),
+        None if ec is None else ctypes.byref(ec), _ptr(extra_idx),
+        0 if extra_idx is None else extra_idx.stride(0), _ptr(extra_lens),
+        _ptr(sink), _ptr(positions), _ptr(cos_sin),
+        0 if cos_sin is None else cos_sin.shape[0], float(scale),
+        out.data_ptr(), lse.data_ptr(), _ptr(device_status), _stream(stream))
+    if check:
+        _check("dsa_decode_run_noalloc", rc)
+    return rc
 
 
 class Decoder:
