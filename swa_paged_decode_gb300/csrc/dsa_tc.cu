@@ -653,27 +653,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       if (!cursor_live(p, cu)) continue;
       seg_worked = true;
       const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
-      // ---- S = K . Q^T, one 128-dim block at a time as the producers land it
+      // ---- S = K . Q^T over the whole tile: the MMAs go out back to back
+      // once all four 128-dim blocks have landed (in steady state they have
+      // by the time the previous tile's PV is issued), which keeps the
+      // issue loop free of waits and warp syncs.
       if (warp == 0) {
-        for (int mb = 0; mb < 4; ++mb) {
-          wait(kBarKvFull + mb, ph_kv[mb]);
-          tc::tc_fence_after();
-          if (issuer && !*abort_s) {
-            const uint32_t d_tmem = tmem + Cfg::kColS + (fp8 ? (uint32_t)mb * HPG : 0u);
+        for (int mb = 0; mb < 4; ++mb) wait(kBarKvFull + mb, ph_kv[mb]);
+        tc::tc_fence_after();
+        if (issuer && !*abort_s) {
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const int kb = 2 * mb + kk;
+          for (int kb = 0; kb < 8; ++kb) {
+            const uint32_t d_tmem = tmem + Cfg::kColS + (fp8 ? (uint32_t)(kb >> 1) * HPG : 0u);
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ad = dA_qk + (uint64_t)((kb * 16384 + ks * 32) >> 4);
-                const uint64_t bd = dB_qk + (uint64_t)((kb * HPG * 128 + ks * 32) >> 4);
-                tc::mma_f16(d_tmem, ad, bd, Cfg::kIdQK, fp8 ? (kk | ks) : (kb | ks));
-              }
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = dA_qk + (uint64_t)((kb * 16384 + ks * 32) >> 4);
+              const uint64_t bd = dB_qk + (uint64_t)((kb * HPG * 128 + ks * 32) >> 4);
+              tc::mma_f16(d_tmem, ad, bd, Cfg::kIdQK, fp8 ? ((kb & 1) | ks) : (kb | ks));
             }
           }
-          __syncwarp();
+          tc::mma_commit(&bars[kBarSFull]);
         }
-        if (issuer && !*abort_s) tc::mma_commit(&bars[kBarSFull]);
         __syncwarp();
       } else {
         // rho / row validity are written with block 0 of the tile
@@ -823,7 +822,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           tc::tc_fence_after();
           const int mb0 = fp8 ? batch * Cfg::kPBufs : 0;
           const int mb1 = fp8 ? mb0 + Cfg::kPBufs : 4;
-          for (int mb = mb0; mb < mb1; ++mb) {
+          // M blocks unrolled with compile-time indices (runtime-indexed
+          // operands slowed the issue loop measurably).
+#pragma unroll
+          for (int mb = 0; mb < 4; ++mb) {
+            if (mb < mb0 || mb >= mb1) continue;
             const uint64_t pb = dB_pv + (fp8 ? (uint64_t)(((mb - mb0) * Cfg::kPBytes) >> 4) : 0ull);
             const uint64_t ab = dA_pv + (uint64_t)((2 * mb * 16384) >> 4);
             const uint32_t dt = tmem + Cfg::kColO + mb * HPG;
