@@ -9,21 +9,19 @@
 //            K-major tile in shared memory, 128-byte swizzle (16-byte chunk c
 //            of row r at chunk c ^ (r % 8)), written one 128-dim block at a
 //            time as soon as the PV MMAs of the previous tile release it.
-//            NVFP4: e2m1 * e4m3 scale (exact in f16). fp8: e4m3 * s_hi with
-//            s_hi = the fp32 block scale rounded to 7 significant bits (the
-//            product is exact in f16); rho = s / s_hi goes to the softmax.
+//            NVFP4: e2m1 * e4m3 scale (exact in f16). fp8: e4m3 * the fp32
+//            block scale rounded to f16, the product rounded to f16
+//            (relative error <= 2^-11 per element).
 //   MMA issue (one thread of warp 0)  swap-AB tcgen05.mma kind::f16:
-//            S[128 rows, H] = K[128, 512] . Q[H, 512]^T into TMEM (fp8 tiles:
-//            one accumulator per 128-dim scale block), issued block by block
-//            as the producers land them; then O^T[512, H] += K^T . P in four
+//            S[128 rows, H] = K[128, 512] . Q[H, 512]^T into TMEM, issued back
+//            to back once the tile has landed; then O^T[512, H] += K^T . P in four
 //            128-dim M blocks, A read MN-major from the same tile. Commits
 //            release tile blocks (to the producers) and S / O (to softmax).
 //   softmax (warps 0-7)     one TMEM lane (= one KV row) and half of the heads
-//            per thread; scores x = (sum_b rho_b S_b) * scale * log2e;
+//            per thread; scores x = S * scale * log2e;
 //            base-2 running max per head that moves only when a score passes
 //            it by 2^8 (then O in TMEM and the partial sums are rescaled);
-//            P = 2^(x - m) as f16 (fp8 tiles: P'_mb = P * rho_mb per M block,
-//            so PV sees the exact row as well). Also stages Q (NeoX RoPE,
+//            P = 2^(x - m) as f16. Also stages Q (NeoX RoPE,
 //            per-head power-of-two prescale into f16) and, per token,
 //            reduces the sums, folds the sink into the denominator and writes
 //            out (bf16) and lse (fp32) -- or an fp32 partial for a token split
@@ -64,12 +62,11 @@ template <int HPG>
 struct TcCfg {
   static constexpr int kHalf = HPG / 2;                  // heads per softmax thread
   static constexpr int kPRow = HPG * 2;                  // bytes per P row
-  static constexpr int kPBufs = HPG == 64 ? 2 : 4;       // P' buffers (fp8: one per M block)
   static constexpr uint32_t kPBytes = 128 * kPRow;
   static constexpr uint32_t kKV = 0;                     // 128 x 512 f16 = 128 KiB
   static constexpr uint32_t kQ = 131072;                 // HPG x 512 f16
-  static constexpr uint32_t kP = kQ + HPG * 1024;        // kPBufs x [128 x HPG] f16
-  static constexpr uint32_t kRho = kP + kPBufs * kPBytes;  // [128][4] f16: rho - 1 (-2: row not kept)
+  static constexpr uint32_t kP = kQ + HPG * 1024;        // [128 x HPG] f16
+  static constexpr uint32_t kRho = kP + kPBytes;         // [128] f32 row flag: 1 kept, 0 not
   static constexpr uint32_t kHeadF = kRho + 1024;        // [64] f32 per-head score factor
   static constexpr uint32_t kM = kHeadF + 256;           // [64] running max (log2)
   static constexpr uint32_t kRed = kM + 256;             // [4][64] f32
@@ -90,9 +87,8 @@ enum Bar : int {
   kBarKvFull = 0,   // [4] producers -> softmax: 128-dim block of the tile written
   kBarKvFree = 4,   // [4] MMA commit -> producers: block no longer read
   kBarSFull = 8,    // MMA commit -> softmax: S ready (and every earlier MMA done)
-  kBarPFree = 9,    // MMA commit -> softmax: first P' batch consumed
-  kBarOFinal = 10,  // MMA commit -> softmax: last PV of a token done
-  kNumBars = 11
+  kBarOFinal = 9,   // MMA commit -> softmax: last PV of a token done
+  kNumBars = 10
 };
 constexpr uint32_t kMiscAbort = 8 * kNumBars;        // int32
 constexpr uint32_t kMiscTmem = kMiscAbort + 4;       // uint32
@@ -175,15 +171,10 @@ __device__ __forceinline__ void cursor_first_live(const Params &p, Cursor &c, in
   if (c.u < u1 && !cursor_live(p, c)) cursor_next_live(p, c, u1);
 }
 
-// fp32 block scale -> (f16 s_hi with 7 significant bits, rho = s / s_hi).
-__device__ __forceinline__ void split_scale(float s, uint32_t &shi2, float &rho) {
-  uint32_t u = __float_as_uint(s);
-  u = (u + 0x10000u) & 0xFFFE0000u;
-  const __half h = __float2half_rn(__uint_as_float(u));
-  const float hf = __half2float(h);
-  rho = (hf != 0.f) ? s / hf : 0.f;
-  const uint32_t hb = (uint32_t)__half_as_ushort(h);
-  shi2 = hb | (hb << 16);
+// fp32 block scale -> f16x2 (both halves = the scale rounded to f16).
+__device__ __forceinline__ uint32_t scale_f16x2(float s) {
+  const uint32_t hb = (uint32_t)__half_as_ushort(__float2half_rn(s));
+  return hb | (hb << 16);
 }
 
 // ---------------------------------------------------------------- producer
@@ -249,7 +240,7 @@ __device__ __forceinline__ int32_t load_sid(const Params &p, const Cursor &c, in
 }
 
 // Dequantize the two 64-dim k-blocks of M block mb for this thread's row.
-__device__ __forceinline__ void dequant_block(bool fp8, const Gather &g, const uint32_t (&shi2)[4],
+__device__ __forceinline__ void dequant_block(bool fp8, const Gather &g, const uint32_t (&scale2)[4],
                                               int mb, int row, int j, uint32_t kv_base) {
   if (fp8) {
     // chunks c = 4m + 2j + e of k-block m; M block mb = k-blocks {2mb, 2mb+1}
@@ -260,7 +251,7 @@ __device__ __forceinline__ void dequant_block(bool fp8, const Gather &g, const u
       for (int e = 0; e < 2; ++e) {
         const int k = 2 * m + e;
         const int c = 4 * m + 2 * j + e;   // dims [16c, 16c+16), scale block mb
-        const uint32_t sc = shi2[mb];
+        const uint32_t sc = scale2[mb];
         const uint32_t w[4] = {g.d[k].x, g.d[k].y, g.d[k].z, g.d[k].w};
         uint32_t f[8];
 #pragma unroll
@@ -337,7 +328,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   const uint32_t kv_base = sbase + Cfg::kKV;
   const uint32_t q_base = sbase + Cfg::kQ;
   const uint32_t p_base = sbase + Cfg::kP;
-  __half *rho_s = reinterpret_cast<__half *>(smem + Cfg::kRho);
+  float *row_ok_s = reinterpret_cast<float *>(smem + Cfg::kRho);
   float *m_s = reinterpret_cast<float *>(smem + Cfg::kM);
   float *red_s = reinterpret_cast<float *>(smem + Cfg::kRed);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kMisc);
@@ -422,13 +413,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const int32_t sid_next = sid_n1;
       const bool last_of_token = cn.u >= u1 || cn.t != t;
       const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
-      uint32_t shi2[4] = {0, 0, 0, 0};
-      float rho[4] = {1.f, 1.f, 1.f, 1.f};
+      uint32_t scale2[4] = {0, 0, 0, 0};
       if (fp8) {
-        split_scale(__uint_as_float(g.s[0].x), shi2[0], rho[0]);
-        split_scale(__uint_as_float(g.s[0].y), shi2[1], rho[1]);
-        split_scale(__uint_as_float(g.s[0].z), shi2[2], rho[2]);
-        split_scale(__uint_as_float(g.s[0].w), shi2[3], rho[3]);
+        scale2[0] = scale_f16x2(__uint_as_float(g.s[0].x));
+        scale2[1] = scale_f16x2(__uint_as_float(g.s[0].y));
+        scale2[2] = scale_f16x2(__uint_as_float(g.s[0].z));
+        scale2[3] = scale_f16x2(__uint_as_float(g.s[0].w));
       }
       if (j == 0 && g.ok) {
         kept += 1;
@@ -451,17 +441,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       }
       for (int mb = 0; mb < 4; ++mb) {
         if (!first) wait(kBarKvFree + mb, ph_free[mb]);
-        if (mb == 0 && j == 0) {
-          // rho - 1 as f16 (|rho - 1| <= 2^-8); -2 marks a row that is not kept
-          const float v0 = g.ok ? rho[0] - 1.f : -2.f, v1 = g.ok ? rho[1] - 1.f : -2.f;
-          const float v2 = g.ok ? rho[2] - 1.f : -2.f, v3 = g.ok ? rho[3] - 1.f : -2.f;
-          __half2 a = __floats2half2_rn(v0, v1), b = __floats2half2_rn(v2, v3);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t *>(&a);
-          pk.y = *reinterpret_cast<uint32_t *>(&b);
-          reinterpret_cast<uint2 *>(rho_s)[row] = pk;
-        }
-        dequant_block(fp8, g, shi2, mb, row, j, kv_base);
+        if (mb == 0 && j == 0) row_ok_s[row] = g.ok ? 1.f : 0.f;
+        dequant_block(fp8, g, scale2, mb, row, j, kv_base);
         tc::fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarKvFull + mb]);
@@ -486,7 +467,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     const uint64_t dB_qk = tc::sdesc(q_base, 16, 1024, tc::kSwz128);
     const uint64_t dA_pv = tc::sdesc(kv_base, 16384, 1024, tc::kSwz128);
     const uint64_t dB_pv = tc::sdesc(p_base, Cfg::kPBytes, 8 * Cfg::kPRow, Cfg::kPSwz);
-    uint32_t ph_s = 0, ph_kv[4] = {0, 0, 0, 0}, ph_pf = 0, ph_of = 0, sord = 0;
+    uint32_t ph_s = 0, ph_kv[4] = {0, 0, 0, 0}, ph_of = 0, sord = 0;
     float l_reg[NH];              // per-head partial sums of this row
     const float4 *m_s4 = reinterpret_cast<const float4 *>(m_s) + half * (NH / 4);
     float headf = 0.f;            // scale * log2(e) * 2^e of the token's Q prescale
@@ -653,7 +634,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       }
       if (!cursor_live(p, cu)) continue;
       seg_worked = true;
-      const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
       // ---- S = K . Q^T over the whole tile: the MMAs go out back to back
       // once all four 128-dim blocks have landed (in steady state they have
       // by the time the previous tile's PV is issued), which keeps the
@@ -664,66 +644,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         if (issuer && !*abort_s) {
 #pragma unroll
           for (int kb = 0; kb < 8; ++kb) {
-            const uint32_t d_tmem = tmem + Cfg::kColS + (fp8 ? (uint32_t)(kb >> 1) * HPG : 0u);
+            const uint32_t d_tmem = tmem + Cfg::kColS;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               const uint64_t ad = dA_qk + (uint64_t)((kb * 16384 + ks * 32) >> 4);
               const uint64_t bd = dB_qk + (uint64_t)((kb * HPG * 128 + ks * 32) >> 4);
-              tc::mma_f16(d_tmem, ad, bd, Cfg::kIdQK, fp8 ? ((kb & 1) | ks) : (kb | ks));
+              tc::mma_f16(d_tmem, ad, bd, Cfg::kIdQK, (kb | ks) ? 1u : 0u);
             }
           }
           tc::mma_commit(&bars[kBarSFull]);
         }
         __syncwarp();
       } else {
-        // rho / row validity are written with block 0 of the tile
+        // the row flags are written with block 0 of the tile
         wait(kBarKvFull, ph_kv[0]);
       }
-      float rho[4];
-      {
-        const uint2 pk = reinterpret_cast<const uint2 *>(rho_s)[prow];
-        const __half2 a = *reinterpret_cast<const __half2 *>(&pk.x);
-        const __half2 b = *reinterpret_cast<const __half2 *>(&pk.y);
-        rho[0] = __low2float(a) + 1.f;
-        rho[1] = __high2float(a) + 1.f;
-        rho[2] = __low2float(b) + 1.f;
-        rho[3] = __high2float(b) + 1.f;
-      }
-      const bool rv = rho[0] >= 0.f;   // -2 + 1 marks a row that is not kept
+      const bool rv = row_ok_s[prow] != 0.f;
       wait(kBarSFull, ph_s);
       tc::tc_fence_after();
       float x[NH];
-      if (fp8) {   // x = sum_b rho_b S_b, two blocks per TMEM wait
-#pragma unroll
-        for (int g16 = 0; g16 < NH / 16; ++g16) {
-          const uint32_t c = tl_lane + Cfg::kColS + half * NH + 16 * g16;
-          uint32_t a[16], b[16];
-          tc::tmem_ld16x2(c, c + HPG, a, b);
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            x[16 * g16 + i] = fmaf(rho[1], __uint_as_float(b[i]), rho[0] * __uint_as_float(a[i]));
-          tc::tmem_ld16x2(c + 2 * HPG, c + 3 * HPG, a, b);
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            x[16 * g16 + i] = fmaf(rho[3], __uint_as_float(b[i]),
-                                   fmaf(rho[2], __uint_as_float(a[i]), x[16 * g16 + i]));
-        }
-        if constexpr (NH % 16 != 0) {
-#pragma unroll
-          for (int g8 = (NH / 16) * 2; g8 < NH / 8; ++g8) {
-            float sv[8];
-            tc::tmem_ld<8>(tl_lane + Cfg::kColS + half * NH + 8 * g8, sv);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[8 * g8 + i] = rho[0] * sv[i];
-#pragma unroll
-            for (int b = 1; b < 4; ++b) {
-              tc::tmem_ld<8>(tl_lane + Cfg::kColS + b * HPG + half * NH + 8 * g8, sv);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) x[8 * g8 + i] = fmaf(rho[b], sv[i], x[8 * g8 + i]);
-            }
-          }
-        }
-      } else if constexpr (NH % 32 == 0) {
+      if constexpr (NH % 32 == 0) {
 #pragma unroll
         for (int g32 = 0; g32 < NH / 32; ++g32) {
           const uint32_t c = tl_lane + Cfg::kColS + half * NH + 32 * g32;
@@ -798,55 +738,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           l_reg[4 * g4 + i] += xv;
         }
       }
-      const int nbatch = fp8 ? 4 / Cfg::kPBufs : 1;
-      for (int batch = 0; batch < nbatch; ++batch) {
-        if (batch > 0) wait(kBarPFree, ph_pf);
-        const int nb = fp8 ? Cfg::kPBufs : 1;
-        for (int i = 0; i < nb; ++i) {
-          const float f = fp8 ? rho[batch * nb + i] : 1.f;
 #pragma unroll
-          for (int k = 0; k < NH / 8; ++k) {
-            uint32_t pw[4];
+      for (int k = 0; k < NH / 8; ++k) {
+        uint32_t pw[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              pw[e] = tc::pack_f16x2(x[8 * k + 2 * e] * f, x[8 * k + 2 * e + 1] * f);
-            const int ci = half * (NH / 8) + k;
-            tc::st_shared_v4(p_base + i * Cfg::kPBytes + p_off<HPG>(prow, ci), pw[0], pw[1],
-                             pw[2], pw[3]);
-          }
-        }
-        tc::fence_async_smem();
-        tc::tc_fence_before();
-        sm_bar();   // P' of this batch written by the whole group
-        // ---- O^T += K^T . P
-        if (issuer && !*abort_s) {
-          tc::tc_fence_after();
-          const int mb0 = fp8 ? batch * Cfg::kPBufs : 0;
-          const int mb1 = fp8 ? mb0 + Cfg::kPBufs : 4;
-          // M blocks unrolled with compile-time indices (runtime-indexed
-          // operands slowed the issue loop measurably).
-#pragma unroll
-          for (int mb = 0; mb < 4; ++mb) {
-            if (mb < mb0 || mb >= mb1) continue;
-            const uint64_t pb = dB_pv + (fp8 ? (uint64_t)(((mb - mb0) * Cfg::kPBytes) >> 4) : 0ull);
-            const uint64_t ab = dA_pv + (uint64_t)((2 * mb * 16384) >> 4);
-            const uint32_t dt = tmem + Cfg::kColO + mb * HPG;
-            tc::mma_f16(dt, ab, pb, Cfg::kIdPV, first_pv ? 0u : 1u);
-#pragma unroll
-            for (int ks = 1; ks < 8; ++ks)
-              tc::mma_f16(dt, ab + (uint64_t)((ks * 2048) >> 4),
-                          pb + (uint64_t)((ks * 16 * Cfg::kPRow) >> 4), Cfg::kIdPV, 1u);
-            tc::mma_commit(&bars[kBarKvFree + mb]);
-          }
-          if (batch + 1 < nbatch) tc::mma_commit(&bars[kBarPFree]);
-          else {
-            Cursor cv = cu;
-            cursor_next_live(p, cv, seg.u_end);
-            if (cv.u >= seg.u_end) tc::mma_commit(&bars[kBarOFinal]);   // last PV of this token
-          }
-        }
-        __syncwarp();
+        for (int e = 0; e < 4; ++e) pw[e] = tc::pack_f16x2(x[8 * k + 2 * e], x[8 * k + 2 * e + 1]);
+        const int ci = half * (NH / 8) + k;
+        tc::st_shared_v4(p_base + p_off<HPG>(prow, ci), pw[0], pw[1], pw[2], pw[3]);
       }
+      tc::fence_async_smem();
+      tc::tc_fence_before();
+      sm_bar();   // P written by the whole group
+      // ---- O^T += K^T . P
+      if (issuer && !*abort_s) {
+        tc::tc_fence_after();
+        // M blocks unrolled with compile-time indices (runtime-indexed
+        // operands slowed the issue loop measurably).
+#pragma unroll
+        for (int mb = 0; mb < 4; ++mb) {
+          const uint64_t ab = dA_pv + (uint64_t)((2 * mb * 16384) >> 4);
+          const uint32_t dt = tmem + Cfg::kColO + mb * HPG;
+          tc::mma_f16(dt, ab, dB_pv, Cfg::kIdPV, first_pv ? 0u : 1u);
+#pragma unroll
+          for (int ks = 1; ks < 8; ++ks)
+            tc::mma_f16(dt, ab + (uint64_t)((ks * 2048) >> 4),
+                        dB_pv + (uint64_t)((ks * 16 * Cfg::kPRow) >> 4), Cfg::kIdPV, 1u);
+          tc::mma_commit(&bars[kBarKvFree + mb]);
+        }
+        Cursor cv = cu;
+        cursor_next_live(p, cv, seg.u_end);
+        if (cv.u >= seg.u_end) tc::mma_commit(&bars[kBarOFinal]);   // last PV of this token
+      }
+      __syncwarp();
       first_pv = false;
     }
     if (cur_t >= 0) finalize(seg);
