@@ -84,11 +84,11 @@ struct TcCfg {
 
 // mbarrier slots in the misc area
 enum Bar : int {
-  kBarKvFull = 0,   // [4] producers -> softmax: 128-dim block of the tile written
-  kBarKvFree = 4,   // [4] MMA commit -> producers: block no longer read
-  kBarSFull = 8,    // MMA commit -> softmax: S ready (and every earlier MMA done)
-  kBarOFinal = 9,   // MMA commit -> softmax: last PV of a token done
-  kNumBars = 10
+  kBarKvFull = 0,   // producers -> MMA / softmax: the whole tile written
+  kBarKvFree = 1,   // [4] MMA commit -> producers: 128-dim block no longer read
+  kBarSFull = 5,    // MMA commit -> softmax: S ready (and every earlier MMA done)
+  kBarOFinal = 6,   // MMA commit -> softmax: last PV of a token done
+  kNumBars = 7
 };
 constexpr uint32_t kMiscAbort = 8 * kNumBars;        // int32
 constexpr uint32_t kMiscTmem = kMiscAbort + 4;       // uint32
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   }
   if (tid == 0) {
     for (int b = 0; b < kNumBars; ++b)
-      tc::mbar_init(&bars[b], (b >= kBarKvFull && b < kBarKvFull + 4) ? kPrWarps : 1u);
+      tc::mbar_init(&bars[b], b == kBarKvFull ? kPrWarps : 1u);
     tc::fence_mbar_init();
     *abort_s = 0;
     for (int i = 0; i < 8; ++i) cnt_s[i] = 0;
@@ -443,10 +443,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         if (!first) wait(kBarKvFree + mb, ph_free[mb]);
         if (mb == 0 && j == 0) row_ok_s[row] = g.ok ? 1.f : 0.f;
         dequant_block(fp8, g, scale2, mb, row, j, kv_base);
-        tc::fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kBarKvFull + mb]);
       }
+      // One hand-off per tile: the QK MMAs are issued once the whole tile is
+      // in place, so per-block fences and arrives would only lengthen the
+      // dequant chain.
+      tc::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarKvFull]);
       first = false;
       prefetch(cn2, sid_n2);
       cu = cn;
@@ -467,7 +470,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     const uint64_t dB_qk = tc::sdesc(q_base, 16, 1024, tc::kSwz128);
     const uint64_t dA_pv = tc::sdesc(kv_base, 16384, 1024, tc::kSwz128);
     const uint64_t dB_pv = tc::sdesc(p_base, Cfg::kPBytes, 8 * Cfg::kPRow, Cfg::kPSwz);
-    uint32_t ph_s = 0, ph_kv[4] = {0, 0, 0, 0}, ph_of = 0, sord = 0;
+    uint32_t ph_s = 0, ph_kv = 0, ph_of = 0, sord = 0;
     float l_reg[NH];              // per-head partial sums of this row
     const float4 *m_s4 = reinterpret_cast<const float4 *>(m_s) + half * (NH / 4);
     float headf = 0.f;            // scale * log2(e) * 2^e of the token's Q prescale
@@ -635,11 +638,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       if (!cursor_live(p, cu)) continue;
       seg_worked = true;
       // ---- S = K . Q^T over the whole tile: the MMAs go out back to back
-      // once all four 128-dim blocks have landed (in steady state they have
-      // by the time the previous tile's PV is issued), which keeps the
-      // issue loop free of waits and warp syncs.
+      // once the producers have landed all of it, which keeps the issue
+      // loop free of waits and warp syncs (an mbarrier access of the issuing
+      // thread stalls its issue while earlier MMAs stream operands).
       if (warp == 0) {
-        for (int mb = 0; mb < 4; ++mb) wait(kBarKvFull + mb, ph_kv[mb]);
+        wait(kBarKvFull, ph_kv);
         tc::tc_fence_after();
         if (issuer && !*abort_s) {
 #pragma unroll
@@ -657,7 +660,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         __syncwarp();
       } else {
         // the row flags are written with block 0 of the tile
-        wait(kBarKvFull, ph_kv[0]);
+        wait(kBarKvFull, ph_kv);
       }
       const bool rv = row_ok_s[prow] != 0.f;
       wait(kBarSFull, ph_s);
