@@ -665,22 +665,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const bool rv = row_ok_s[prow] != 0.f;
       wait(kBarSFull, ph_s);
       tc::tc_fence_after();
-      float x[NH];
-      if constexpr (NH % 32 == 0) {
+      // S of this thread's row and head half (TMEM -> registers)
+      auto load_s = [&](float (&v)[NH]) {
+        if constexpr (NH % 32 == 0) {
 #pragma unroll
-        for (int g32 = 0; g32 < NH / 32; ++g32) {
-          const uint32_t c = tl_lane + Cfg::kColS + half * NH + 32 * g32;
-          uint32_t a[16], b[16];
-          tc::tmem_ld16x2(c, c + 16, a, b);
+          for (int g32 = 0; g32 < NH / 32; ++g32) {
+            const uint32_t c = tl_lane + Cfg::kColS + half * NH + 32 * g32;
+            uint32_t a[16], b[16];
+            tc::tmem_ld16x2(c, c + 16, a, b);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            x[32 * g32 + i] = __uint_as_float(a[i]);
-            x[32 * g32 + 16 + i] = __uint_as_float(b[i]);
+            for (int i = 0; i < 16; ++i) {
+              v[32 * g32 + i] = __uint_as_float(a[i]);
+              v[32 * g32 + 16 + i] = __uint_as_float(b[i]);
+            }
           }
+        } else {
+          tc::tmem_ld<NH>(tl_lane + Cfg::kColS + half * NH, v);
         }
-      } else {
-        tc::tmem_ld<NH>(tl_lane + Cfg::kColS + half * NH, x);
-      }
+      };
+      // P as f16, MN-major [128 rows, HPG]
+      auto store_p = [&](const float (&v)[NH]) {
+#pragma unroll
+        for (int k = 0; k < NH / 8; ++k) {
+          uint32_t pw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pw[e] = tc::pack_f16x2(v[8 * k + 2 * e], v[8 * k + 2 * e + 1]);
+          const int ci = half * (NH / 8) + k;
+          tc::st_shared_v4(p_base + p_off<HPG>(prow, ci), pw[0], pw[1], pw[2], pw[3]);
+        }
+      };
+      float x[NH];
+      load_s(x);
+      // Scores and, against the current running max, P -- optimistically:
+      // the max moves on only when a score passes it by kRescaleSlack (a few
+      // tiles per token), and then the whole group redoes P below.
       bool need = false;
 #pragma unroll
       for (int g4 = 0; g4 < NH / 4; ++g4) {
@@ -689,12 +707,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float &xv = x[4 * g4 + i];
-          xv = rv ? xv * headf : -INFINITY;
-          need |= xv > mm[i] + kRescaleSlack;
+          const float xs = rv ? xv * headf : -INFINITY;
+          need |= xs > mm[i] + kRescaleSlack;
+          xv = (xs == -INFINITY) ? 0.f : tc::ex2(xs - mm[i]);
         }
       }
+      store_p(x);
+      tc::fence_async_smem();
+      tc::tc_fence_before();
       if (sm_bar_or(need ? 1 : 0)) {
-        // Raise the running max to the tile max; rescale sums and O.
+        // Raise the running max to the tile max; rescale sums and O; redo P.
+        tc::tc_fence_after();
+        load_s(x);
+#pragma unroll
+        for (int j = 0; j < NH; ++j) x[j] = rv ? x[j] * headf : -INFINITY;
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
           float v = x[j];
@@ -727,31 +753,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
             }
           }
         }
-        sm_bar();   // red_s free again before the next use
-      }
-      // P = 2^(x - m) (<= 2^8) as f16, MN-major [128 rows, HPG]
 #pragma unroll
-      for (int g4 = 0; g4 < NH / 4; ++g4) {
-        const float4 m4 = m_s4[g4];
-        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+        for (int g4 = 0; g4 < NH / 4; ++g4) {
+          const float4 m4 = m_s4[g4];
+          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float &xv = x[4 * g4 + i];
-          xv = (xv == -INFINITY) ? 0.f : tc::ex2(xv - mm[i]);
-          l_reg[4 * g4 + i] += xv;
+          for (int i = 0; i < 4; ++i) {
+            float &xv = x[4 * g4 + i];
+            xv = (xv == -INFINITY) ? 0.f : tc::ex2(xv - mm[i]);
+          }
         }
+        store_p(x);
+        tc::fence_async_smem();
+        tc::tc_fence_before();
+        sm_bar();   // P, O and red_s settled before PV
       }
 #pragma unroll
-      for (int k = 0; k < NH / 8; ++k) {
-        uint32_t pw[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pw[e] = tc::pack_f16x2(x[8 * k + 2 * e], x[8 * k + 2 * e + 1]);
-        const int ci = half * (NH / 8) + k;
-        tc::st_shared_v4(p_base + p_off<HPG>(prow, ci), pw[0], pw[1], pw[2], pw[3]);
-      }
-      tc::fence_async_smem();
-      tc::tc_fence_before();
-      sm_bar();   // P written by the whole group
+      for (int j = 0; j < NH; ++j) l_reg[j] += x[j];
       // ---- O^T += K^T . P
       if (issuer && !*abort_s) {
         tc::tc_fence_after();
