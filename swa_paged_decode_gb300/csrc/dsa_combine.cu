@@ -11,16 +11,20 @@
 // FlashMLA's sparse_decode.h runs the same merge as a separate combine launch
 // over o_accum / lse_accum.
 //
-// Grid: one block per (CTA boundary, head group). Boundary b (1 <= b < C)
-// falls inside token t = b*upc / tpt; the block works only when b is the
-// first boundary inside that token, so every split token is merged once.
+// Grid: x = one block per (CTA boundary, head group), y = chunks of 8 heads.
+// Boundary b (1 <= b < C) falls inside token t = b*upc / tpt; the blocks of
+// b work only when b is the first boundary inside that token, so every split
+// token is merged once, by hpg/8 blocks per head group. A block first turns
+// the parts' lse into weights in shared memory, then streams the partial O.
 #include "dsa_internal.cuh"
 
 namespace dsa {
 
 constexpr int kCombineThreads = 256;
+constexpr int kCombineHeads = 8;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
+  extern __shared__ float cs[];   // w[nparts][kCombineHeads], then inv[kCombineHeads]
   const int hg = blockIdx.x % p.HG;
   const int b = 1 + blockIdx.x / p.HG;
   const int64_t ub = (int64_t)b * p.upc;
@@ -30,14 +34,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   if (b > 1 && (int64_t)(b - 1) * p.upc > ts) return;    // not the first boundary in t
   const int32_t c0 = (int32_t)(ts / p.upc);
   const int32_t c1 = (int32_t)((ts + p.tpt - 1) / p.upc);
-  const int hpg = p.hpg, h0 = hg * hpg;
+  const int np = c1 - c0 + 1;
+  const int hpg = p.hpg, h0 = hg * hpg, hb = blockIdx.y * kCombineHeads;
   const int64_t slot_base = (int64_t)hg * 2 * p.C;
+  // Partial slot of CTA c for token t: 2c when t is the CTA's first token,
+  // else 2c + 1 (only the first CTA of the token can start in an earlier one).
+  const bool c0_late = (int64_t)c0 * p.upc < ts;
+  auto slot_of = [&](int32_t c) -> int64_t { return 2 * (int64_t)c + ((c == c0 && c0_late) ? 1 : 0); };
+  float *w_s = cs;
+  float *inv_s = cs + np * kCombineHeads;
+  const int tid = threadIdx.x;
 
-  // Row-selection record: sum of the parts (head group 0).
-  if (hg == 0 && threadIdx.x == 0) {
+  // Row-selection record: sum of the parts (one block per token).
+  if (hg == 0 && blockIdx.y == 0 && tid == 0) {
     uint32_t k = 0, s = 0;
     for (int32_t c = c0; c <= c1; ++c) {
-      const int32_t slot = 2 * c + (t == (int32_t)(cta_unit_begin(p, c) / p.tpt) ? 0 : 1);
+      const int64_t slot = slot_of(c);
       k += (uint32_t)p.part_sel[2 * slot];
       s += (uint32_t)p.part_sel[2 * slot + 1];
     }
@@ -45,48 +57,61 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
     p.sel[2 * (int64_t)t + 1] = (int32_t)s;
   }
 
-  // Each thread: one head h and 4 consecutive dims per pass.
-  for (int e = threadIdx.x; e < hpg * (kD / 4); e += kCombineThreads) {
-    const int h = e / (kD / 4), d4 = e % (kD / 4);
-    float mx = -INFINITY;
-    for (int32_t c = c0; c <= c1; ++c) {
-      const int32_t slot = 2 * c + (t == (int32_t)(cta_unit_begin(p, c) / p.tpt) ? 0 : 1);
-      mx = fmaxf(mx, p.part_lse[(slot_base + slot) * hpg + h]);
-    }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // lse of every (part, head) of the chunk
+  for (int i = tid; i < np * kCombineHeads; i += kCombineThreads) {
+    const int q = i / kCombineHeads, h = i % kCombineHeads;
+    w_s[i] = p.part_lse[(slot_base + slot_of(c0 + q)) * hpg + hb + h];
+  }
+  __syncthreads();
+  // per head: M = max_i lse_i, w_i = e^{lse_i - M}, z = sum_i w_i
+  float mx = -INFINITY;
+  if (tid < kCombineHeads)
+    for (int q = 0; q < np; ++q) mx = fmaxf(mx, w_s[q * kCombineHeads + tid]);
+  __syncthreads();
+  if (tid < kCombineHeads) {
     float z = 0.f;
-    if (mx != -INFINITY) {
-      for (int32_t c = c0; c <= c1; ++c) {
-        const int32_t slot = 2 * c + (t == (int32_t)(cta_unit_begin(p, c) / p.tpt) ? 0 : 1);
-        const float li = p.part_lse[(slot_base + slot) * hpg + h];
-        if (li == -INFINITY) continue;
-        const float w = expf(li - mx);
-        const float4 o = reinterpret_cast<const float4 *>(
-            p.part_o + ((slot_base + slot) * hpg + h) * kD)[d4];
-        z += w;
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
-      }
+    for (int q = 0; q < np; ++q) {
+      const float li = w_s[q * kCombineHeads + tid];
+      const float w = (li == -INFINITY) ? 0.f : expf(li - mx);
+      w_s[q * kCombineHeads + tid] = w;
+      z += w;
     }
     float inv = 0.f;
     if (z > 0.f) {
       float den = z;
       if (p.sink) {
-        const float sk = __ldg(p.sink + h0 + h);
+        const float sk = __ldg(p.sink + h0 + hb + tid);
         den = (sk == INFINITY) ? INFINITY : z + expf(sk - mx);
       }
       inv = 1.f / den;
     }
-    __nv_bfloat16 *o = p.out + ((int64_t)t * p.H + h0 + h) * kD + 4 * d4;
+    inv_s[tid] = inv;
+    p.lse[(int64_t)t * p.H + h0 + hb + tid] = (z > 0.f) ? mx + logf(z) : -INFINITY;
+  }
+  __syncthreads();
+
+  // out = sum_i w_i O_i * inv: one head and 4 consecutive dims per item
+  for (int e = tid; e < kCombineHeads * (kD / 4); e += kCombineThreads) {
+    const int h = e / (kD / 4), d4 = e % (kD / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < np; ++q) {
+      const float w = w_s[q * kCombineHeads + h];
+      if (w == 0.f) continue;
+      const float4 o = reinterpret_cast<const float4 *>(
+          p.part_o + ((slot_base + slot_of(c0 + q)) * hpg + hb + h) * kD)[d4];
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+    }
+    const float inv = inv_s[h];
+    __nv_bfloat16 *o = p.out + ((int64_t)t * p.H + h0 + hb + h) * kD + 4 * d4;
     __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
     __nv_bfloat162 c2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
     uint2 pk;
     pk.x = *reinterpret_cast<uint32_t *>(&a);
     pk.y = *reinterpret_cast<uint32_t *>(&c2);
     *reinterpret_cast<uint2 *>(o) = pk;
-    if (d4 == 0) p.lse[(int64_t)t * p.H + h0 + h] = (z > 0.f) ? mx + logf(z) : -INFINITY;
   }
 }
 
@@ -95,7 +120,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
 cudaError_t dsa_launch_combine(const dsa::Params &p, cudaStream_t stream) {
   using namespace dsa;
   if (p.C <= 1) return cudaSuccess;
-  const dim3 grid((unsigned)((p.C - 1) * p.HG)), block(kCombineThreads);
-  combine_kernel<<<grid, block, 0, stream>>>(p);
+  // A token spans at most min(C, tpt + 1) CTAs.
+  const int64_t np_max = p.C < (int64_t)p.tpt + 1 ? p.C : (int64_t)p.tpt + 1;
+  const size_t smem = (size_t)(np_max + 1) * kCombineHeads * sizeof(float);
+  if (smem > 48 * 1024) {
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    const cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid((unsigned)((p.C - 1) * p.HG), (unsigned)(p.hpg / kCombineHeads)), block(kCombineThreads);
+  combine_kernel<<<grid, block, smem, stream>>>(p);
   return cudaGetLastError();
 }
