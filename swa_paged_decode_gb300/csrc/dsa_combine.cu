@@ -22,6 +22,7 @@ namespace dsa {
 
 constexpr int kCombineThreads = 256;
 constexpr int kCombineHeads = 8;
+constexpr int kCombineUnroll = 4;   // parts whose partial O loads are in flight together
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   extern __shared__ float cs[];   // w[nparts][kCombineHeads], then inv[kCombineHeads]
@@ -90,24 +91,49 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   }
   __syncthreads();
 
-  // out = sum_i w_i O_i * inv: one head and 4 consecutive dims per item
-  for (int e = tid; e < kCombineHeads * (kD / 4); e += kCombineThreads) {
-    const int h = e / (kD / 4), d4 = e % (kD / 4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < np; ++q) {
-      const float w = w_s[q * kCombineHeads + h];
-      if (w == 0.f) continue;
-      const float4 o = reinterpret_cast<const float4 *>(
-          p.part_o + ((slot_base + slot_of(c0 + q)) * hpg + hb + h) * kD)[d4];
-      acc.x = fmaf(w, o.x, acc.x);
-      acc.y = fmaf(w, o.y, acc.y);
-      acc.z = fmaf(w, o.z, acc.z);
-      acc.w = fmaf(w, o.w, acc.w);
+  // out = sum_i w_i O_i * inv. Thread: four items (one head, 4 consecutive
+  // dims each); the loads of kCombineUnroll parts are issued before use.
+  constexpr int kItems = kCombineHeads * (kD / 4) / kCombineThreads;
+  static_assert(kItems * kCombineThreads == kCombineHeads * (kD / 4), "items per thread");
+  float4 acc[kItems];
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q0 = 0; q0 < np; q0 += kCombineUnroll) {
+    float4 o[kCombineUnroll][kItems];
+#pragma unroll
+    for (int u = 0; u < kCombineUnroll; ++u) {
+      const int q = q0 + u;
+#pragma unroll
+      for (int k = 0; k < kItems; ++k) {
+        const int e = tid + k * kCombineThreads, h = e / (kD / 4), d4 = e % (kD / 4);
+        o[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (q < np && w_s[q * kCombineHeads + h] != 0.f)
+          o[u][k] = __ldg(reinterpret_cast<const float4 *>(
+              p.part_o + ((slot_base + slot_of(c0 + q)) * hpg + hb + h) * kD) + d4);
+      }
     }
+#pragma unroll
+    for (int u = 0; u < kCombineUnroll; ++u) {
+      const int q = q0 + u;
+#pragma unroll
+      for (int k = 0; k < kItems; ++k) {
+        const int h = (tid + k * kCombineThreads) / (kD / 4);
+        const float w = q < np ? w_s[q * kCombineHeads + h] : 0.f;
+        if (w == 0.f) continue;
+        acc[k].x = fmaf(w, o[u][k].x, acc[k].x);
+        acc[k].y = fmaf(w, o[u][k].y, acc[k].y);
+        acc[k].z = fmaf(w, o[u][k].z, acc[k].z);
+        acc[k].w = fmaf(w, o[u][k].w, acc[k].w);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const int e = tid + k * kCombineThreads, h = e / (kD / 4), d4 = e % (kD / 4);
     const float inv = inv_s[h];
     __nv_bfloat16 *o = p.out + ((int64_t)t * p.H + h0 + hb + h) * kD + 4 * d4;
-    __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 c2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
+    __nv_bfloat162 c2 = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
     uint2 pk;
     pk.x = *reinterpret_cast<uint32_t *>(&a);
     pk.y = *reinterpret_cast<uint32_t *>(&c2);
