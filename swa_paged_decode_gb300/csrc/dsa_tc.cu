@@ -330,6 +330,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   const uint32_t p_base = sbase + Cfg::kP;
   float *row_ok_s = reinterpret_cast<float *>(smem + Cfg::kRho);
   float *m_s = reinterpret_cast<float *>(smem + Cfg::kM);
+  float *headf_s = reinterpret_cast<float *>(smem + Cfg::kHeadF);
   float *red_s = reinterpret_cast<float *>(smem + Cfg::kRed);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kMisc);
   volatile int32_t *abort_s = reinterpret_cast<volatile int32_t *>(smem + Cfg::kMisc + kMiscAbort);
@@ -473,75 +474,75 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     uint32_t ph_s = 0, ph_kv = 0, ph_of = 0, sord = 0;
     float l_reg[NH];              // per-head partial sums of this row
     const float4 *m_s4 = reinterpret_cast<const float4 *>(m_s) + half * (NH / 4);
-    float headf = 0.f;            // scale * log2(e) * 2^e of the token's Q prescale
+    // per head: scale * log2(e) * 2^e, e the exponent of the head's Q prescale
+    const float4 *hf_s4 = reinterpret_cast<const float4 *>(headf_s) + half * (NH / 4);
     int32_t cur_t = -1;
     bool seg_worked = false, first_pv = true;
 
-    // Q of token t -> f16 K-major SW128 tile. RoPE (NeoX) in fp32, then one
-    // power-of-two prescale for the whole token so max |q| lies in [1, 2):
-    // exact for bf16 inputs whose exponents fit f16's range after scaling.
-    auto load_q = [&](int32_t t, int h, int64_t pos, float (&v)[16]) {
-      const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)(h0 + h) * p.q_sh;
-      const uint4 a = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane);
-      const uint4 b = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane + 1);
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-        v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-      }
-      if (p.cos_sin) {   // NeoX: dim 448+i pairs with 480+i; lanes 28..31 hold 448..511
-        const float *cs = p.cos_sin + pos * 64;
-        const bool rope = lane >= 28;
-        const bool firsth = lane < 30;
-        const int i0 = (lane & 1) * 16;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float other = __shfl_xor_sync(0xffffffffu, v[k], 2);
-          if (rope) {
-            const float c = __ldg(cs + i0 + k), s = __ldg(cs + kRopeHalf + i0 + k);
-            v[k] = firsth ? (v[k] * c - other * s) : (v[k] * c + other * s);
-          }
-        }
-      }
-    };
+    // Q of token t -> f16 K-major SW128 tile. RoPE (NeoX) in fp32, then a
+    // power-of-two prescale per head so its max |q| lies in [1, 2): exact
+    // for bf16 inputs whose exponents fit f16's range after scaling; the
+    // factor goes to headf_s. Each warp stages heads warp, warp + 8, ...:
+    // all their loads are issued first (one round trip), then each head is
+    // rotated, reduced and stored without any cross-warp step.
+    static_assert(HPG % kSmWarps == 0, "heads per softmax warp");
+    constexpr int kQH = HPG / kSmWarps;
     auto stage_q = [&](int32_t t) {
       int64_t pos = p.positions ? __ldg(p.positions + t) : 0;
       if (pos < 0 || (p.cos_sin && pos >= p.cs_rows)) {   // outside the table: flag, row 0
         if (tid == 0) report_status(p.status, DSA_ERR_INVALID_ARG);
         pos = 0;
       }
-      for (int h = warp; h < HPG; h += kSmWarps) {
+      uint4 qa[kQH], qb[kQH];
+#pragma unroll
+      for (int i = 0; i < kQH; ++i) {
+        const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)(h0 + warp + kSmWarps * i) * p.q_sh;
+        qa[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane);
+        qb[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane + 1);
+      }
+      // NeoX: dim 448+i pairs with 480+i; lanes 28..31 hold dims 448..511
+      const bool rope = p.cos_sin != nullptr;
+      const bool rlane = rope && lane >= 28, firsth = lane < 30;
+      const float *cs = p.cos_sin + (rope ? pos * 64 + (lane & 1) * 16 : 0);
+#pragma unroll
+      for (int i = 0; i < kQH; ++i) {
+        const int h = warp + kSmWarps * i;
+        const uint32_t w[8] = {qa[i].x, qa[i].y, qa[i].z, qa[i].w, qb[i].x, qb[i].y, qb[i].z, qb[i].w};
         float v[16];
-        load_q(t, h, pos, v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          v[2 * k] = bf16_bits_to_f32(w[k] & 0xFFFFu);
+          v[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
+        }
+        if (rope) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[k], 2);
+            if (rlane) {   // the row stays in L1 across the heads
+              const float c = __ldg(cs + k), sn = __ldg(cs + kRopeHalf + k);
+              v[k] = firsth ? (v[k] * c - other * sn) : (v[k] * c + other * sn);
+            }
+          }
+        }
         float mx = 0.f;
 #pragma unroll
         for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(v[k]));
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        if (lane == 0) red_s[h] = mx;
-      }
-      sm_bar();
-      float mx = 0.f;
-      for (int h = 0; h < HPG; ++h) mx = fmaxf(mx, red_s[h]);
-      int e = (mx > 0.f) ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
-      e = e < -126 ? -126 : (e > 126 ? 126 : e);
-      const float down = __uint_as_float((uint32_t)(127 - e) << 23);
-      headf = p.scale_log2 * __uint_as_float((uint32_t)(127 + e) << 23);
-      for (int h = warp; h < HPG; h += kSmWarps) {
-        float v[16];
-        load_q(t, h, pos, v);
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        int e = (mx > 0.f) ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+        e = e < -126 ? -126 : (e > 126 ? 126 : e);
+        const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+        if (lane == 0) headf_s[h] = p.scale_log2 * __uint_as_float((uint32_t)(127 + e) << 23);
         uint32_t f[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = tc::pack_f16x2(v[2 * i] * down, v[2 * i + 1] * down);
+        for (int k = 0; k < 8; ++k) f[k] = tc::pack_f16x2(v[2 * k] * down, v[2 * k + 1] * down);
         const int kb = lane >> 2, ci = (lane & 3) * 2;
         tc::st_shared_v4(q_base + sw128_off(h, kb, ci, HPG * 128), f[0], f[1], f[2], f[3]);
         tc::st_shared_v4(q_base + sw128_off(h, kb, ci + 1, HPG * 128), f[4], f[5], f[6], f[7]);
       }
       if (tid < HPG) m_s[tid] = -INFINITY;
       tc::fence_async_smem();
-      sm_bar();   // Q (async proxy) and m_s visible; red_s free again
+      sm_bar();   // Q (async proxy), head factors and m_s visible
     };
 
     // Token finished: sums over rows, sink, out / lse (or partial), selection.
@@ -702,12 +703,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       bool need = false;
 #pragma unroll
       for (int g4 = 0; g4 < NH / 4; ++g4) {
-        const float4 m4 = m_s4[g4];
-        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+        const float4 m4 = m_s4[g4], f4 = hf_s4[g4];
+        const float mm[4] = {m4.x, m4.y, m4.z, m4.w}, hf[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float &xv = x[4 * g4 + i];
-          const float xs = rv ? xv * headf : -INFINITY;
+          const float xs = rv ? xv * hf[i] : -INFINITY;
           need |= xs > mm[i] + kRescaleSlack;
           xv = (xs == -INFINITY) ? 0.f : tc::ex2(xs - mm[i]);
         }
@@ -720,7 +721,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         tc::tc_fence_after();
         load_s(x);
 #pragma unroll
-        for (int j = 0; j < NH; ++j) x[j] = rv ? x[j] * headf : -INFINITY;
+        for (int j = 0; j < NH; ++j) x[j] = rv ? x[j] * headf_s[half * NH + j] : -INFINITY;
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
           float v = x[j];
