@@ -514,14 +514,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           v[2 * k] = bf16_bits_to_f32(w[k] & 0xFFFFu);
           v[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
         }
-        if (rope) {
+        if (rope) {   // branch-free: every lane reads a valid row entry, lanes 28..31 use it
+          float c[16], sn[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            c[k] = __ldg(cs + k);   // the row stays in L1 across the heads
+            sn[k] = __ldg(cs + kRopeHalf + k);
+          }
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             const float other = __shfl_xor_sync(0xffffffffu, v[k], 2);
-            if (rlane) {   // the row stays in L1 across the heads
-              const float c = __ldg(cs + k), sn = __ldg(cs + kRopeHalf + k);
-              v[k] = firsth ? (v[k] * c - other * sn) : (v[k] * c + other * sn);
-            }
+            const float r = firsth ? fmaf(v[k], c[k], -other * sn[k]) : fmaf(v[k], c[k], other * sn[k]);
+            v[k] = rlane ? r : v[k];
           }
         }
         float mx = 0.f;
@@ -549,13 +553,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     auto finalize = [&](const Segment &seg) {
       if (seg_worked) wait(kBarOFinal, ph_of);
       tc::tc_fence_after();
+      // Sums over the warp's 32 rows, in place (l_reg restarts at zero with
+      // the next token; it is all zeros when no tile was worked): recursive
+      // halving -- at step st a lane keeps the upper half of its 2*st values
+      // when lane bit st is set, else the lower half, and adds the partner's
+      // copy of that half -- leaves head j's sum in lane j (NH < 32: lanes j,
+      // j + NH, ... hold parts, folded by the last shuffles).
 #pragma unroll
-      for (int j = 0; j < NH; ++j) {
-        float v = seg_worked ? l_reg[j] : 0.f;
+      for (int st = NH / 2; st >= 1; st >>= 1) {
+        const bool up = (lane & st) != 0;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) red_s[q4 * 64 + half * NH + j] = v;
+        for (int i = 0; i < st; ++i) {
+          const float send = up ? l_reg[i] : l_reg[i + st];
+          const float keep = up ? l_reg[i + st] : l_reg[i];
+          l_reg[i] = keep + __shfl_xor_sync(0xffffffffu, send, st);
+        }
       }
+#pragma unroll
+      for (int off = NH; off < 32; off <<= 1) l_reg[0] += __shfl_xor_sync(0xffffffffu, l_reg[0], off);
+      if (lane < NH) red_s[q4 * 64 + half * NH + lane] = l_reg[0];
       sm_bar();
       if (tid < HPG) {   // 1 / denominator of head tid, lse
         const int h = tid;
