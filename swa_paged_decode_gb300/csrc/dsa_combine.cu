@@ -11,10 +11,11 @@
 // FlashMLA's sparse_decode.h runs the same merge as a separate combine launch
 // over o_accum / lse_accum.
 //
-// Grid: x = one block per (CTA boundary, head group), y = chunks of 8 heads.
+// Grid: x = one block per (CTA boundary, head group), y = chunks of 8 heads
+// x 4 quarters of the dims.
 // Boundary b (1 <= b < C) falls inside token t = b*upc / tpt; the blocks of
 // b work only when b is the first boundary inside that token, so every split
-// token is merged once, by hpg/8 blocks per head group. A block first turns
+// token is merged once, by hpg/2 blocks per head group. A block first turns
 // the parts' lse into weights in shared memory, then streams the partial O.
 #include "dsa_internal.cuh"
 
@@ -22,7 +23,8 @@ namespace dsa {
 
 constexpr int kCombineThreads = 256;
 constexpr int kCombineHeads = 8;
-constexpr int kCombineUnroll = 4;   // parts whose partial O loads are in flight together
+constexpr int kCombineUnroll = 8;   // parts whose partial O loads are in flight together
+constexpr int kCombineQuarters = 4; // blocks per head chunk, one per quarter of the 512 dims
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   extern __shared__ float cs[];   // w[nparts][kCombineHeads], then inv[kCombineHeads]
@@ -36,7 +38,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   const int32_t c0 = (int32_t)(ts / p.upc);
   const int32_t c1 = (int32_t)((ts + p.tpt - 1) / p.upc);
   const int np = c1 - c0 + 1;
-  const int hpg = p.hpg, h0 = hg * hpg, hb = blockIdx.y * kCombineHeads;
+  const int hpg = p.hpg, h0 = hg * hpg, hb = (blockIdx.y / kCombineQuarters) * kCombineHeads;
+  const int dq = (blockIdx.y % kCombineQuarters) * (kD / 4 / kCombineQuarters);   // first float4 of the quarter
   const int64_t slot_base = (int64_t)hg * 2 * p.C;
   // Partial slot of CTA c for token t: 2c when t is the CTA's first token,
   // else 2c + 1 (only the first CTA of the token can start in an earlier one).
@@ -47,7 +50,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   const int tid = threadIdx.x;
 
   // Row-selection record: sum of the parts (one block per token).
-  if (hg == 0 && blockIdx.y == 0 && tid == 0) {
+  if (hg == 0 && blockIdx.y == 0 && tid == 0) {   // one block of the token
     uint32_t k = 0, s = 0;
     for (int32_t c = c0; c <= c1; ++c) {
       const int64_t slot = slot_of(c);
@@ -87,14 +90,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
       inv = 1.f / den;
     }
     inv_s[tid] = inv;
-    p.lse[(int64_t)t * p.H + h0 + hb + tid] = (z > 0.f) ? mx + logf(z) : -INFINITY;
+    if (dq == 0) p.lse[(int64_t)t * p.H + h0 + hb + tid] = (z > 0.f) ? mx + logf(z) : -INFINITY;
   }
   __syncthreads();
 
-  // out = sum_i w_i O_i * inv. Thread: four items (one head, 4 consecutive
-  // dims each); the loads of kCombineUnroll parts are issued before use.
-  constexpr int kItems = kCombineHeads * (kD / 4) / kCombineThreads;
-  static_assert(kItems * kCombineThreads == kCombineHeads * (kD / 4), "items per thread");
+  // out = sum_i w_i O_i * inv. Thread: one item (one head, 4 consecutive
+  // dims of the block's quarter); the loads of kCombineUnroll parts are
+  // issued before use.
+  constexpr int kQ4 = kD / 4 / kCombineQuarters;   // float4s per head in a quarter
+  constexpr int kItems = kCombineHeads * kQ4 / kCombineThreads;
+  static_assert(kItems * kCombineThreads == kCombineHeads * kQ4, "items per thread");
   float4 acc[kItems];
 #pragma unroll
   for (int k = 0; k < kItems; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -105,7 +110,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
       const int q = q0 + u;
 #pragma unroll
       for (int k = 0; k < kItems; ++k) {
-        const int e = tid + k * kCombineThreads, h = e / (kD / 4), d4 = e % (kD / 4);
+        const int e = tid + k * kCombineThreads, h = e / kQ4, d4 = dq + e % kQ4;
         o[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (q < np && w_s[q * kCombineHeads + h] != 0.f)
           o[u][k] = __ldg(reinterpret_cast<const float4 *>(
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
       const int q = q0 + u;
 #pragma unroll
       for (int k = 0; k < kItems; ++k) {
-        const int h = (tid + k * kCombineThreads) / (kD / 4);
+        const int h = (tid + k * kCombineThreads) / kQ4;
         const float w = q < np ? w_s[q * kCombineHeads + h] : 0.f;
         if (w == 0.f) continue;
         acc[k].x = fmaf(w, o[u][k].x, acc[k].x);
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   }
 #pragma unroll
   for (int k = 0; k < kItems; ++k) {
-    const int e = tid + k * kCombineThreads, h = e / (kD / 4), d4 = e % (kD / 4);
+    const int e = tid + k * kCombineThreads, h = e / kQ4, d4 = dq + e % kQ4;
     const float inv = inv_s[h];
     __nv_bfloat16 *o = p.out + ((int64_t)t * p.H + h0 + hb + h) * kD + 4 * d4;
     __nv_bfloat162 a = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
@@ -155,7 +160,8 @@ cudaError_t dsa_launch_combine(const dsa::Params &p, cudaStream_t stream) {
                                                (int)smem);
     if (e != cudaSuccess) return e;
   }
-  const dim3 grid((unsigned)((p.C - 1) * p.HG), (unsigned)(p.hpg / kCombineHeads)), block(kCombineThreads);
+  const dim3 grid((unsigned)((p.C - 1) * p.HG), (unsigned)(p.hpg / kCombineHeads * kCombineQuarters)),
+      block(kCombineThreads);
   combine_kernel<<<grid, block, smem, stream>>>(p);
   return cudaGetLastError();
 }
