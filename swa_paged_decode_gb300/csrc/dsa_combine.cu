@@ -28,6 +28,7 @@ constexpr int kCombineQuarters = 4; // blocks per head chunk, one per quarter of
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   extern __shared__ float cs[];   // w[nparts][kCombineHeads], then inv[kCombineHeads]
+  pdl_wait_primary();   // the decode kernel's partials are complete and visible
   const int hg = blockIdx.x % p.HG;
   const int b = 1 + blockIdx.x / p.HG;
   const int64_t ub = (int64_t)b * p.upc;
@@ -162,6 +163,17 @@ cudaError_t dsa_launch_combine(const dsa::Params &p, cudaStream_t stream) {
   }
   const dim3 grid((unsigned)((p.C - 1) * p.HG), (unsigned)(p.hpg / kCombineHeads * kCombineQuarters)),
       block(kCombineThreads);
-  combine_kernel<<<grid, block, smem, stream>>>(p);
-  return cudaGetLastError();
+  // Launched as a programmatic dependent of the decode kernel before it on
+  // the stream: its blocks may be scheduled while that kernel drains.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }

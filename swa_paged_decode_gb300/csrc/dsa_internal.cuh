@@ -159,6 +159,16 @@ __device__ inline float e2m1_to_f32(uint32_t nib) {
   return (nib & 0x8u) ? -mag : mag;
 }
 
+// Programmatic dependent launch: the decode kernels let the combine grid be
+// scheduled early; the combine kernel waits for their completion (and
+// memory) before reading the partials.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ inline float bf16_bits_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }

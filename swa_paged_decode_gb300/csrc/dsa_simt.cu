@@ -87,6 +87,7 @@ __device__ void load_subtile(const Params &p, SimtSmem &sm, int32_t lid, int32_t
 
 template <int HPG>
 __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) {
+  pdl_launch_dependents();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtSmem &sm = *reinterpret_cast<SimtSmem *>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
