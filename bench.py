@@ -223,47 +223,68 @@ def e2e_steps(w: W.Workload, B, steps: int, warmup: int, flush: torch.Tensor):
     """Same step through the public API from pinned HOST buffers: per step the
     per-token inputs (Q, slot lists, lengths, positions) go host->device and
     out + lse come back device->host inside the timed region. The caches and
-    the sink (model state) stay resident."""
-    host = {}
+    the sink (model state) stay resident.
+
+    Steps are double-buffered as a serving loop runs them: step k's inputs
+    are copied on one copy stream while step k-1 computes, and step k-1's
+    result is copied back on another; two sets of device buffers alternate.
+    The timed region spans all `steps` steps, from the first copy in to the
+    last copy out."""
     names = ["q", "swa_ids", "swa_lens"] + (["extra_ids", "extra_lens"] if w.extra is not None else []) \
         + (["positions"] if w.positions is not None else [])
     src = {"q": w.q, "swa_ids": w.swa.ids, "swa_lens": w.swa.lens,
            "extra_ids": None if w.extra is None else w.extra.ids,
            "extra_lens": None if w.extra is None else w.extra.lens, "positions": w.positions}
-    dev = {}
-    for n in names:
-        host[n] = src[n].cpu().pin_memory()
-        dev[n] = torch.empty_like(src[n])
+    host = {n: src[n].cpu().pin_memory() for n in names}
     dec = B.Decoder(w)
-    out_h = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
-    lse_h = torch.empty(dec.lse.shape, dtype=dec.lse.dtype).pin_memory()
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    E = lambda: torch.cuda.Event()
+    sets = []
+    for _ in range(2):
+        sets.append({"dev": {n: torch.empty_like(src[n]) for n in names},
+                     "out": torch.empty_like(dec.out), "lse": torch.empty_like(dec.lse),
+                     "out_h": torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory(),
+                     "lse_h": torch.empty(dec.lse.shape, dtype=dec.lse.dtype).pin_memory(),
+                     "in_ready": E(), "comp_done": E(), "out_done": E(), "used": False})
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    d2h = dec.out.numel() * 2 + dec.lse.numel() * 4
 
-    def one():
-        for n in names:
-            dev[n].copy_(host[n], non_blocking=True)
-        B.dsa_decode_run(dec.plan, dec.workspace, dev["q"], w.swa_cache, dev["swa_ids"],
-                         dev["swa_lens"], w.extra_cache, dev.get("extra_ids"), dev.get("extra_lens"),
-                         w.sink, dev.get("positions"), w.cos_sin, w.scale, dec.out, dec.lse)
-        B.dsa_decode_combine(dec.plan, dec.workspace, w.sink, dec.out, dec.lse)
-        out_h.copy_(dec.out, non_blocking=True)
-        lse_h.copy_(dec.lse, non_blocking=True)
-
-    for _ in range(warmup):
+    def step(k):
+        b = sets[k % 2]
+        if b["used"]:                       # its previous result has been read back
+            s_in.wait_event(b["out_done"])
+        b["used"] = True
+        with torch.cuda.stream(s_in):
+            for n in names:
+                b["dev"][n].copy_(host[n], non_blocking=True)
+            b["in_ready"].record(s_in)
+        comp.wait_event(b["in_ready"])
         flush.zero_()
-        one()
+        d = b["dev"]
+        B.dsa_decode_run(dec.plan, dec.workspace, d["q"], w.swa_cache, d["swa_ids"],
+                         d["swa_lens"], w.extra_cache, d.get("extra_ids"), d.get("extra_lens"),
+                         w.sink, d.get("positions"), w.cos_sin, w.scale, b["out"], b["lse"], comp)
+        B.dsa_decode_combine(dec.plan, dec.workspace, w.sink, b["out"], b["lse"], comp)
+        b["comp_done"].record(comp)
+        s_out.wait_event(b["comp_done"])
+        with torch.cuda.stream(s_out):
+            b["out_h"].copy_(b["out"], non_blocking=True)
+            b["lse_h"].copy_(b["lse"], non_blocking=True)
+            b["out_done"].record(s_out)
+
+    for k in range(warmup):
+        step(k)
     torch.cuda.synchronize()
-    total = 0.0
-    for _ in range(steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        one()
-        b.record()
-        b.synchronize()
-        total += a.elapsed_time(b)
-    return total, h2d, d2h
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    s_in.wait_stream(comp)
+    for k in range(steps):
+        step(k)
+    comp.wait_stream(s_out)
+    e.record(comp)
+    e.synchronize()
+    return a.elapsed_time(e), h2d, d2h
 
 
 def roofline(w: W.Workload, alg, kern_ms_avg: float, peaks, peak_kind):
