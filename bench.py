@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # while the kernel sources hash to `sources`. The capture is summarised under
 # profiles/ with the command that made it.
 NCU_TRAFFIC = {
-    "sources": "e6bc37e7a086fbd0",
+    "sources": "b026673f8f112022",
     "workload": "config5_T256_H64",
     "bytes_per_launch": 447782400 + 27637760,
     "rows_per_launch": 256 * (128 + 4096),
@@ -191,10 +191,30 @@ class Step:
         B.dsa_decode_combine(d.plan, d.workspace, w.sink, d.out, d.lse)
 
 
-def time_steps(step: Step, steps: int, warmup: int, flush: torch.Tensor, clocks=None):
+def rank_barrier(world: int):
+    """Barrier across the replicas (one process per GPU); no-op alone."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest replica's figure (every rank gets it)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(step: Step, steps: int, warmup: int, flush: torch.Tensor, clocks=None,
+               world: int = 1):
     for _ in range(warmup):
         flush.zero_()
         step()
+    torch.cuda.synchronize()
+    rank_barrier(world)            # all replicas start the timed region together
     torch.cuda.synchronize()
     E = lambda: torch.cuda.Event(enable_timing=True)
     evs = [(E(), E(), E(), E()) for _ in range(steps)]
@@ -206,6 +226,7 @@ def time_steps(step: Step, steps: int, warmup: int, flush: torch.Tensor, clocks=
             step(k0, k1)
             s1.record()
         torch.cuda.synchronize()
+    rank_barrier(world)
     step_ms = [a.elapsed_time(b) for a, _, _, b in evs]
     kern_ms = [a.elapsed_time(b) for _, a, b, _ in evs]
     return sum(step_ms), step_ms, kern_ms
@@ -333,12 +354,8 @@ def gpu_arm(args, rank, world, B, peaks, peak_kind):
     alg = algorithmic(w)
     step = Step(w, B)
     clocks = ClockSampler(dev.index)
-    total_ms, step_ms, kern_ms = time_steps(step, args.steps, args.warmup, flush, clocks)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, step_ms, kern_ms = time_steps(step, args.steps, args.warmup, flush, clocks, world)
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     value = w.T * world / (ms_per_step * 1e-3)
     kern_avg = sum(kern_ms) / len(kern_ms)

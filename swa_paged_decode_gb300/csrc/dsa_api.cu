@@ -9,10 +9,29 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "dsa_internal.cuh"
 
 using dsa::Params;
+
+namespace {
+constexpr int kCfgDevices = 64;
+std::mutex g_cfg_mutex;
+uint64_t g_cfg_done[kCfgDevices] = {};   // per device: bit i = variant i set up
+}  // namespace
+
+cudaError_t dsa::dsa_configure_once(int bit, cudaError_t (*f)(void *), void *arg) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kCfgDevices || bit < 0 || bit >= 64) return f(arg);
+  std::lock_guard<std::mutex> lock(g_cfg_mutex);
+  if (g_cfg_done[dev] & (1ull << bit)) return cudaSuccess;
+  e = f(arg);
+  if (e == cudaSuccess) g_cfg_done[dev] |= 1ull << bit;
+  return e;
+}
 
 namespace {
 

@@ -149,16 +149,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
 
 }  // namespace dsa
 
+namespace {
+cudaError_t combine_setup(void *) {
+  return cudaFuncSetAttribute(dsa::combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              227 * 1024);
+}
+}  // namespace
+
 cudaError_t dsa_launch_combine(const dsa::Params &p, cudaStream_t stream) {
   using namespace dsa;
   if (p.C <= 1) return cudaSuccess;
   // A token spans at most min(C, tpt + 1) CTAs.
   const int64_t np_max = p.C < (int64_t)p.tpt + 1 ? p.C : (int64_t)p.tpt + 1;
   const size_t smem = (size_t)(np_max + 1) * kCombineHeads * sizeof(float);
-  if (smem > 48 * 1024) {
+  if (smem > 48 * 1024) {   // raised once per device to the largest opt-in size
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
-    const cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem);
+    const cudaError_t e = dsa_configure_once(16, &combine_setup, nullptr);
     if (e != cudaSuccess) return e;
   }
   const dim3 grid((unsigned)((p.C - 1) * p.HG), (unsigned)(p.hpg / kCombineHeads * kCombineQuarters)),

@@ -159,6 +159,12 @@ __device__ inline float e2m1_to_f32(uint32_t nib) {
   return (nib & 0x8u) ? -mag : mag;
 }
 
+// One-time per-device kernel set-up (function attributes): `f` runs on the
+// first launch of kernel variant `bit` on the current device, later launches
+// skip it (they may be captured into a CUDA graph, where no set-up call is
+// wanted). Thread-safe.
+cudaError_t dsa_configure_once(int bit, cudaError_t (*f)(void *), void *arg);
+
 // Programmatic dependent launch: the decode kernels let the combine grid be
 // scheduled early; the combine kernel waits for their completion (and
 // memory) before reading the partials.

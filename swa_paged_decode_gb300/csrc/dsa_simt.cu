@@ -258,23 +258,30 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) 
 
 }  // namespace dsa
 
+namespace {
+template <int N>
+cudaError_t simt_setup(void *) {
+  return cudaFuncSetAttribute(dsa::simt_decode_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(dsa::SimtSmem));
+}
+}  // namespace
+
 cudaError_t dsa_launch_simt(const dsa::Params &p, cudaStream_t stream) {
   using namespace dsa;
   const size_t smem = sizeof(SimtSmem);
   const dim3 grid((unsigned)(p.C * p.HG)), block(kSimtThreads);
   cudaError_t err = cudaSuccess;
   switch (p.hpg) {
-#define DSA_SIMT_CASE(N)                                                                  \
+#define DSA_SIMT_CASE(N, BIT)                                                             \
   case N:                                                                                 \
-    err = cudaFuncSetAttribute(simt_decode_kernel<N>,                                     \
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);   \
+    err = dsa_configure_once(BIT, &simt_setup<N>, nullptr);                               \
     if (err != cudaSuccess) return err;                                                   \
     simt_decode_kernel<N><<<grid, block, smem, stream>>>(p);                              \
     break;
-    DSA_SIMT_CASE(16)
-    DSA_SIMT_CASE(32)
-    DSA_SIMT_CASE(48)
-    DSA_SIMT_CASE(64)
+    DSA_SIMT_CASE(16, 8)
+    DSA_SIMT_CASE(32, 9)
+    DSA_SIMT_CASE(48, 10)
+    DSA_SIMT_CASE(64, 11)
 #undef DSA_SIMT_CASE
     default:
       return cudaErrorInvalidValue;

@@ -826,28 +826,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 
 bool dsa_tc_supports(int hpg) { return hpg == 16 || hpg == 32 || hpg == 64; }
 
+namespace {
+// Checks that the kernel kept exactly kLaunchRegs registers per thread (the
+// warpgroup register split assumes it) and raises its shared-memory limit.
+template <int N>
+cudaError_t tc_setup(void *) {
+  using namespace dsa;
+  cudaFuncAttributes fa;
+  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N>);
+  if (err != cudaSuccess) return err;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  return cudaFuncSetAttribute(tc_decode_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)TcCfg<N>::kSmem);
+}
+}  // namespace
+
 cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
   using namespace dsa;
   const dim3 grid((unsigned)(p.C * p.HG)), block(kTcThreads);
   cudaError_t err = cudaSuccess;
   switch (p.hpg) {
-#define DSA_TC_CASE(N)                                                                   \
+#define DSA_TC_CASE(N, BIT)                                                              \
   case N: {                                                                              \
     const int smem = (int)TcCfg<N>::kSmem;                                               \
-    cudaFuncAttributes fa;                                                               \
-    err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N>);                               \
-    if (err != cudaSuccess) return err;                                                  \
-    /* the warpgroup register split assumes exactly kLaunchRegs per thread */           \
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;                 \
-    err = cudaFuncSetAttribute(tc_decode_kernel<N>,                                      \
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
+    err = dsa_configure_once(BIT, &tc_setup<N>, nullptr);                                \
     if (err != cudaSuccess) return err;                                                  \
     tc_decode_kernel<N><<<grid, block, smem, stream>>>(p);                               \
     break;                                                                               \
   }
-    DSA_TC_CASE(16)
-    DSA_TC_CASE(32)
-    DSA_TC_CASE(64)
+    DSA_TC_CASE(16, 0)
+    DSA_TC_CASE(32, 1)
+    DSA_TC_CASE(64, 2)
 #undef DSA_TC_CASE
     default:
       return cudaErrorInvalidValue;
