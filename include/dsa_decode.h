@@ -97,7 +97,7 @@ typedef struct {
   int32_t tiles_swa;       /* 128-row tiles per token in each list           */
   int32_t tiles_extra;
   int32_t tiles_per_token;
-  int32_t units_per_cta;   /* contiguous (token, tile) units per CTA         */
+  int32_t units_per_cta;   /* units per CTA of an even split (grid sizing)   */
   int32_t ctas_per_group;  /* CTAs per head group                            */
   int32_t split_tokens;    /* upper bound on tokens split over CTAs          */
   int32_t kernel;          /* internal kernel variant                        */
@@ -107,7 +107,15 @@ typedef struct {
   int64_t ws_part_sel_offset;
   int64_t ws_part_o_offset;
   int64_t workspace_bytes;
-  int64_t reserved[16];
+  int64_t ws_bounds_offset; /* int64 [ctas_per_group + 1]: CTA c owns units
+                              [bounds[c], bounds[c+1]), set by the run kernel
+                              (see balance_live; a tile is live when its first
+                              row lies below min(len, width)) and read by the
+                              combine                                       */
+  int64_t balance_live;     /* 1: CTA boundaries balance live tiles (set when
+                              a CTA covers >= 2 tokens on average); 0: even
+                              split of the units, bounds[c] = c*units_per_cta */
+  int64_t reserved[14];
 } dsa_decode_plan_t;
 
 /* Plan one decode call.
@@ -222,7 +230,7 @@ const char *dsa_decode_status_string(dsa_status s);
 /* ABI version of this header (bumped on any layout change). */
 int32_t dsa_decode_abi_version(void);
 
-#define DSA_DECODE_ABI_VERSION 1
+#define DSA_DECODE_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

@@ -45,7 +45,8 @@ class Plan(ctypes.Structure):
         "tiles_per_token", "units_per_cta", "ctas_per_group", "split_tokens", "kernel")] + \
         [(n, ctypes.c_int64) for n in (
             "total_units", "ws_sel_offset", "ws_part_lse_offset", "ws_part_sel_offset",
-            "ws_part_o_offset", "workspace_bytes")] + [("reserved", ctypes.c_int64 * 16)]
+            "ws_part_o_offset", "workspace_bytes", "ws_bounds_offset", "balance_live")] + \
+        [("reserved", ctypes.c_int64 * 14)]
 
 
 _lib = None

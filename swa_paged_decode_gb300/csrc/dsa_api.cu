@@ -98,6 +98,8 @@ void fill_schedule(const dsa_decode_plan_t *plan, void *ws, Params &p) {
   p.part_lse = reinterpret_cast<float *>(w + plan->ws_part_lse_offset);
   p.part_sel = reinterpret_cast<int32_t *>(w + plan->ws_part_sel_offset);
   p.part_o = reinterpret_cast<float *>(w + plan->ws_part_o_offset);
+  p.bounds = reinterpret_cast<int64_t *>(w + plan->ws_bounds_offset);
+  p.balance = (int32_t)plan->balance_live;
 }
 
 dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
@@ -155,9 +157,10 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   plan->kernel = dsa_tc_supports(plan->heads_per_group) ? dsa::kKernelTc : dsa::kKernelSimt;
   if (const char *k = std::getenv("DSA_DECODE_KERNEL"))
     if (std::strcmp(k, "simt") == 0) plan->kernel = dsa::kKernelSimt;
-  // Balanced static split: every CTA of a head group gets the same number of
-  // consecutive units (FlashMLA's num_sm_parts idea, sparse_decode.h get_meta,
-  // with the units cut evenly instead of per request).
+  // Grid: as many CTAs per head group as an even split of the units needs
+  // (FlashMLA's num_sm_parts idea, sparse_decode.h get_meta). The run kernel
+  // then places the CTA boundaries so that each CTA gets the same number of
+  // live tiles (lengths are read on the device; the plan stays lens-free).
   int64_t target = num_sms / plan->head_groups;
   if (target < 1) target = 1;
   int64_t U = plan->total_units;
@@ -168,8 +171,12 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   plan->units_per_cta = (int32_t)upc;
   plan->ctas_per_group = (int32_t)ctas;
   plan->split_tokens = ctas > 1 ? (int32_t)(ctas - 1) : 0;
+  // Balancing live tiles pays off once a CTA covers several tokens; with
+  // fewer, the per-token cost (Q staging, finalize) dominates and the even
+  // split (no length scan at kernel start) is faster.
+  plan->balance_live = ((int64_t)num_tokens >= 2 * ctas) ? 1 : 0;
   // Workspace: status | sel[T][2] | part_lse[HG][2C][hpg] | part_sel[2C][2] |
-  //            part_o[HG][2C][hpg][512]
+  //            part_o[HG][2C][hpg][512] | bounds[C+1]
   const int64_t slots = 2 * ctas;
   int64_t off = kStatusBytes;
   plan->ws_sel_offset = off;
@@ -181,6 +188,8 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   plan->ws_part_o_offset = off;
   off = align_up(off + 4 * plan->head_groups * slots * plan->heads_per_group * (int64_t)dsa::kD,
                  kAlignWs);
+  plan->ws_bounds_offset = off;
+  off = align_up(off + 8 * (ctas + 1), kAlignWs);
   plan->workspace_bytes = num_tokens == 0 ? 0 : off;
   *workspace_bytes = (size_t)plan->workspace_bytes;
   return DSA_OK;

@@ -13,8 +13,9 @@
 //
 // Grid: x = one block per (CTA boundary, head group), y = chunks of 8 heads
 // x 4 quarters of the dims.
-// Boundary b (1 <= b < C) falls inside token t = b*upc / tpt; the blocks of
-// b work only when b is the first boundary inside that token, so every split
+// Boundary b (1 <= b < C) is the first unit bounds[b] of CTA b (ranges set
+// by the run kernel); it falls inside token t = bounds[b] / tpt and its
+// blocks work only when b is the first boundary inside that token, so every split
 // token is merged once, by hpg/2 blocks per head group. A block first turns
 // the parts' lse into weights in shared memory, then streams the partial O.
 #include "dsa_internal.cuh"
@@ -31,20 +32,29 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   pdl_wait_primary();   // the decode kernel's partials are complete and visible
   const int hg = blockIdx.x % p.HG;
   const int b = 1 + blockIdx.x / p.HG;
-  const int64_t ub = (int64_t)b * p.upc;
+  const int64_t ub = __ldg(p.bounds + b);
+  if (ub >= p.U) return;                                 // empty CTAs at the end
   const int32_t t = (int32_t)(ub / p.tpt);
-  const int64_t ts = (int64_t)t * p.tpt;
+  const int64_t ts = (int64_t)t * p.tpt, te = ts + p.tpt;
   if (ub == ts) return;                                  // boundary on a token start
-  if (b > 1 && (int64_t)(b - 1) * p.upc > ts) return;    // not the first boundary in t
-  const int32_t c0 = (int32_t)(ts / p.upc);
-  const int32_t c1 = (int32_t)((ts + p.tpt - 1) / p.upc);
+  if (b > 1 && __ldg(p.bounds + b - 1) > ts) return;     // not the first boundary in t
+  // parts: CTA b-1 (holds unit ts) through the CTA holding unit te-1
+  const int32_t c0 = b - 1;
+  int32_t c1;
+  if (!p.balance) {   // even split: the CTA holding unit te-1 directly
+    const int64_t cl = (te - 1) / p.upc;
+    c1 = (int32_t)(cl < p.C - 1 ? cl : p.C - 1);
+  } else {            // balanced ranges: a token spans a few CTAs at most
+    c1 = b;
+    while (c1 + 1 < p.C && __ldg(p.bounds + c1 + 1) < te) ++c1;
+  }
   const int np = c1 - c0 + 1;
   const int hpg = p.hpg, h0 = hg * hpg, hb = (blockIdx.y / kCombineQuarters) * kCombineHeads;
   const int dq = (blockIdx.y % kCombineQuarters) * (kD / 4 / kCombineQuarters);   // first float4 of the quarter
   const int64_t slot_base = (int64_t)hg * 2 * p.C;
   // Partial slot of CTA c for token t: 2c when t is the CTA's first token,
   // else 2c + 1 (only the first CTA of the token can start in an earlier one).
-  const bool c0_late = (int64_t)c0 * p.upc < ts;
+  const bool c0_late = __ldg(p.bounds + c0) < ts;
   auto slot_of = [&](int32_t c) -> int64_t { return 2 * (int64_t)c + ((c == c0 && c0_late) ? 1 : 0); };
   float *w_s = cs;
   float *inv_s = cs + np * kCombineHeads;

@@ -56,6 +56,8 @@ struct Params {
   int32_t T, H, hpg, HG, tpt, upc, C;
   int64_t U;
   // workspace
+  int64_t *bounds;             // [C+1]: CTA c owns units [bounds[c], bounds[c+1])
+  int32_t balance;             // 1: live-tile balanced ranges, 0: c*upc
   int32_t *status;             // device status word
   int32_t *sel;                // [T][2]: kept rows, checksum
   float *part_lse;             // [HG][2C][hpg]
@@ -64,10 +66,16 @@ struct Params {
 };
 
 // ---------------------------------------------------------------- schedule
-// Units are (token, tile) pairs in token-major order; CTA c of a head group
-// owns units [c*upc, min(U, (c+1)*upc)). Inside a CTA, the first and last
-// tokens may be partial ("split"); their partial results go to slot 2c (the
-// first token) and 2c+1 (the last token, when different from the first).
+// Units are (token, tile) pairs in token-major order. A tile is live when its
+// first row lies below min(len, width) of its list; dead tiles cost nothing
+// but a skip. The C CTAs of a head group split the units into contiguous
+// ranges. With p.balance the ranges hold equal numbers of LIVE tiles
+// (FlashMLA's decoding-schedule idea, sparse_decode.h get_decoding_sched_meta,
+// balanced on live tiles): CTA c < Ce = max(1, min(C, L)) starts at the unit
+// of live tile floor(c L / Ce) (CTA 0 at unit 0), CTAs >= Ce are empty;
+// otherwise CTA c owns [c*upc, (c+1)*upc) clipped to U. Inside a CTA, the
+// first and last tokens may be partial ("split"); their partial results go
+// to slot 2c (the first token) and 2c+1 (the last token, when different).
 struct Segment {
   int32_t t;        // token
   int64_t u_begin;  // first unit
@@ -76,16 +84,87 @@ struct Segment {
   int32_t slot;     // partial slot when !whole
 };
 
-__host__ __device__ inline int64_t cta_unit_begin(const Params &p, int32_t c) {
-  return (int64_t)c * p.upc;
+// live tiles of list L for token t
+__device__ inline int32_t live_tiles(const ListArgs &L, int64_t t) {
+  int32_t n = __ldg(L.lens + t);
+  n = n < 0 ? 0 : (n > L.width ? L.width : n);
+  return (n + kTile - 1) / kTile;
 }
-__host__ __device__ inline int64_t cta_unit_end(const Params &p, int32_t c) {
-  int64_t e = (int64_t)(c + 1) * p.upc;
-  return e < p.U ? e : p.U;
+__device__ inline int64_t live_tiles_token(const Params &p, int64_t t) {
+  return live_tiles(p.list[0], t) + (p.nlists > 1 ? live_tiles(p.list[1], t) : 0);
 }
 
-__device__ inline Segment make_segment(const Params &p, int32_t c, int32_t t) {
-  int64_t u0 = cta_unit_begin(p, c), u1 = cta_unit_end(p, c);
+// Unit range [u0, u1) of CTA c. Called by every thread of the block (it
+// synchronizes the block); scr: shared scratch of blockDim.x + 2 int64. Also
+// publishes the range to p.bounds for the combine kernel.
+__device__ inline void cta_range(const Params &p, int32_t c, int64_t *scr, int64_t &u0,
+                                 int64_t &u1) {
+  const int n = blockDim.x, tid = threadIdx.x;
+  if (!p.balance) {   // even split of the units
+    u0 = (int64_t)c * p.upc;
+    u0 = u0 < p.U ? u0 : p.U;
+    u1 = u0 + p.upc < p.U ? u0 + p.upc : p.U;
+    if (tid == 0) {
+      p.bounds[c] = u0;
+      if (c == p.C - 1) p.bounds[p.C] = p.U;
+    }
+    return;
+  }
+  const int64_t T = p.T;
+  const int64_t t0 = T * tid / n, t1 = T * (tid + 1) / n;
+  int64_t sum = 0;
+  for (int64_t t = t0; t < t1; ++t) sum += live_tiles_token(p, t);
+  scr[tid] = sum;
+  __syncthreads();
+  for (int off = 1; off < n; off <<= 1) {   // inclusive scan over the threads' token chunks
+    const int64_t v = tid >= off ? scr[tid - off] : 0;
+    __syncthreads();
+    scr[tid] += v;
+    __syncthreads();
+  }
+  const int64_t L = scr[n - 1];
+  if (tid < 2) {
+    const int64_t cc = (int64_t)c + tid;
+    const int64_t ce = L < 1 ? 1 : (L < p.C ? L : p.C);
+    int64_t b;
+    if (cc == 0) {
+      b = 0;
+    } else if (cc >= ce) {
+      b = p.U;
+    } else {
+      const int64_t li = cc * L / ce;   // live tile that starts CTA cc
+      int lo = 0, hi = n - 1;           // first chunk whose inclusive prefix exceeds li
+      while (lo < hi) {
+        const int mid = (lo + hi) / 2;
+        if (scr[mid] > li) hi = mid; else lo = mid + 1;
+      }
+      int64_t acc = lo > 0 ? scr[lo - 1] : 0;
+      b = p.U;
+      for (int64_t t = T * lo / n, te = T * (lo + 1) / n; t < te; ++t) {
+        const int64_t n0 = live_tiles(p.list[0], t);
+        const int64_t lt = n0 + (p.nlists > 1 ? live_tiles(p.list[1], t) : 0);
+        if (li < acc + lt) {
+          const int64_t k = li - acc;
+          b = t * p.tpt + (k < n0 ? k : p.list[0].tiles + (k - n0));
+          break;
+        }
+        acc += lt;
+      }
+    }
+    scr[n + tid] = b;
+  }
+  __syncthreads();
+  u0 = scr[n];
+  u1 = scr[n + 1];
+  __syncthreads();   // scratch free again
+  if (tid == 0) {
+    p.bounds[c] = u0;
+    if (c == p.C - 1) p.bounds[p.C] = p.U;
+  }
+}
+
+__device__ inline Segment make_segment(const Params &p, int32_t c, int32_t t, int64_t u0,
+                                       int64_t u1) {
   int64_t ts = (int64_t)t * p.tpt, te = ts + p.tpt;
   Segment s;
   s.t = t;

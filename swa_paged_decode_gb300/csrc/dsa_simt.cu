@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int hg = blockIdx.x % p.HG;
   const int c = blockIdx.x / p.HG;
-  const int64_t u0 = cta_unit_begin(p, c), u1 = cta_unit_end(p, c);
+  int64_t u0, u1;   // live-balanced unit range (the Q area is free scratch here)
+  cta_range(p, c, reinterpret_cast<int64_t *>(sm.q), u0, u1);
   if (u0 >= u1) return;
   const int32_t tf = (int32_t)(u0 / p.tpt), tl = (int32_t)((u1 - 1) / p.tpt);
   const int h0 = hg * HPG;
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) 
   static_assert(kSimtThreads * 2 == kD, "accumulator layout assumes 2 dims per thread per head");
 
   for (int32_t t = tf; t <= tl; ++t) {
-    const Segment seg = make_segment(p, c, t);
+    const Segment seg = make_segment(p, c, t, u0, u1);
     // Q (fp32) with NeoX RoPE on dims 448..511.
     int64_t pos = p.positions ? __ldg(p.positions + t) : 0;
     if (pos < 0 || (p.cos_sin && pos >= p.cs_rows)) {   // outside the table: flag, use row 0

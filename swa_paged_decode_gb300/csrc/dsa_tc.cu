@@ -342,7 +342,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   const int hg = blockIdx.x % p.HG;
   const int cta = blockIdx.x / p.HG;
   const int h0 = hg * HPG;
-  const int64_t u0 = cta_unit_begin(p, cta), u1 = cta_unit_end(p, cta);
+  int64_t u0, u1;   // live-balanced unit range (the KV area is free scratch here)
+  cta_range(p, cta, reinterpret_cast<int64_t *>(smem + Cfg::kKV), u0, u1);
   if (u0 >= u1) return;
 
   if (warp == 0) {
@@ -643,7 +644,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       if (t != cur_t) {
         if (cur_t >= 0) finalize(seg);
         cur_t = t;
-        seg = make_segment(p, cta, t);
+        seg = make_segment(p, cta, t, u0, u1);
         seg_worked = false;
         first_pv = true;
 #pragma unroll

@@ -199,3 +199,31 @@ def test_position_outside_table_sets_status():
     dec = B.Decoder(w)
     dec(w)
     assert B.dsa_decode_read_status(dec.workspace) == -1
+
+
+@pytest.mark.parametrize("cfg,T", [(4, None), (2, 512), (3, 512)])
+def test_live_tile_balanced_ranges(cfg, T):
+    """When the plan asks for it (a CTA covers >= 2 tokens), the run kernel
+    splits the units over the CTAs by live tiles: the published ranges
+    partition [0, U) and hold equal live-tile counts (to within one)."""
+    w = W.make_config(cfg, T=T, device="cuda")
+    dec, out, lse, kept, chk = run_gpu(w)
+    plan = dec.plan
+    assert plan.balance_live == 1
+    tok = sample_tokens(w.T, 24)
+    compare(out, lse, kept, chk, oracle_ref(w, tokens=tok), tokens=tok, what=w.name)
+    C = plan.ctas_per_group
+    nb = (C + 1) * 8
+    b = dec.workspace[plan.ws_bounds_offset: plan.ws_bounds_offset + nb].view(torch.int64).cpu().numpy()
+    assert b[0] == 0 and b[-1] == plan.total_units and np.all(np.diff(b) >= 0)
+    tpt = plan.tiles_per_token
+    live = np.zeros(plan.total_units, dtype=np.int64)
+    lists = [(w.swa, plan.tiles_swa, 0)] + ([(w.extra, plan.tiles_extra, plan.tiles_swa)] if w.extra is not None else [])
+    for lst, tiles, off in lists:
+        lim = lst.lens.clamp(0, lst.width).cpu().numpy()
+        for t in range(w.T):
+            nlive = -(-int(lim[t]) // 128)
+            live[t * tpt + off: t * tpt + off + nlive] = 1
+    per = np.array([live[b[c]:b[c + 1]].sum() for c in range(C)])
+    busy = per[np.diff(b) > 0]
+    assert busy.min() >= 1 and busy.max() - busy.min() <= 1, (busy.min(), busy.max())
