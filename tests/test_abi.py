@@ -47,8 +47,8 @@ def test_status_strings(lib):
 
 
 def test_plan_struct_size_matches_header():
-    # 16 int32 + 6 int64 + 16 reserved int64
-    assert ctypes.sizeof(B.Plan) == 16 * 4 + 6 * 8 + 16 * 8
+    # 16 int32 + 8 int64 + 14 reserved int64
+    assert ctypes.sizeof(B.Plan) == 16 * 4 + 8 * 8 + 14 * 8
 
 
 @pytest.mark.parametrize("T,H,ws,we,sms", [
@@ -207,3 +207,16 @@ def test_combine_and_selection_validation(lib):
                                   None) == -3
     assert lib.dsa_decode_selection(ctypes.byref(a.plan), None, FAKE, FAKE, None) == -1
     assert lib.dsa_decode_read_status(None, None, None) == -1
+
+
+@pytest.mark.parametrize("T,sms", [(1, 152), (64, 152), (128, 152), (256, 152), (1024, 152), (4, 1)])
+def test_plan_live_balancing_flag_and_bounds_slot(lib, T, sms):
+    """Live-tile balancing is planned exactly when a CTA covers >= 2 tokens;
+    the CTA-range array (C + 1 int64) sits inside the workspace, after the
+    partials, 256-byte aligned."""
+    plan, nbytes = B.dsa_decode_plan(T, 64, 128, 2048, sms)
+    C = plan.ctas_per_group
+    assert plan.balance_live == (1 if T >= 2 * C else 0)
+    assert plan.ws_bounds_offset % 256 == 0
+    assert plan.ws_bounds_offset >= plan.ws_part_o_offset
+    assert plan.ws_bounds_offset + 8 * (C + 1) <= nbytes
