@@ -171,10 +171,11 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   plan->units_per_cta = (int32_t)upc;
   plan->ctas_per_group = (int32_t)ctas;
   plan->split_tokens = ctas > 1 ? (int32_t)(ctas - 1) : 0;
-  // Balancing live tiles pays off once a CTA covers several tokens; with
-  // fewer, the per-token cost (Q staging, finalize) dominates and the even
-  // split (no length scan at kernel start) is faster.
-  plan->balance_live = ((int64_t)num_tokens >= 2 * ctas) ? 1 : 0;
+  // Balancing the work (live tiles plus a per-token cost) pays off when the
+  // tokens have many tiles, so ragged lengths leave many dead ones, and
+  // there are enough tokens to spread; elsewhere the length scan at kernel
+  // start costs more latency than it saves (measured on the five configs).
+  plan->balance_live = (num_tokens >= 16 && plan->tiles_per_token >= 8) ? 1 : 0;
   // Workspace: status | sel[T][2] | part_lse[HG][2C][hpg] | part_sel[2C][2] |
   //            part_o[HG][2C][hpg][512] | bounds[C+1]
   const int64_t slots = 2 * ctas;

@@ -69,11 +69,13 @@ struct Params {
 // Units are (token, tile) pairs in token-major order. A tile is live when its
 // first row lies below min(len, width) of its list; dead tiles cost nothing
 // but a skip. The C CTAs of a head group split the units into contiguous
-// ranges. With p.balance the ranges hold equal numbers of LIVE tiles
-// (FlashMLA's decoding-schedule idea, sparse_decode.h get_decoding_sched_meta,
-// balanced on live tiles): CTA c < Ce = max(1, min(C, L)) starts at the unit
-// of live tile floor(c L / Ce) (CTA 0 at unit 0), CTAs >= Ce are empty;
-// otherwise CTA c owns [c*upc, (c+1)*upc) clipped to U. Inside a CTA, the
+// ranges. With p.balance the ranges hold equal work (FlashMLA's
+// decoding-schedule idea, sparse_decode.h get_decoding_sched_meta): with
+// kCostTile per live tile and kCostToken per token that has any (its Q
+// staging and finalize), total L, CTA c starts at the unit where cost
+// floor(c L / C) falls (CTA 0 at unit 0); when L / (kCostTile + kCostToken)
+// < C, or without p.balance, CTA c owns [c*upc, (c+1)*upc) clipped to U.
+// Inside a CTA, the
 // first and last tokens may be partial ("split"); their partial results go
 // to slot 2c (the first token) and 2c+1 (the last token, when different).
 struct Segment {
@@ -92,6 +94,12 @@ __device__ inline int32_t live_tiles(const ListArgs &L, int64_t t) {
 }
 __device__ inline int64_t live_tiles_token(const Params &p, int64_t t) {
   return live_tiles(p.list[0], t) + (p.nlists > 1 ? live_tiles(p.list[1], t) : 0);
+}
+// Work of a token in cost units: kCostTile per live tile plus kCostToken
+// for the per-token steps (Q staging, finalize) when it has any live tile.
+constexpr int64_t kCostTile = 4, kCostToken = 10;
+__device__ inline int64_t token_cost(int64_t live) {
+  return live > 0 ? kCostTile * live + kCostToken : 0;
 }
 
 // Unit range [u0, u1) of CTA c. Called by every thread of the block (it
@@ -113,7 +121,7 @@ __device__ inline void cta_range(const Params &p, int32_t c, int64_t *scr, int64
   const int64_t T = p.T;
   const int64_t t0 = T * tid / n, t1 = T * (tid + 1) / n;
   int64_t sum = 0;
-  for (int64_t t = t0; t < t1; ++t) sum += live_tiles_token(p, t);
+  for (int64_t t = t0; t < t1; ++t) sum += token_cost(live_tiles_token(p, t));
   scr[tid] = sum;
   __syncthreads();
   for (int off = 1; off < n; off <<= 1) {   // inclusive scan over the threads' token chunks
@@ -122,17 +130,24 @@ __device__ inline void cta_range(const Params &p, int32_t c, int64_t *scr, int64
     scr[tid] += v;
     __syncthreads();
   }
-  const int64_t L = scr[n - 1];
+  const int64_t L = scr[n - 1];   // total cost
   if (tid < 2) {
     const int64_t cc = (int64_t)c + tid;
-    const int64_t ce = L < 1 ? 1 : (L < p.C ? L : p.C);
+    // boundaries at least kCostToken + kCostTile cost units apart fall on
+    // distinct units, so no CTA below ce is left empty
+    const int64_t cmax = L / (kCostToken + kCostTile);
+    const int64_t ce = cmax < 1 ? 1 : (cmax < p.C ? cmax : p.C);
     int64_t b;
-    if (cc == 0) {
+    if (ce < p.C) {
+      // too little work to keep every CTA busy at that spacing: the even
+      // split keeps all C CTAs (every CTA has units; live or not)
+      b = cc * p.upc < p.U ? cc * p.upc : p.U;
+    } else if (cc == 0) {
       b = 0;
     } else if (cc >= ce) {
       b = p.U;
     } else {
-      const int64_t li = cc * L / ce;   // live tile that starts CTA cc
+      const int64_t li = cc * L / ce;   // cost unit that starts CTA cc
       int lo = 0, hi = n - 1;           // first chunk whose inclusive prefix exceeds li
       while (lo < hi) {
         const int mid = (lo + hi) / 2;
@@ -143,12 +158,14 @@ __device__ inline void cta_range(const Params &p, int32_t c, int64_t *scr, int64
       for (int64_t t = T * lo / n, te = T * (lo + 1) / n; t < te; ++t) {
         const int64_t n0 = live_tiles(p.list[0], t);
         const int64_t lt = n0 + (p.nlists > 1 ? live_tiles(p.list[1], t) : 0);
-        if (li < acc + lt) {
-          const int64_t k = li - acc;
+        const int64_t ct = token_cost(lt);
+        if (li < acc + ct) {   // the token's fixed cost maps to its first live tile
+          int64_t k = (li - acc - kCostToken) / kCostTile;
+          k = k < 0 ? 0 : k;
           b = t * p.tpt + (k < n0 ? k : p.list[0].tiles + (k - n0));
           break;
         }
-        acc += lt;
+        acc += ct;
       }
     }
     scr[n + tid] = b;

@@ -211,12 +211,14 @@ def test_combine_and_selection_validation(lib):
 
 @pytest.mark.parametrize("T,sms", [(1, 152), (64, 152), (128, 152), (256, 152), (1024, 152), (4, 1)])
 def test_plan_live_balancing_flag_and_bounds_slot(lib, T, sms):
-    """Live-tile balancing is planned exactly when a CTA covers >= 2 tokens;
-    the CTA-range array (C + 1 int64) sits inside the workspace, after the
+    """Work balancing is planned for >= 16 tokens of >= 8 tiles each; the
+    CTA-range array (C + 1 int64) sits inside the workspace, after the
     partials, 256-byte aligned."""
     plan, nbytes = B.dsa_decode_plan(T, 64, 128, 2048, sms)
     C = plan.ctas_per_group
-    assert plan.balance_live == (1 if T >= 2 * C else 0)
+    assert plan.balance_live == (1 if T >= 16 and plan.tiles_per_token >= 8 else 0)
+    narrow, _ = B.dsa_decode_plan(T, 64, 128, 512, sms)   # 5 tiles per token
+    assert narrow.balance_live == 0
     assert plan.ws_bounds_offset % 256 == 0
     assert plan.ws_bounds_offset >= plan.ws_part_o_offset
     assert plan.ws_bounds_offset + 8 * (C + 1) <= nbytes

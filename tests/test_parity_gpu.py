@@ -201,11 +201,13 @@ def test_position_outside_table_sets_status():
     assert B.dsa_decode_read_status(dec.workspace) == -1
 
 
-@pytest.mark.parametrize("cfg,T", [(4, None), (2, 512), (3, 512)])
-def test_live_tile_balanced_ranges(cfg, T):
-    """When the plan asks for it (a CTA covers >= 2 tokens), the run kernel
-    splits the units over the CTAs by live tiles: the published ranges
-    partition [0, U) and hold equal live-tile counts (to within one)."""
+@pytest.mark.parametrize("cfg,T", [(3, None), (4, None), (3, 512)])
+def test_work_balanced_ranges(cfg, T):
+    """When the plan asks for it, the run kernel places the CTA boundaries so
+    that every CTA gets the same work: 4 units per live tile plus 10 per
+    token with a live tile (charged at its first live tile). The published
+    ranges partition [0, U) and their work differs by at most the rounding
+    of two boundaries to unit edges."""
     w = W.make_config(cfg, T=T, device="cuda")
     dec, out, lse, kept, chk = run_gpu(w)
     plan = dec.plan
@@ -215,15 +217,19 @@ def test_live_tile_balanced_ranges(cfg, T):
     C = plan.ctas_per_group
     nb = (C + 1) * 8
     b = dec.workspace[plan.ws_bounds_offset: plan.ws_bounds_offset + nb].view(torch.int64).cpu().numpy()
-    assert b[0] == 0 and b[-1] == plan.total_units and np.all(np.diff(b) >= 0)
+    assert b[0] == 0 and b[-1] == plan.total_units and np.all(np.diff(b) > 0)
     tpt = plan.tiles_per_token
-    live = np.zeros(plan.total_units, dtype=np.int64)
-    lists = [(w.swa, plan.tiles_swa, 0)] + ([(w.extra, plan.tiles_extra, plan.tiles_swa)] if w.extra is not None else [])
-    for lst, tiles, off in lists:
-        lim = lst.lens.clamp(0, lst.width).cpu().numpy()
-        for t in range(w.T):
-            nlive = -(-int(lim[t]) // 128)
-            live[t * tpt + off: t * tpt + off + nlive] = 1
-    per = np.array([live[b[c]:b[c + 1]].sum() for c in range(C)])
-    busy = per[np.diff(b) > 0]
-    assert busy.min() >= 1 and busy.max() - busy.min() <= 1, (busy.min(), busy.max())
+    cost = np.zeros(plan.total_units, dtype=np.int64)
+    lists = [(w.swa, 0)] + ([(w.extra, plan.tiles_swa)] if w.extra is not None else [])
+    lim = [(l.lens.clamp(0, l.width).cpu().numpy(), off) for l, off in lists]
+    for t in range(w.T):
+        first = None
+        for lm, off in lim:
+            nlive = -(-int(lm[t]) // 128)
+            cost[t * tpt + off: t * tpt + off + nlive] = 4
+            if nlive and first is None:
+                first = t * tpt + off
+        if first is not None:
+            cost[first] += 10
+    per = np.array([cost[b[c]:b[c + 1]].sum() for c in range(C)])
+    assert per.max() - per.min() <= 2 * 14, (per.min(), per.max())
