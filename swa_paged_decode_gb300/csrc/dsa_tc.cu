@@ -200,9 +200,14 @@ __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, in
   if (L.fmt == DSA_REC_FP8_528) {
     if (g.ok) {
       const uint8_t *rec = record_ptr(L, sid);
+      if ((reinterpret_cast<uintptr_t>(rec) & 31u) == 0) {   // chunk pairs are whole 32-byte sectors
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        g.d[k] = tc::ldg_nc_v4(rec + 16 * (4 * (k >> 1) + 2 * j + (k & 1)));
+        for (int m = 0; m < 8; ++m) tc::ldg_nc_v8(rec + 64 * m + 32 * j, g.d[2 * m], g.d[2 * m + 1]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          g.d[k] = tc::ldg_nc_v4(rec + 16 * (4 * (k >> 1) + 2 * j + (k & 1)));
+      }
       g.s[0] = tc::ldg_nc_v4(rec + 512);
     } else {
 #pragma unroll
@@ -383,9 +388,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     const int row = 32 * (pw & 3) + lane, j = pw >> 2;
     uint32_t ph_free[4] = {0, 0, 0, 0};
     bool first = true;
+    int warm = 0;
     uint32_t kept = 0, chk = 0, pord = 0;
-    // Tile records are prefetched into L2 (bulk, one thread per row) two
-    // tiles ahead and loaded into registers one tile ahead.
+    // Tile records are loaded into registers one tile ahead; while the CTA
+    // warms up (its first tiles) they are also prefetched into L2 (bulk, one
+    // thread per row) two tiles ahead. In steady state the register loads
+    // cover the latency and the extra prefetch traffic measured slower.
     auto prefetch = [&](const Cursor &c, int32_t sid) {
       if (j != 0 || c.u >= u1) return;
       int32_t lid2, row02;
@@ -454,7 +462,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarKvFull]);
       first = false;
-      prefetch(cn2, sid_n2);
+      if (warm < 2) prefetch(cn2, sid_n2);   // L2 prefetch only while the CTA warms up
+      ++warm;
       cu = cn;
       cn = cn2;
       sid_n1 = sid_n2;
