@@ -75,7 +75,7 @@ dsa_status fill_list(const dsa_cache_desc *c, const int32_t *idx, int64_t stride
   L.width = width;
   L.tiles = (width + dsa::kTile - 1) / dsa::kTile;
   L.aligned32 = (aligned(c->base, 32) && c->page_stride_bytes % 32 == 0 && rb % 32 == 0) ? 1 : 0;
-  L.pad_ = 0;
+  L.sectors32 = (aligned(c->base, 32) && c->page_stride_bytes % 32 == 0) ? 1 : 0;
   return DSA_OK;
 }
 

@@ -36,7 +36,7 @@ struct ListArgs {
   int32_t width;
   int32_t tiles;         // ceil(width / kTile)
   int32_t aligned32;     // every record starts on a 32-byte boundary
-  int32_t pad_;
+  int32_t sectors32;     // base and page stride 32-byte aligned (records may not be)
 };
 
 struct Params {

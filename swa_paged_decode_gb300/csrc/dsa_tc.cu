@@ -180,12 +180,20 @@ __device__ __forceinline__ uint32_t scale_f16x2(float s) {
 // ---------------------------------------------------------------- producer
 // Thread (producer warp pw, lane l): row 32*(pw%4) + l, half j = pw/4 of the
 // record's 16-byte chunks: c = 4m + 2j + e (e in {0,1}) -- whole sectors.
+// One row half of a tile held in registers. Pair layout (pl): d[2m], d[2m+1]
+// are the thread's 16-byte chunks 4m+2j and 4m+2j+1. fp8: m = 0..7, the 4
+// fp32 scales in d[17]; NVFP4: m = 0..3, the 32 e4m3 scales in d[8], d[9].
+// Sector layout (fp8 records 16 bytes off the 32-byte grid, !pl): d[2k],
+// d[2k+1] = 32-byte sector 2k + j of the grid that starts 16 bytes before
+// the record (sector s holds chunks 2s-1 and 2s); lane j = 0 also holds
+// sector 16 (chunk 31 and the scales) in d[16], d[17]. The two lanes of a
+// row rebuild their pairs with one shuffle per pair (dequant_block).
 struct Gather {
-  uint4 d[16];   // fp8: 16 chunks; NVFP4: 8 chunks
-  uint4 s[2];    // fp8: 4 fp32 scales; NVFP4: 32 e4m3 scales
+  uint4 d[18];
   int32_t sid;
   int32_t r;
   bool ok;
+  bool pl;
 };
 
 __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, int32_t sid, int row,
@@ -197,41 +205,48 @@ __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, in
   g.sid = sid;
   g.ok = slot_valid(L, g.r, lid == 0 ? c.lim0 : c.lim1, sid);
   const uint4 z = make_uint4(0, 0, 0, 0);
+  g.pl = true;
   if (L.fmt == DSA_REC_FP8_528) {
     if (g.ok) {
       const uint8_t *rec = record_ptr(L, sid);
       if ((reinterpret_cast<uintptr_t>(rec) & 31u) == 0) {   // chunk pairs are whole 32-byte sectors
 #pragma unroll
         for (int m = 0; m < 8; ++m) tc::ldg_nc_v8(rec + 64 * m + 32 * j, g.d[2 * m], g.d[2 * m + 1]);
+        g.d[17] = tc::ldg_nc_v4(rec + 512);
+      } else if (L.sectors32) {
+        // 16 bytes off the grid (an odd slot of a 32-byte aligned page, so
+        // the sector that starts 16 bytes before the record lies in the page)
+        g.pl = false;
+        const uint8_t *base = rec - 16;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) tc::ldg_nc_v8(base + 32 * (2 * k + j), g.d[2 * k], g.d[2 * k + 1]);
+        if (j == 0) tc::ldg_nc_v8(base + 32 * 16, g.d[16], g.d[17]);
       } else {
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           g.d[k] = tc::ldg_nc_v4(rec + 16 * (4 * (k >> 1) + 2 * j + (k & 1)));
+        g.d[17] = tc::ldg_nc_v4(rec + 512);
       }
-      g.s[0] = tc::ldg_nc_v4(rec + 512);
     } else {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) g.d[k] = z;
-      g.s[0] = z;
+      for (int k = 0; k < 18; ++k) g.d[k] = z;
     }
   } else {
     if (g.ok && L.aligned32) {   // whole 32-byte sectors per request
       const uint8_t *rec = record_ptr(L, sid);
 #pragma unroll
       for (int m = 0; m < 4; ++m) tc::ldg_nc_v8(rec + 64 * m + 32 * j, g.d[2 * m], g.d[2 * m + 1]);
-      tc::ldg_nc_v8(rec + 256, g.s[0], g.s[1]);
+      tc::ldg_nc_v8(rec + 256, g.d[8], g.d[9]);
     } else if (g.ok) {
       const uint8_t *rec = record_ptr(L, sid);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         g.d[k] = tc::ldg_nc_v4(rec + 16 * (4 * (k >> 1) + 2 * j + (k & 1)));
-      g.s[0] = tc::ldg_nc_v4(rec + 256);
-      g.s[1] = tc::ldg_nc_v4(rec + 272);
+      g.d[8] = tc::ldg_nc_v4(rec + 256);
+      g.d[9] = tc::ldg_nc_v4(rec + 272);
     } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) g.d[k] = z;
-      g.s[0] = z;
-      g.s[1] = z;
+      for (int k = 0; k < 10; ++k) g.d[k] = z;
     }
   }
 }
@@ -245,6 +260,18 @@ __device__ __forceinline__ int32_t load_sid(const Params &p, const Cursor &c, in
 }
 
 // Dequantize the two 64-dim k-blocks of M block mb for this thread's row.
+__device__ __forceinline__ uint4 shfl_xor_u4(const uint4 v, int mask) {
+  uint4 r;
+  r.x = __shfl_xor_sync(0xffffffffu, v.x, mask);
+  r.y = __shfl_xor_sync(0xffffffffu, v.y, mask);
+  r.z = __shfl_xor_sync(0xffffffffu, v.z, mask);
+  r.w = __shfl_xor_sync(0xffffffffu, v.w, mask);
+  return r;
+}
+
+// Dequantize the two 64-dim k-blocks of M block mb for this thread's row
+// half. Called by all 32 lanes of the warp (fp8 rows in sector layout get the
+// missing half of each chunk pair from the other lane of their row).
 __device__ __forceinline__ void dequant_block(bool fp8, const Gather &g, const uint32_t (&scale2)[4],
                                               int mb, int row, int j, uint32_t kv_base) {
   if (fp8) {
@@ -252,12 +279,13 @@ __device__ __forceinline__ void dequant_block(bool fp8, const Gather &g, const u
 #pragma unroll
     for (int mm = 0; mm < 2; ++mm) {
       const int m = 2 * mb + mm;
+      const uint4 recv = shfl_xor_u4(j == 0 ? g.d[2 * m + 2] : g.d[2 * m], 1);
+      const uint4 pr[2] = {g.pl ? g.d[2 * m] : g.d[2 * m + 1], g.pl ? g.d[2 * m + 1] : recv};
+      const uint32_t sc = scale2[mb];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int k = 2 * m + e;
         const int c = 4 * m + 2 * j + e;   // dims [16c, 16c+16), scale block mb
-        const uint32_t sc = scale2[mb];
-        const uint32_t w[4] = {g.d[k].x, g.d[k].y, g.d[k].z, g.d[k].w};
+        const uint32_t w[4] = {pr[e].x, pr[e].y, pr[e].z, pr[e].w};
         uint32_t f[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -272,14 +300,15 @@ __device__ __forceinline__ void dequant_block(bool fp8, const Gather &g, const u
     }
   } else {
     // chunk c = 4m + 2j + e holds dims [32c, 32c+32) of k-block 2m + j;
-    // M block mb is m = mb, e in {0, 1}
-    const uint32_t sw[8] = {g.s[0].x, g.s[0].y, g.s[0].z, g.s[0].w,
-                            g.s[1].x, g.s[1].y, g.s[1].z, g.s[1].w};
+    // M block mb is m = mb, e in {0, 1}; its 4 scales are word 2mb + j of
+    // the scale bytes (d[8] words 0..3, d[9] words 4..7)
+    const uint4 sq = mb < 2 ? g.d[8] : g.d[9];
+    const uint32_t sw = j == 0 ? ((mb & 1) ? sq.z : sq.x) : ((mb & 1) ? sq.w : sq.y);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int k = 2 * mb + e;
       const int c = 4 * mb + 2 * j + e;
-      const uint32_t pair = (sw[c >> 1] >> (16 * (c & 1))) & 0xFFFFu;
+      const uint32_t pair = (sw >> (16 * e)) & 0xFFFFu;
       const uint32_t s2 = tc::e4m3x2_to_f16x2(pair);
       const uint32_t sa = __byte_perm(s2, s2, 0x1010), sb = __byte_perm(s2, s2, 0x3232);
       const uint32_t w[4] = {g.d[k].x, g.d[k].y, g.d[k].z, g.d[k].w};
@@ -385,7 +414,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     // ======================================================== producers
     tc::setmaxnreg_dec<kPrRegs>();
     const int pw = warp - kSmWarps;
-    const int row = 32 * (pw & 3) + lane, j = pw >> 2;
+    // the two lanes of a row hold its two halves (j), so they can trade data
+    const int row = 16 * pw + (lane >> 1), j = lane & 1;
     uint32_t ph_free[4] = {0, 0, 0, 0};
     bool first = true;
     int warm = 0;
@@ -425,11 +455,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const bool last_of_token = cn.u >= u1 || cn.t != t;
       const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
       uint32_t scale2[4] = {0, 0, 0, 0};
-      if (fp8) {
-        scale2[0] = scale_f16x2(__uint_as_float(g.s[0].x));
-        scale2[1] = scale_f16x2(__uint_as_float(g.s[0].y));
-        scale2[2] = scale_f16x2(__uint_as_float(g.s[0].z));
-        scale2[3] = scale_f16x2(__uint_as_float(g.s[0].w));
+      if (fp8) {   // sector layout: lane j = 1 takes the scales from lane j = 0
+        const uint4 sp = shfl_xor_u4(g.d[17], 1);
+        const uint4 sv = (!g.pl && j == 1) ? sp : g.d[17];
+        scale2[0] = scale_f16x2(__uint_as_float(sv.x));
+        scale2[1] = scale_f16x2(__uint_as_float(sv.y));
+        scale2[2] = scale_f16x2(__uint_as_float(sv.z));
+        scale2[3] = scale_f16x2(__uint_as_float(sv.w));
       }
       if (j == 0 && g.ok) {
         kept += 1;
@@ -450,6 +482,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         chk = 0;
         ++pord;
       }
+#pragma unroll
       for (int mb = 0; mb < 4; ++mb) {
         if (!first) wait(kBarKvFree + mb, ph_free[mb]);
         if (mb == 0 && j == 0) row_ok_s[row] = g.ok ? 1.f : 0.f;
