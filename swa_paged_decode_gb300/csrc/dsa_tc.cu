@@ -47,19 +47,19 @@ namespace dsa {
 constexpr int kSmWarps = 8;                    // softmax / epilogue / MMA issue
 constexpr int kPrWarps = 8;                    // producers
 constexpr int kTcThreads = 32 * (kSmWarps + kPrWarps);
-// Register split (per thread): the kernel is launched with 128, softmax
-// warpgroups raise theirs to 152 and producer warpgroups drop to 104, which
-// sums to exactly the launch allocation (2*128*152 + 2*128*104 = 512*128);
-// at this split ptxas reports no spills for any head count.
+// Register split (per thread): the kernel is launched with 128; softmax
+// warpgroups raise theirs and producer warpgroups drop theirs by the same
+// amount, so the split sums to exactly the launch allocation. 64 heads per
+// group: 152 / 104 (the softmax side needs the room); 16 and 32: 144 / 112,
+// where ptxas reports no spills.
 constexpr int kLaunchRegs = 128;
-constexpr int kSmRegs = 152;
-constexpr int kPrRegs = 104;
-static_assert(kSmRegs + kPrRegs == 2 * kLaunchRegs, "register split must match the launch");
 constexpr long long kWaitBudget = 4000000000ll;  // SM cycles (~2 s) per wait
 constexpr float kRescaleSlack = 8.0f;            // log2 headroom of the running max
 
 template <int HPG>
 struct TcCfg {
+  static constexpr int kSmRegs = HPG == 64 ? 152 : 144;
+  static constexpr int kPrRegs = 2 * kLaunchRegs - kSmRegs;
   static constexpr int kHalf = HPG / 2;                  // heads per softmax thread
   static constexpr int kPRow = HPG * 2;                  // bytes per P row
   static constexpr uint32_t kPBytes = 128 * kPRow;
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 
   if (warp >= kSmWarps) {
     // ======================================================== producers
-    tc::setmaxnreg_dec<kPrRegs>();
+    tc::setmaxnreg_dec<Cfg::kPrRegs>();
     const int pw = warp - kSmWarps;
     // the two lanes of a row hold its two halves (j), so they can trade data
     const int row = 16 * pw + (lane >> 1), j = lane & 1;
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     }
   } else {
     // ======================================================== softmax / epilogue / MMA
-    tc::setmaxnreg_inc<kSmRegs>();
+    tc::setmaxnreg_inc<Cfg::kSmRegs>();
     const int q4 = warp & 3, half = warp >> 2;
     const int prow = 32 * q4 + lane;
     const uint32_t tl_lane = tmem + ((uint32_t)(32 * q4) << 16);
