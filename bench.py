@@ -42,9 +42,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # while the kernel sources hash to `sources`. The capture is summarised under
 # profiles/ with the command that made it.
 NCU_TRAFFIC = {
-    "sources": "b0abbc59ac8688d7",
+    "sources": "3bfa6a593ccef033",
     "workload": "config5_T256_H64",
-    "bytes_per_launch": 430850560 + 25888000,
+    "bytes_per_launch": 426152704 + 25781248,
     "rows_per_launch": 256 * (128 + 4096),
 }
 KERNEL_SOURCES = ("swa_paged_decode_gb300/csrc/dsa_tc.cu", "swa_paged_decode_gb300/csrc/tc_ptx.cuh",
