@@ -427,7 +427,7 @@ def oracle_timing(w: W.Workload, target_s: float, seed: int = 0):
     tok = np.sort(rng.choice(w.T, size=n, replace=False))
     t0 = time.perf_counter()
     oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
-                  positions=a["positions"], cos_sin=a["cos_sin"], tokens=tok, nthreads=cores)
+                  positions=a["positions"], cos_sin=a["cos_sin"], rope_style=a["rope_style"], tokens=tok, nthreads=cores)
     dt = time.perf_counter() - t0
     per_tok = dt / n
     n2 = int(max(1, min(w.T, target_s / max(per_tok, 1e-9))))
@@ -435,7 +435,7 @@ def oracle_timing(w: W.Workload, target_s: float, seed: int = 0):
         tok = np.sort(rng.choice(w.T, size=n2, replace=False))
         t0 = time.perf_counter()
         oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
-                      positions=a["positions"], cos_sin=a["cos_sin"], tokens=tok, nthreads=cores)
+                      positions=a["positions"], cos_sin=a["cos_sin"], rope_style=a["rope_style"], tokens=tok, nthreads=cores)
         dt = time.perf_counter() - t0
         n = n2
     return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -457,7 +457,7 @@ def reference_arm(args):
         tok = np.sort(rng.choice(w.T, size=n, replace=False))
         t0 = time.perf_counter()
         oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
-                      positions=a["positions"], cos_sin=a["cos_sin"], tokens=tok, nthreads=cores)
+                      positions=a["positions"], cos_sin=a["cos_sin"], rope_style=a["rope_style"], tokens=tok, nthreads=cores)
         return time.perf_counter() - t0
     for _ in range(args.warmup):
         one()

@@ -5,7 +5,8 @@ benchmark's CPU-baseline leg use this package. The product library never
 imports it, and it imports nothing from the product package.
 
 ``dsa_oracle.c`` holds the definition (candidate rows, record dequantization,
-NeoX RoPE of Q, scores, lse and the sink-weighted output). This module only
+NeoX or GPT-J RoPE of Q, scores, lse and the sink-weighted output; the V4.1
+output epilogue: inverse RoPE, MXFP8 cast, o-fused layout). This module only
 compiles it with gcc, marshals numpy/torch CPU arrays into it, and adds
 ``combine`` -- the split-KV merge written as the plain formula from the
 "production.py" page's Python KV merge (out = sum_i e^{lse_i} O_i /
@@ -29,16 +30,20 @@ _lib = None
 
 FMT_FP8_528 = 0
 FMT_NVFP4_288 = 1
-RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288}
+FMT_FP8_528_UE8M0 = 2
+RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288, FMT_FP8_528_UE8M0: 528}
+ROPE_NEOX = 0
+ROPE_GPTJ = 1
 
 
 def build(force: bool = False) -> str:
-    """Compile dsa_oracle.c into liboracle.so next to it (gcc, -O2, no fast-math)."""
+    """Compile dsa_oracle.c into liboracle.so next to it (gcc, -O2, no fast-math,
+    no contraction of products and sums into fused multiply-adds)."""
     if (not force and os.path.exists(_LIB)
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-Wall",
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-Wall", "-ffp-contract=off",
            "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
@@ -70,14 +75,25 @@ def _load():
             lib.oracle_dequant_record.restype = None
             lib.oracle_dequant_record.argtypes = [ctypes.c_void_p, ctypes.c_int32,
                                                   ctypes.c_void_p]
+            lib.oracle_ue8m0_value.restype = ctypes.c_double
+            lib.oracle_ue8m0_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+            lib.oracle_ue8m0_ceil.restype = ctypes.c_uint8
+            lib.oracle_ue8m0_ceil.argtypes = [ctypes.c_float]
             lib.oracle_decode.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [
                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                 ctypes.POINTER(_Cache), ctypes.POINTER(_List), ctypes.c_int32,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
-                ctypes.c_double, ctypes.c_void_p, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_double, ctypes.c_void_p, ctypes.c_int32,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_int32]
+            lib.oracle_mxfp8_epilogue.restype = ctypes.c_int
+            lib.oracle_mxfp8_epilogue.argtypes = [
+                ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -88,6 +104,20 @@ def e4m3_value(code: int) -> float:
 
 def e2m1_value(nibble: int) -> float:
     return _load().oracle_e2m1_value(nibble & 0xF)
+
+
+def ue8m0_value(byte: int) -> float:
+    return _load().oracle_ue8m0_value(byte & 0xFF)
+
+
+def e4m3_encode(y: float) -> int:
+    """Nearest e4m3 code (ties to even, saturating at 448, sign kept)."""
+    return int(_load().oracle_e4m3_encode(float(y)))
+
+
+def ue8m0_ceil(v: float) -> int:
+    """ue8m0 byte of the smallest power of two >= the fp32 value v."""
+    return int(_load().oracle_ue8m0_ceil(float(v)))
 
 
 def dequant_record(record: np.ndarray, fmt: int) -> np.ndarray:
@@ -119,7 +149,7 @@ def _np(x, dtype):
 
 
 def decode(q, caches, lists, *, scale: float, sink=None, positions=None, cos_sin=None,
-           tokens=None, nthreads: int | None = None):
+           tokens=None, nthreads: int | None = None, rope_style: int = ROPE_NEOX):
     """Run the oracle.
 
     q        : bf16 [T, H, 512] (torch CPU tensor) or uint16 numpy bit patterns.
@@ -128,6 +158,8 @@ def decode(q, caches, lists, *, scale: float, sink=None, positions=None, cos_sin
     lists    : sequence of dicts {ids: int32 [T, >=width], lens: int32 [T], width}.
     sink     : fp32 [H] or None. positions: int64 [T]; cos_sin: fp32 [P, 64] or None.
     tokens   : token indices to evaluate (default: all).
+    rope_style: ROPE_NEOX (dim 448+i pairs with 480+i) or ROPE_GPTJ (448+2i
+               with 449+2i).
     Returns (out fp64 [n, H, 512], lse fp64 [n, H], kept int32 [n], checksum uint32 [n]).
     """
     lib = _load()
@@ -179,12 +211,40 @@ def decode(q, caches, lists, *, scale: float, sink=None, positions=None, cos_sin
         sk.ctypes.data if sk is not None else None,
         pos.ctypes.data if pos is not None else None,
         cs.ctypes.data if cs is not None else None,
-        cs.shape[0] if cs is not None else 0,
+        cs.shape[0] if cs is not None else 0, int(rope_style),
         float(scale), tok.ctypes.data, n,
         out.ctypes.data, lse.ctypes.data, kept.ctypes.data, chk.ctypes.data, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_decode rejected its arguments")
     return out, lse, kept, chk
+
+
+def mxfp8_epilogue(out, *, group_size: int, positions=None, cos_sin=None,
+                   rope_style: int = ROPE_GPTJ):
+    """V4.1 output epilogue of fp64 outputs out [n, H, 512] (rows of decode's
+    out): inverse RoPE of dims >= 448 (when cos_sin is given; positions [n]
+    are the rows' positions), fp32 rounding, MXFP8 cast (one ue8m0 scale per
+    head and 32 dims), o-fused layout with `group_size` heads per group.
+    Returns (codes uint8 [n, H/G, G*512], scales uint8 [n, H/G, G*16],
+    x fp32 [n, H, 512] -- the values the cast was applied to)."""
+    o = np.ascontiguousarray(out, dtype=np.float64)
+    n, H, D = o.shape
+    assert D == 512 and H % group_size == 0
+    G = int(group_size)
+    pos = _np(positions, np.int64)
+    cs = _np(cos_sin, np.float32)
+    if cs is not None:
+        assert cs.ndim == 2 and cs.shape[1] == 64 and pos is not None and pos.shape == (n,)
+    codes = np.zeros((n, H // G, G * 512), dtype=np.uint8)
+    scales = np.zeros((n, H // G, G * 16), dtype=np.uint8)
+    x = np.zeros((n, H, 512), dtype=np.float32)
+    rc = _load().oracle_mxfp8_epilogue(
+        o.ctypes.data, n, H, pos.ctypes.data if pos is not None else None,
+        cs.ctypes.data if cs is not None else None, cs.shape[0] if cs is not None else 0,
+        int(rope_style), G, x.ctypes.data, codes.ctypes.data, scales.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_mxfp8_epilogue rejected its arguments")
+    return codes, scales, x
 
 
 def combine(parts_out, parts_lse, sink=None):

@@ -25,15 +25,18 @@
  *      stage_inputs splits the id by the power-of-two page size; its
  *      __call__ docstring allows pages further apart than page*record).
  *   3. Dequantize in fp64 (record formats: the fp8 record holds 512 e4m3
- *      bytes then 4 little-endian fp32 scales, one per 128 dims; the NVFP4
- *      record holds 256 bytes of e2m1 nibbles then 32 e4m3 scales, one per 16
- *      dims, element 2i in the low nibble of byte i and 2i+1 in the high one).
- *      k[d] = code(d) * scale(d).
+ *      bytes then 4 little-endian fp32 scales, one per 128 dims; the V4.1
+ *      fp8 record of the swapab page (stage_inputs, fp8 branch) holds 512
+ *      e4m3 bytes then 16 ue8m0 scale bytes, one per 32 dims, scale byte b
+ *      meaning 2^(b-127); the NVFP4 record holds 256 bytes of e2m1 nibbles
+ *      then 32 e4m3 scales, one per 16 dims, element 2i in the low nibble of
+ *      byte i and 2i+1 in the high one). k[d] = code(d) * scale(d).
  *   4. Q.  q = bf16 value of q[t, h, :] in fp64. With RoPE on, the last 64
- *      dims are rotated NeoX style (first half against second half) by the
- *      fp32 table row cos_sin[positions[t]] = [cos(32) | sin(32)]:
- *      x1 = q[448+i], x2 = q[480+i]; q[448+i] = x1 c - x2 s,
- *      q[480+i] = x2 c + x1 s.
+ *      dims are rotated by the fp32 table row cos_sin[positions[t]] =
+ *      [cos(32) | sin(32)], pair i taking c = cos[i], s = sin[i]:
+ *      NeoX style pairs x1 = q[448+i] with x2 = q[480+i]; GPT-J style (the
+ *      swapab page, stage_inputs Q RoPE) pairs x1 = q[448+2i] with
+ *      x2 = q[449+2i]; either way x1 <- x1 c - x2 s, x2 <- x2 c + x1 s.
  *   5. Scores s_j = scale * (q . k_j). The sink logit is not scaled
  *      (swapab page, merge step: the sink enters as exp(sink) in natural-log
  *      units next to the partial sums).
@@ -43,6 +46,10 @@
  *      shared row serves as key and value). No rows, or sink = +inf, gives
  *      out = 0 (swapab page, merge step: a zero denominator or an infinite
  *      sink yields a zero output).
+ *
+ * The V4.1 output epilogue (swapab page, merge step: inverse RoPE, MXFP8
+ * cast, o-fused store) is a separate function, oracle_mxfp8_epilogue, applied
+ * to the fp64 out of steps 1-6.
  *
  * Masking instrumentation: per token, the count of kept rows and the sum
  * (mod 2^32) over kept rows of fmix32(id * 0x9E3779B1 + 2*r + L), where
@@ -59,7 +66,8 @@
 #define ORACLE_ROPE_START 448
 #define ORACLE_ROPE_HALF 32
 
-enum { ORACLE_FMT_FP8_528 = 0, ORACLE_FMT_NVFP4_288 = 1 };
+enum { ORACLE_FMT_FP8_528 = 0, ORACLE_FMT_NVFP4_288 = 1, ORACLE_FMT_FP8_528_UE8M0 = 2 };
+enum { ORACLE_ROPE_NEOX = 0, ORACLE_ROPE_GPTJ = 1 };
 
 typedef struct {
   const uint8_t *base;  /* host bytes of the whole cache                      */
@@ -103,6 +111,12 @@ double oracle_e2m1_value(uint8_t nib) {
   return sign ? -v : v;
 }
 
+/* OCP MX E8M0 scale: 2^(b - 127); b = 0xFF is NaN. */
+double oracle_ue8m0_value(uint8_t b) {
+  if (b == 0xFF) return NAN;
+  return ldexp(1.0, (int)b - 127);
+}
+
 static double le_f32(const uint8_t *p) {
   uint32_t u = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) |
                ((uint32_t)p[3] << 24);
@@ -119,7 +133,7 @@ static double bf16_value(uint16_t u) {
 }
 
 static int record_bytes(int32_t format) {
-  return format == ORACLE_FMT_FP8_528 ? 528 : 288;
+  return format == ORACLE_FMT_NVFP4_288 ? 288 : 528;
 }
 
 /* Step 3: one record -> 512 fp64 values. */
@@ -127,6 +141,9 @@ void oracle_dequant_record(const uint8_t *rec, int32_t format, double *k) {
   if (format == ORACLE_FMT_FP8_528) {
     for (int d = 0; d < ORACLE_D; ++d)
       k[d] = oracle_e4m3_value(rec[d]) * le_f32(rec + 512 + 4 * (d / 128));
+  } else if (format == ORACLE_FMT_FP8_528_UE8M0) {
+    for (int d = 0; d < ORACLE_D; ++d)
+      k[d] = oracle_e4m3_value(rec[d]) * oracle_ue8m0_value(rec[512 + d / 32]);
   } else {
     for (int d = 0; d < ORACLE_D; ++d) {
       uint8_t byte = rec[d / 2];
@@ -176,6 +193,7 @@ typedef struct {
   const int64_t *positions;
   const float *cos_sin;
   int64_t cs_rows;
+  int32_t rope_style;   /* ORACLE_ROPE_* */
   double scale;
   const int32_t *tokens;
   int32_t n_tokens;
@@ -206,10 +224,17 @@ static void one_token(oracle_job *J, int32_t i, double *K, double *s) {
       const float *row = J->cos_sin + pos * 64;
       for (int i2 = 0; i2 < ORACLE_ROPE_HALF; ++i2) {
         double c = (double)row[i2], sn = (double)row[ORACLE_ROPE_HALF + i2];
-        double x1 = q[ORACLE_ROPE_START + i2];
-        double x2 = q[ORACLE_ROPE_START + ORACLE_ROPE_HALF + i2];
-        q[ORACLE_ROPE_START + i2] = x1 * c - x2 * sn;
-        q[ORACLE_ROPE_START + ORACLE_ROPE_HALF + i2] = x2 * c + x1 * sn;
+        int d1, d2;   /* the pair's two dims */
+        if (J->rope_style == ORACLE_ROPE_GPTJ) {
+          d1 = ORACLE_ROPE_START + 2 * i2;
+          d2 = d1 + 1;
+        } else {
+          d1 = ORACLE_ROPE_START + i2;
+          d2 = d1 + ORACLE_ROPE_HALF;
+        }
+        double x1 = q[d1], x2 = q[d2];
+        q[d1] = x1 * c - x2 * sn;
+        q[d2] = x2 * c + x1 * sn;
       }
     }
     /* Step 5: scores. */
@@ -262,14 +287,16 @@ static void *worker(void *arg) {
 
 /* Runs steps 1-6 for the listed tokens. Outputs are indexed by position in
  * `tokens`: out[n_tokens][H][512], lse[n_tokens][H], kept[n_tokens],
- * checksum[n_tokens]. Returns 0, or -1 on bad arguments / out of memory. */
+ * checksum[n_tokens]. rope_style: ORACLE_ROPE_NEOX or ORACLE_ROPE_GPTJ.
+ * Returns 0, or -1 on bad arguments / out of memory. */
 int oracle_decode(int32_t H, const uint16_t *q, int64_t q_st, int64_t q_sh,
                   const oracle_cache *caches, const oracle_list *lists, int32_t nlists,
                   const float *sink, const int64_t *positions, const float *cos_sin,
-                  int64_t cs_rows, double scale, const int32_t *tokens, int32_t n_tokens,
-                  double *out, double *lse, int32_t *kept, uint32_t *checksum,
-                  int32_t nthreads) {
+                  int64_t cs_rows, int32_t rope_style, double scale, const int32_t *tokens,
+                  int32_t n_tokens, double *out, double *lse, int32_t *kept,
+                  uint32_t *checksum, int32_t nthreads) {
   if (H <= 0 || !q || !caches || !lists || nlists < 1 || nlists > 2 || n_tokens < 0) return -1;
+  if (rope_style != ORACLE_ROPE_NEOX && rope_style != ORACLE_ROPE_GPTJ) return -1;
   if (cos_sin && !positions) return -1;
   if (nthreads < 1) nthreads = 1;
   if (nthreads > n_tokens && n_tokens > 0) nthreads = n_tokens;
@@ -285,6 +312,7 @@ int oracle_decode(int32_t H, const uint16_t *q, int64_t q_st, int64_t q_sh,
     J->H = H; J->q = q; J->q_st = q_st; J->q_sh = q_sh;
     J->caches = caches; J->lists = lists; J->nlists = nlists;
     J->sink = sink; J->positions = positions; J->cos_sin = cos_sin; J->cs_rows = cs_rows;
+    J->rope_style = rope_style;
     J->scale = scale; J->tokens = tokens; J->n_tokens = n_tokens;
     J->out = out; J->lse = lse; J->kept = kept; J->checksum = checksum;
     J->nthreads = nthreads; J->tid = w; J->status = 0;
@@ -315,4 +343,114 @@ int oracle_decode(int32_t H, const uint16_t *q, int64_t q_st, int64_t q_sh,
   free(jobs);
   free(th);
   return rc;
+}
+
+/* ------------------------------------------------------------------------
+ * V4.1 output epilogue (the swapab page, merge step, after the sink merge:
+ * inverse RoPE on dims >= 448, MXFP8 cast with one ue8m0 scale per 32 dims,
+ * "o-fused" store).
+ */
+
+/* Nearest E4M3 code to y, ties to the code with an even mantissa; |y| past
+ * 448 saturates to 448 (the page's cast to fp8 is a saturating one); the
+ * sign of y is kept, also for results that round to zero; NaN gives 0x7F.
+ * Brute force over the 127 finite magnitudes, whose values increase with the
+ * code, so a tie is between codes c and c + 1 and goes to the even one. */
+uint8_t oracle_e4m3_encode(double y) {
+  if (isnan(y)) return 0x7F;
+  const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+  const double a = fabs(y);
+  int best = 0;
+  double bd = INFINITY;
+  for (int c = 0; c <= 126; ++c) {
+    const double d = fabs(oracle_e4m3_value((uint8_t)c) - a);
+    if (d < bd || (d == bd && (c & 1) == 0)) {
+      bd = d;
+      best = c;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* ue8m0 byte of the smallest power of two >= v (v a positive finite fp32
+ * value): with v = f * 2^e, f in [0.5, 1), ceil(log2 v) is e - 1 when
+ * f = 0.5 (v a power of two) and e otherwise; biased by 127 and saturated
+ * to 0..254 (0xFF is NaN in E8M0). */
+uint8_t oracle_ue8m0_ceil(float v) {
+  int e = 0;
+  const double f = frexp((double)v, &e);
+  int E = (f == 0.5) ? e - 1 : e;
+  int b = E + 127;
+  if (b < 0) b = 0;
+  if (b > 254) b = 254;
+  return (uint8_t)b;
+}
+
+/* out: [n][H][512] fp64 outputs (rows of out from oracle_decode). pos: [n]
+ * the rows' positions (read only with cos_sin). cos_sin: fp32 [cs_rows][64]
+ * or NULL (no RoPE: no inverse rotation). rope_style: the pairing of the
+ * forward rotation. G: heads per output group (divides H).
+ *   1. Inverse rotation of dims >= 448 with the row's c = cos[i], s = sin[i]
+ *      (the forward rotation with s negated): x1 <- x1 c + x2 s,
+ *      x2 <- x2 c - x1 s, pairs as in step 4 of oracle_decode.
+ *   2. Each value is rounded to fp32: the page takes the scale and code
+ *      decisions in fp32.
+ *   3. Per head h and 32-dim chunk cc: amax = max(max_d |x|, 1e-10) and
+ *      v = amax * fp32(1/448), a product rounded to fp32; scale byte
+ *      E = oracle_ue8m0_ceil(v) (= ceil(log2(amax / 448)) + 127); the code of
+ *      x is oracle_e4m3_encode(x * 2^(127 - E)) (the product is exact).
+ *   4. o-fused layout: group g = h / G, slot ka = cc * G + h % G;
+ *      codes[n][H/G][G*512] at [g][ka*32 + d%32], scales[n][H/G][G*16] at
+ *      [g][ka] (one byte per (head, chunk); the page packs them four to an
+ *      int32 word, little-endian, which is the same byte order).
+ * x_out (optional, [n][H][512] fp32): the values after steps 1-2.
+ * Returns 0, or -1 on bad arguments. */
+int oracle_mxfp8_epilogue(const double *out, int32_t n, int32_t H, const int64_t *pos,
+                          const float *cos_sin, int64_t cs_rows, int32_t rope_style,
+                          int32_t G, float *x_out, uint8_t *codes, uint8_t *scales) {
+  if (!out || n < 0 || H <= 0 || G <= 0 || H % G != 0 || !codes || !scales) return -1;
+  if (cos_sin && !pos) return -1;
+  if (rope_style != ORACLE_ROPE_NEOX && rope_style != ORACLE_ROPE_GPTJ) return -1;
+  const float inv448 = 1.0f / 448.0f;
+  for (int32_t r = 0; r < n; ++r) {
+    if (cos_sin && (pos[r] < 0 || pos[r] >= cs_rows)) return -1;
+    for (int32_t h = 0; h < H; ++h) {
+      double o[ORACLE_D];
+      memcpy(o, out + ((int64_t)r * H + h) * ORACLE_D, sizeof(o));
+      if (cos_sin) {
+        const float *row = cos_sin + pos[r] * 64;
+        for (int i = 0; i < ORACLE_ROPE_HALF; ++i) {
+          const double c = (double)row[i], sn = (double)row[ORACLE_ROPE_HALF + i];
+          int d1, d2;
+          if (rope_style == ORACLE_ROPE_GPTJ) {
+            d1 = ORACLE_ROPE_START + 2 * i;
+            d2 = d1 + 1;
+          } else {
+            d1 = ORACLE_ROPE_START + i;
+            d2 = d1 + ORACLE_ROPE_HALF;
+          }
+          const double x1 = o[d1], x2 = o[d2];
+          o[d1] = x1 * c + x2 * sn;
+          o[d2] = x2 * c - x1 * sn;
+        }
+      }
+      float x[ORACLE_D];
+      for (int d = 0; d < ORACLE_D; ++d) x[d] = (float)o[d];
+      if (x_out) memcpy(x_out + ((int64_t)r * H + h) * ORACLE_D, x, sizeof(x));
+      const int32_t g = h / G, hg = h % G;
+      for (int cc = 0; cc < ORACLE_D / 32; ++cc) {
+        float amax = 0.0f;
+        for (int d = 32 * cc; d < 32 * cc + 32; ++d) amax = fmaxf(amax, fabsf(x[d]));
+        amax = fmaxf(amax, 1e-10f);
+        const float v = amax * inv448;
+        const uint8_t E = oracle_ue8m0_ceil(v);
+        const int64_t ka = (int64_t)cc * G + hg;
+        uint8_t *crow = codes + ((int64_t)r * (H / G) + g) * ((int64_t)G * ORACLE_D);
+        for (int d = 32 * cc; d < 32 * cc + 32; ++d)
+          crow[ka * 32 + d % 32] = oracle_e4m3_encode(ldexp((double)x[d], 127 - (int)E));
+        scales[((int64_t)r * (H / G) + g) * ((int64_t)G * 16) + ka] = E;
+      }
+    }
+  }
+  return 0;
 }

@@ -15,6 +15,11 @@ workloads of this method):
     i, 2i+1 in the high nibble), then 32 e4m3 scales, one per 16 dims;
     scale = e4m3(block absmax / 6), code = e2m1 round-to-nearest-even of
     x / scale, saturated at +-6.
+  * fp8-528 with ue8m0 scales (the V4.1 record of the swapab page): 512 e4m3
+    codes, then 16 ue8m0 bytes, one per 32 dims; scale = 2^ceil(log2(group
+    absmax / 448)) (the page's rule for its MXFP8 output, taken for the cache
+    too), byte = exponent + 127, code = e4m3 round-to-nearest-even of
+    x / scale.
 
 The five named workloads follow the configurations the method is measured on
 (T tokens, H query heads, one shared 512-dim KV row per slot). Seeds: workload
@@ -32,7 +37,12 @@ import torch
 HEAD_DIM = 512
 FMT_FP8_528 = 0
 FMT_NVFP4_288 = 1
-RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288}
+FMT_FP8_528_UE8M0 = 2
+RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288, FMT_FP8_528_UE8M0: 528}
+FMT_NAMES = {FMT_FP8_528: "fp8_528", FMT_NVFP4_288: "nvfp4_288",
+             FMT_FP8_528_UE8M0: "fp8_528_ue8m0"}
+ROPE_NEOX = 0   # dim 448+i pairs with 480+i
+ROPE_GPTJ = 1   # dim 448+2i pairs with 449+2i
 ROPE_TABLE_ROWS = 131072
 ROPE_THETA = 10000.0
 
@@ -90,6 +100,7 @@ class Workload:
     sink: Optional[torch.Tensor] = None  # fp32 [H]
     positions: Optional[torch.Tensor] = None  # int64 [T]
     cos_sin: Optional[torch.Tensor] = None    # fp32 [ROPE_TABLE_ROWS, 64]
+    rope_style: int = ROPE_NEOX
 
     def to(self, device) -> "Workload":
         f = lambda x: None if x is None else x.to(device)
@@ -97,7 +108,7 @@ class Workload:
                         self.swa_cache.to(device), self.swa.to(device),
                         None if self.extra_cache is None else self.extra_cache.to(device),
                         None if self.extra is None else self.extra.to(device),
-                        f(self.sink), f(self.positions), f(self.cos_sin))
+                        f(self.sink), f(self.positions), f(self.cos_sin), self.rope_style)
 
 
 # --------------------------------------------------------------------------
@@ -113,6 +124,19 @@ def encode_fp8_records(x: torch.Tensor) -> torch.Tensor:
     y = (xb / safe[..., None]).clamp(-448.0, 448.0)
     codes = y.to(torch.float8_e4m3fn).view(torch.uint8).reshape(n, 512)
     sbytes = scale.contiguous().view(torch.uint8).reshape(n, 16)  # little endian
+    return torch.cat([codes, sbytes], dim=1)
+
+
+def encode_fp8_ue8m0_records(x: torch.Tensor) -> torch.Tensor:
+    """[n, 512] float -> [n, 528] uint8 fp8-528 records with ue8m0 scales."""
+    n = x.shape[0]
+    xb = x.float().reshape(n, 16, 32)
+    amax = xb.abs().amax(dim=-1).double()                       # [n, 16]
+    ex = torch.where(amax > 0, torch.ceil(torch.log2(amax / 448.0)), torch.zeros_like(amax))
+    ex = ex.clamp(-127, 127)
+    y = (xb.double() / torch.exp2(ex)[..., None]).clamp(-448.0, 448.0).float()
+    codes = y.to(torch.float8_e4m3fn).view(torch.uint8).reshape(n, 512)
+    sbytes = (ex + 127).to(torch.uint8)
     return torch.cat([codes, sbytes], dim=1)
 
 
@@ -152,7 +176,8 @@ def make_cache(num_slots: int, page_size: int, fmt: int, gen: torch.Generator,
     stride = page_size * rb + page_pad
     data = torch.zeros((num_pages, stride), dtype=torch.uint8, device=device)
     recs = data[:, :page_size * rb].view(num_pages, page_size, rb)
-    enc = encode_fp8_records if fmt == FMT_FP8_528 else encode_nvfp4_records
+    enc = {FMT_FP8_528: encode_fp8_records, FMT_NVFP4_288: encode_nvfp4_records,
+           FMT_FP8_528_UE8M0: encode_fp8_ue8m0_records}[fmt]
     chunk = max(page_size, chunk - chunk % page_size)
     for s0 in range(0, num_slots, chunk):
         s1 = min(num_slots, s0 + chunk)          # both multiples of page_size
@@ -205,7 +230,7 @@ def _lens(T, width, lens, gen, device):
 def make_workload(*, T: int, H: int, swa: dict, extra: Optional[dict] = None,
                   sink: bool = False, rope: bool = False, seed: int = 0,
                   device="cpu", name: str = "custom", page_pad: int = 0,
-                  scale: Optional[float] = None) -> Workload:
+                  scale: Optional[float] = None, rope_style: int = ROPE_NEOX) -> Workload:
     """Build a workload.
 
     swa / extra: dict(width, lens=(lo, hi) inclusive or "full", fmt, page,
@@ -238,7 +263,7 @@ def make_workload(*, T: int, H: int, swa: dict, extra: Optional[dict] = None,
     return Workload(name, T, H, scale if scale is not None else HEAD_DIM ** -0.5, q,
                     caches[0], lists[0],
                     caches[1] if extra is not None else None,
-                    lists[1] if extra is not None else None, sk, pos, cs)
+                    lists[1] if extra is not None else None, sk, pos, cs, rope_style)
 
 
 # The five measured configurations (sizes as stated; the open choices -- full
@@ -281,12 +306,13 @@ def workload_summary(w: Workload) -> dict:
     """Shape description (no selection arithmetic)."""
     def cache(c):
         return None if c is None else dict(
-            fmt=["fp8_528", "nvfp4_288"][c.fmt], page=c.page_size, slots=c.num_slots,
+            fmt=FMT_NAMES[c.fmt], page=c.page_size, slots=c.num_slots,
             bytes=int(c.data.numel()))
     return dict(workload=w.name, T=w.T, H=w.H, swa_width=w.swa.width,
                 extra_width=0 if w.extra is None else w.extra.width,
                 swa_cache=cache(w.swa_cache), extra_cache=cache(w.extra_cache),
-                sink=w.sink is not None, rope=w.cos_sin is not None)
+                sink=w.sink is not None, rope=w.cos_sin is not None,
+                rope_style=["neox", "gptj"][w.rope_style])
 
 
 def oracle_args(w: Workload) -> dict:
@@ -304,4 +330,4 @@ def oracle_args(w: Workload) -> dict:
                            format=w.extra_cache.fmt))
         lists.append(dict(ids=w.extra.ids, lens=w.extra.lens, width=w.extra.width))
     return dict(q=w.q, caches=caches, lists=lists, scale=w.scale, sink=w.sink,
-                positions=w.positions, cos_sin=w.cos_sin)
+                positions=w.positions, cos_sin=w.cos_sin, rope_style=w.rope_style)

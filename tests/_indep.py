@@ -24,6 +24,9 @@ def lib_dequant(rec: np.ndarray, fmt: int) -> np.ndarray:
         codes = lib_e4m3(rec[:512])
         scales = np.frombuffer(rec[512:528].tobytes(), dtype="<f4").astype(np.float64)
         return codes * np.repeat(scales, 128)
+    if fmt == 2:   # ue8m0 byte b = 2^(b - 127), one per 32 dims
+        codes = lib_e4m3(rec[:512])
+        return np.ldexp(codes, np.repeat(rec[512:528].astype(np.int64) - 127, 32))
     nib = np.empty(512, dtype=np.uint8)
     nib[0::2] = rec[:256] & 0xF
     nib[1::2] = rec[:256] >> 4
@@ -59,11 +62,47 @@ def q_rows(w, t: int) -> np.ndarray:
     q = w.q[t].to(torch.float64).numpy().copy()
     if w.cos_sin is not None:
         row = w.cos_sin[int(w.positions[t])].to(torch.float64).numpy()
-        rot = row[:32] + 1j * row[32:]
-        z = (q[:, 448:480] + 1j * q[:, 480:512]) * rot[None, :]
-        q[:, 448:480] = z.real
-        q[:, 480:512] = z.imag
+        rotate_rope(q, row, getattr(w, "rope_style", 0))
     return q
+
+
+def rotate_rope(x: np.ndarray, row: np.ndarray, style: int, inverse: bool = False) -> None:
+    """In place on x [..., 512]: the rope dims as complex numbers times
+    cos + i sin (conjugate for the inverse). NeoX (style 0): real parts are
+    dims 448..479, imaginary parts 480..511; GPT-J (style 1): real parts the
+    even dims of 448..511, imaginary parts the odd ones."""
+    rot = row[:32] + 1j * row[32:]
+    if inverse:
+        rot = np.conj(rot)
+    if style == 0:
+        re, im = slice(448, 480), slice(480, 512)
+    else:
+        re, im = slice(448, 512, 2), slice(449, 512, 2)
+    z = (x[..., re] + 1j * x[..., im]) * rot
+    x[..., re] = z.real
+    x[..., im] = z.imag
+
+
+def lib_mxfp8(x: np.ndarray, G: int):
+    """MXFP8 cast and o-fused layout of fp32 values x [n, H, 512] with torch
+    ops: per (head, 32 dims) amax (floor 1e-10) times fp32(1/448) in fp32,
+    exponent = ceil(log2) of that (float64 log2 of an fp32 value), codes by
+    torch's round-to-nearest-even float8_e4m3fn conversion of x * 2^-exponent
+    (clamped to +-448: a saturating cast). Returns (codes [n, H/G, G*512],
+    scale bytes [n, H/G, G*16])."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    n, H, _ = t.shape
+    c = t.reshape(n, H, 16, 32)
+    amax = c.abs().amax(dim=-1).clamp(min=1e-10)
+    v = amax * torch.tensor(1.0 / 448.0, dtype=torch.float32)
+    e = torch.ceil(torch.log2(v.double()))
+    y = (c.double() * torch.exp2(-e)[..., None]).clamp(-448.0, 448.0).float()
+    codes = y.to(torch.float8_e4m3fn).view(torch.uint8)          # [n, H, 16, 32]
+    sc = (e + 127).clamp(0, 254).to(torch.uint8)                  # [n, H, 16]
+    # o-fused: group g = h // G, slot ka = chunk * G + h % G
+    codes = codes.reshape(n, H // G, G, 16, 32).permute(0, 1, 3, 2, 4).reshape(n, H // G, G * 512)
+    sc = sc.reshape(n, H // G, G, 16).permute(0, 1, 3, 2).reshape(n, H // G, G * 16)
+    return codes.numpy(), sc.numpy()
 
 
 def fmix32(h: int) -> int:

@@ -16,7 +16,7 @@ LSE_ATOL = 1e-3
 def oracle_ref(w: W.Workload, tokens=None):
     a = W.oracle_args(w)
     return oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
-                         positions=a["positions"], cos_sin=a["cos_sin"], tokens=tokens)
+                         positions=a["positions"], cos_sin=a["cos_sin"], rope_style=a["rope_style"], tokens=tokens)
 
 
 def run_gpu(w: W.Workload, num_sms: int = 0):

@@ -23,7 +23,7 @@ def run(w, tokens=None, **over):
     a = W.oracle_args(w)
     a.update(over)
     return oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
-                         positions=a["positions"], cos_sin=a["cos_sin"], tokens=tokens,
+                         positions=a["positions"], cos_sin=a["cos_sin"], rope_style=a["rope_style"], tokens=tokens,
                          nthreads=2)
 
 
@@ -302,7 +302,7 @@ def test_split_invariance_via_combine():
                 keep[:, r0:r1] = True
             l["ids"] = torch.where(keep, ids, torch.full_like(ids, -1))
         o, l_, _, _ = oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"],
-                                    positions=a["positions"], cos_sin=a["cos_sin"])
+                                    positions=a["positions"], cos_sin=a["cos_sin"], rope_style=a["rope_style"])
         p_out.append(o)
         p_lse.append(l_)
     out_c, lse_c = oracle.combine(p_out, p_lse, sink=w.sink.double().numpy()[None, :])
