@@ -60,10 +60,22 @@ typedef enum {
  *            dims); value = code * scale.
  * NVFP4_288: 256 bytes of e2m1 nibbles (element 2i in the low nibble of byte
  *            i), then 32 e4m3 scales (one per 16 dims); value = code * scale.
+ * FP8_528_UE8M0: 512 e4m3 codes, then 16 ue8m0 scale bytes (one per 32
+ *            dims); value = code * 2^(byte - 127) (the V4.1 record of the
+ *            swapab page, stage_inputs fp8 branch). The kernels compute in
+ *            f16 tiles: values are exact while every scale exponent
+ *            byte - 127 lies in [-15, 7]; outside that range they are rounded
+ *            to f16 (a scale byte of 0xFF, NaN in E8M0, gives non-finite
+ *            values).
  * Source: the swapab page (record sizes 528 and 288, NVFP4 block of 16 with
  * e4m3 scales) with the fp32-per-128 scale layout of FlashMLA's V3.2 record
  * (sparse_decode.h, bytes_per_token = 512 + ... + (512/128)*4).            */
-enum { DSA_REC_FP8_528 = 0, DSA_REC_NVFP4_288 = 1 };
+enum { DSA_REC_FP8_528 = 0, DSA_REC_NVFP4_288 = 1, DSA_REC_FP8_528_UE8M0 = 2 };
+
+/* RoPE pairings of q dims 448..511 with a table row [cos(32) | sin(32)]:
+ * NEOX pairs dim 448+i with 480+i, GPTJ pairs 448+2i with 449+2i (the swapab
+ * page's Q RoPE); pair i uses cos[i], sin[i]. */
+enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 };
 
 /* A paged cache: base[num_pages][page_stride_bytes] bytes; the record of slot
  * s lies at base + (s / page_size) * page_stride_bytes
@@ -173,6 +185,61 @@ dsa_status dsa_decode_combine(const dsa_decode_plan_t *plan, void *workspace,
                               size_t workspace_bytes, const float *sink, void *out,
                               float *lse, dsa_stream_t stream);
 
+/* MXFP8 output of the V4.1 epilogue (the swapab page's merge step: inverse
+ * RoPE, MXFP8 cast, "o-fused" store). For token t, head h, dim d, with
+ * G = group_size, g = h / G, chunk c = d / 32 and slot ka = c * G + h % G:
+ *   code (e4m3) at  (uint8_t *)data + t*data_stride_t + g*data_stride_g
+ *                   + ka*32 + d % 32;
+ *   scale (ue8m0 byte, one per head and chunk) = byte ka % 4 (little-endian)
+ *                   of the int32 word scale[t*scale_stride_t + g*scale_stride_g
+ *                   + (ka / 4)*scale_stride_w].
+ * The value stored is x * 2^(127 - E) cast to e4m3 (round to nearest even,
+ * saturating), E = ceil(log2(max(amax, 1e-10) * fp32(1/448))) + 127, amax =
+ * max |x| over the chunk, x the fp32 output after the inverse rotation of
+ * dims >= 448 (when RoPE is on).
+ * data: 4-byte aligned, data strides multiples of 4. scale: 4-byte aligned.
+ * group_size >= 1 and divides num_heads. The caller owns both buffers. */
+typedef struct {
+  void *data;
+  int32_t *scale;
+  int64_t data_stride_t;   /* bytes  */
+  int64_t data_stride_g;   /* bytes  */
+  int64_t scale_stride_t;  /* int32 words */
+  int64_t scale_stride_g;
+  int64_t scale_stride_w;
+  int32_t group_size;
+  int32_t reserved;
+} dsa_mxfp8_out;
+
+/* dsa_decode_run with the V4.1 options (the swapab page's mega-kernel call):
+ *   rope_style: DSA_ROPE_NEOX or DSA_ROPE_GPTJ (used when RoPE is on).
+ *   out / mx  : exactly one non-NULL. out: bf16 [T, H, 512] as in
+ *               dsa_decode_run. mx: MXFP8 output; with RoPE on, dims >= 448
+ *               of the output are first rotated back (the inverse of the Q
+ *               rotation, same table row); that inverse is implemented for
+ *               DSA_ROPE_GPTJ only (NEOX with RoPE and mx: DSA_ERR_UNSUPPORTED).
+ * Every other argument as for dsa_decode_run. Split tokens get their output
+ * from dsa_decode_combine_v41 (same rope_style, positions, cos_sin, out / mx). */
+dsa_status dsa_decode_run_v41(const dsa_decode_plan_t *plan, void *workspace,
+                              size_t workspace_bytes, const void *q, int64_t q_stride_t,
+                              int64_t q_stride_h, const dsa_cache_desc *swa_cache,
+                              const int32_t *swa_idx, int64_t swa_idx_stride,
+                              const int32_t *swa_lens, const dsa_cache_desc *extra_cache,
+                              const int32_t *extra_idx, int64_t extra_idx_stride,
+                              const int32_t *extra_lens, const float *sink,
+                              const int64_t *positions, const float *cos_sin,
+                              int64_t cos_sin_rows, int32_t rope_style, float scale,
+                              void *out, const dsa_mxfp8_out *mx, float *lse,
+                              dsa_stream_t stream);
+
+/* dsa_decode_combine for dsa_decode_run_v41: the same plan, workspace, sink,
+ * positions, cos_sin, rope_style and output (out or mx) as given to run. */
+dsa_status dsa_decode_combine_v41(const dsa_decode_plan_t *plan, void *workspace,
+                                  size_t workspace_bytes, const float *sink,
+                                  const int64_t *positions, const float *cos_sin,
+                                  int64_t cos_sin_rows, int32_t rope_style, void *out,
+                                  const dsa_mxfp8_out *mx, float *lse, dsa_stream_t stream);
+
 /* Row-selection record of the last run+combine on this workspace: per token
  * the number of kept rows (kept[T], int32, device) and the sum mod 2^32 over
  * kept rows of fmix32(id * 0x9E3779B1 + 2*position + list) (checksum[T],
@@ -230,7 +297,7 @@ const char *dsa_decode_status_string(dsa_status s);
 /* ABI version of this header (bumped on any layout change). */
 int32_t dsa_decode_abi_version(void);
 
-#define DSA_DECODE_ABI_VERSION 2
+#define DSA_DECODE_ABI_VERSION 3
 
 #ifdef __cplusplus
 }

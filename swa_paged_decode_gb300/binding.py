@@ -23,7 +23,10 @@ STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED
                 -3: "DSA_ERR_ALIGNMENT", -4: "DSA_ERR_WORKSPACE", -5: "DSA_ERR_CUDA",
                 -6: "DSA_ERR_TIMEOUT", -7: "DSA_ERR_PLAN"}
 EXPORTED = ("dsa_decode_plan", "dsa_decode_run", "dsa_decode_combine", "dsa_decode_selection",
-            "dsa_decode_read_status", "dsa_decode_status_string", "dsa_decode_abi_version")
+            "dsa_decode_read_status", "dsa_decode_status_string", "dsa_decode_abi_version",
+            "dsa_decode_run_noalloc", "dsa_decode_run_v41", "dsa_decode_combine_v41")
+DSA_ROPE_NEOX = 0
+DSA_ROPE_GPTJ = 1
 
 
 class DsaError(RuntimeError):
@@ -50,6 +53,35 @@ class Plan(ctypes.Structure):
 
 
 _lib = None
+
+
+class MxOutDesc(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("data_stride_t", ctypes.c_int64), ("data_stride_g", ctypes.c_int64),
+                ("scale_stride_t", ctypes.c_int64), ("scale_stride_g", ctypes.c_int64),
+                ("scale_stride_w", ctypes.c_int64), ("group_size", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class MxOut:
+    """MXFP8 output buffers in the o-fused layout: data uint8 [T, H/G, G*512]
+    (e4m3 codes), scale int32 [T, H/G, G*4] (ue8m0 bytes, four to a word)."""
+
+    def __init__(self, T: int, H: int, group_size: int, device):
+        assert H % group_size == 0
+        G = group_size
+        self.group_size = G
+        self.data = torch.zeros((T, H // G, G * W.HEAD_DIM), dtype=torch.uint8, device=device)
+        self.scale = torch.zeros((T, H // G, G * 4), dtype=torch.int32, device=device)
+
+    def desc(self) -> MxOutDesc:
+        d, s = self.data, self.scale
+        return MxOutDesc(d.data_ptr(), s.data_ptr(), d.stride(0), d.stride(1), s.stride(0),
+                         s.stride(1), s.stride(2), self.group_size, 0)
+
+    def scale_bytes(self) -> torch.Tensor:
+        """[T, H/G, G*16] uint8 (byte ka of a group's scales, little-endian words)."""
+        return self.scale.contiguous().view(torch.uint8)
 
 
 def load(path: str = LIB_PATH):
@@ -81,6 +113,15 @@ def load(path: str = LIB_PATH):
                                            ctypes.POINTER(CacheDesc), vp, i64, vp,
                                            ctypes.POINTER(CacheDesc), vp, i64, vp,
                                            vp, vp, vp, i64, ctypes.c_float, vp, vp, vp, vp]
+    lib.dsa_decode_run_v41.restype = ctypes.c_int
+    lib.dsa_decode_run_v41.argtypes = [ctypes.POINTER(Plan), vp, ctypes.c_size_t, vp, i64, i64,
+                                       ctypes.POINTER(CacheDesc), vp, i64, vp,
+                                       ctypes.POINTER(CacheDesc), vp, i64, vp,
+                                       vp, vp, vp, i64, i32, ctypes.c_float, vp,
+                                       ctypes.POINTER(MxOutDesc), vp, vp]
+    lib.dsa_decode_combine_v41.restype = ctypes.c_int
+    lib.dsa_decode_combine_v41.argtypes = [ctypes.POINTER(Plan), vp, ctypes.c_size_t, vp, vp, vp,
+                                           i64, i32, vp, ctypes.POINTER(MxOutDesc), vp, vp]
     lib.dsa_decode_status_string.restype = ctypes.c_char_p
     lib.dsa_decode_status_string.argtypes = [ctypes.c_int]
     lib.dsa_decode_abi_version.restype = ctypes.c_int32
@@ -153,6 +194,46 @@ def dsa_decode_combine(plan: Plan, workspace: Optional[torch.Tensor], sink: Opti
     return rc
 
 
+def dsa_decode_run_v41(plan: Plan, workspace: Optional[torch.Tensor], q: torch.Tensor,
+                       swa_cache: W.PagedCache, swa_idx: torch.Tensor, swa_lens: torch.Tensor,
+                       extra_cache: Optional[W.PagedCache], extra_idx: Optional[torch.Tensor],
+                       extra_lens: Optional[torch.Tensor], sink: Optional[torch.Tensor],
+                       positions: Optional[torch.Tensor], cos_sin: Optional[torch.Tensor],
+                       rope_style: int, scale: float, out: Optional[torch.Tensor],
+                       mx: Optional[MxOut], lse: torch.Tensor, stream=None,
+                       check: bool = True) -> int:
+    sc, ec = cache_desc(swa_cache), cache_desc(extra_cache)
+    md = None if mx is None else mx.desc()
+    rc = load().dsa_decode_run_v41(
+        ctypes.byref(plan), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        q.data_ptr(), q.stride(0), q.stride(1),
+        ctypes.byref(sc), swa_idx.data_ptr(), swa_idx.stride(0), swa_lens.data_ptr(),
+        None if ec is None else ctypes.byref(ec), _ptr(extra_idx),
+        0 if extra_idx is None else extra_idx.stride(0), _ptr(extra_lens),
+        _ptr(sink), _ptr(positions), _ptr(cos_sin),
+        0 if cos_sin is None else cos_sin.shape[0], int(rope_style), float(scale),
+        _ptr(out), None if md is None else ctypes.byref(md), lse.data_ptr(), _stream(stream))
+    if check:
+        _check("dsa_decode_run_v41", rc)
+    return rc
+
+
+def dsa_decode_combine_v41(plan: Plan, workspace: Optional[torch.Tensor],
+                           sink: Optional[torch.Tensor], positions: Optional[torch.Tensor],
+                           cos_sin: Optional[torch.Tensor], rope_style: int,
+                           out: Optional[torch.Tensor], mx: Optional[MxOut], lse: torch.Tensor,
+                           stream=None, check: bool = True) -> int:
+    md = None if mx is None else mx.desc()
+    rc = load().dsa_decode_combine_v41(
+        ctypes.byref(plan), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _ptr(sink), _ptr(positions), _ptr(cos_sin), 0 if cos_sin is None else cos_sin.shape[0],
+        int(rope_style), _ptr(out), None if md is None else ctypes.byref(md), lse.data_ptr(),
+        _stream(stream))
+    if check:
+        _check("dsa_decode_combine_v41", rc)
+    return rc
+
+
 def dsa_decode_selection(plan: Plan, workspace: torch.Tensor, kept: torch.Tensor,
                          checksum: torch.Tensor, stream=None):
     _check("dsa_decode_selection", load().dsa_decode_selection(
@@ -192,26 +273,40 @@ def dsa_decode_run_noalloc(plan: Plan, q: torch.Tensor, swa_cache: W.PagedCache,
 
 class Decoder:
     """Plan + workspace for one workload shape; ``__call__`` runs run+combine
-    on the current stream. Allocation uses torch; compute is the library's."""
+    on the current stream. Allocation uses torch; compute is the library's.
+    With ``mx_group`` the output is MXFP8 (``self.mx``, o-fused with that many
+    heads per group) instead of bf16 ``self.out``; a GPT-J workload or an
+    MXFP8 output goes through the V4.1 entry points."""
 
-    def __init__(self, w: W.Workload, num_sms: int = 0):
+    def __init__(self, w: W.Workload, num_sms: int = 0, mx_group: Optional[int] = None):
         self.plan, nbytes = dsa_decode_plan(w.T, w.H, w.swa.width,
                                             0 if w.extra is None else w.extra.width, num_sms)
         dev = w.q.device
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
-        self.out = torch.empty((w.T, w.H, W.HEAD_DIM), dtype=torch.bfloat16, device=dev)
+        self.mx = None if mx_group is None else MxOut(w.T, w.H, mx_group, dev)
+        self.out = (torch.empty((w.T, w.H, W.HEAD_DIM), dtype=torch.bfloat16, device=dev)
+                    if self.mx is None else None)
         self.lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
 
     def __call__(self, w: W.Workload, stream=None):
-        dsa_decode_run(self.plan, self.workspace, w.q, w.swa_cache, w.swa.ids, w.swa.lens,
-                       w.extra_cache, None if w.extra is None else w.extra.ids,
-                       None if w.extra is None else w.extra.lens, w.sink, w.positions,
-                       w.cos_sin, w.scale, self.out, self.lse, stream)
-        dsa_decode_combine(self.plan, self.workspace, w.sink, self.out, self.lse, stream)
-        return self.out, self.lse
+        ei = None if w.extra is None else w.extra.ids
+        el = None if w.extra is None else w.extra.lens
+        if self.mx is None and w.rope_style == DSA_ROPE_NEOX:
+            dsa_decode_run(self.plan, self.workspace, w.q, w.swa_cache, w.swa.ids, w.swa.lens,
+                           w.extra_cache, ei, el, w.sink, w.positions, w.cos_sin, w.scale,
+                           self.out, self.lse, stream)
+            dsa_decode_combine(self.plan, self.workspace, w.sink, self.out, self.lse, stream)
+            return self.out, self.lse
+        dsa_decode_run_v41(self.plan, self.workspace, w.q, w.swa_cache, w.swa.ids, w.swa.lens,
+                           w.extra_cache, ei, el, w.sink, w.positions, w.cos_sin, w.rope_style,
+                           w.scale, self.out, self.mx, self.lse, stream)
+        dsa_decode_combine_v41(self.plan, self.workspace, w.sink, w.positions, w.cos_sin,
+                               w.rope_style, self.out, self.mx, self.lse, stream)
+        return (self.out if self.mx is None else self.mx), self.lse
 
     def selection(self, stream=None):
-        kept = torch.empty(self.plan.num_tokens, dtype=torch.int32, device=self.out.device)
-        chk = torch.empty(self.plan.num_tokens, dtype=torch.int32, device=self.out.device)
+        dev = self.lse.device
+        kept = torch.empty(self.plan.num_tokens, dtype=torch.int32, device=dev)
+        chk = torch.empty(self.plan.num_tokens, dtype=torch.int32, device=dev)
         dsa_decode_selection(self.plan, self.workspace, kept, chk, stream)
         return kept, chk

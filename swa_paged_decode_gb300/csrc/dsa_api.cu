@@ -42,7 +42,8 @@ int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 int record_bytes(int32_t fmt) {
-  return fmt == DSA_REC_FP8_528 ? 528 : (fmt == DSA_REC_NVFP4_288 ? 288 : -1);
+  if (fmt == DSA_REC_FP8_528 || fmt == DSA_REC_FP8_528_UE8M0) return 528;
+  return fmt == DSA_REC_NVFP4_288 ? 288 : -1;
 }
 
 bool heads_supported(int32_t H) {
@@ -103,6 +104,124 @@ void fill_schedule(const dsa_decode_plan_t *plan, void *ws, Params &p) {
 }
 
 dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+// Output options shared by run and combine: bf16 `out` or the MXFP8
+// descriptor, the RoPE pairing and the inverse-rotation rule.
+dsa_status fill_output(const dsa_decode_plan_t *plan, const int64_t *positions,
+                       const float *cos_sin, int64_t cos_sin_rows, int32_t rope_style, void *out,
+                       const dsa_mxfp8_out *mx, Params &p) {
+  if (rope_style != DSA_ROPE_NEOX && rope_style != DSA_ROPE_GPTJ) return DSA_ERR_INVALID_ARG;
+  if ((out == nullptr) == (mx == nullptr)) return DSA_ERR_INVALID_ARG;
+  p.rope_gptj = rope_style == DSA_ROPE_GPTJ ? 1 : 0;
+  p.positions = positions;
+  p.cos_sin = cos_sin;
+  p.cs_rows = cos_sin_rows;
+  if (out) {
+    if (!aligned(out, 16)) return DSA_ERR_ALIGNMENT;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    return DSA_OK;
+  }
+  if (!mx->data || !mx->scale || mx->group_size < 1 || plan->num_heads % mx->group_size != 0)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(mx->data, 4) || mx->data_stride_t % 4 != 0 || mx->data_stride_g % 4 != 0 ||
+      !aligned(mx->scale, 4))
+    return DSA_ERR_ALIGNMENT;
+  if (cos_sin && rope_style == DSA_ROPE_NEOX) return DSA_ERR_UNSUPPORTED;
+  p.mx_on = 1;
+  p.mx_g = mx->group_size;
+  p.mx_data = static_cast<uint8_t *>(mx->data);
+  p.mx_scale = reinterpret_cast<uint8_t *>(mx->scale);
+  p.mx_st = mx->data_stride_t;
+  p.mx_sg = mx->data_stride_g;
+  p.mx_sst = mx->scale_stride_t;
+  p.mx_ssg = mx->scale_stride_g;
+  p.mx_ssw = mx->scale_stride_w;
+  return DSA_OK;
+}
+
+dsa_status run_impl(const dsa_decode_plan_t *plan, void *workspace, size_t workspace_bytes,
+                    const void *q, int64_t q_stride_t, int64_t q_stride_h,
+                    const dsa_cache_desc *swa_cache, const int32_t *swa_idx,
+                    int64_t swa_idx_stride, const int32_t *swa_lens,
+                    const dsa_cache_desc *extra_cache, const int32_t *extra_idx,
+                    int64_t extra_idx_stride, const int32_t *extra_lens, const float *sink,
+                    const int64_t *positions, const float *cos_sin, int64_t cos_sin_rows,
+                    int32_t rope_style, float scale, void *out, const dsa_mxfp8_out *mx,
+                    float *lse, dsa_stream_t stream) {
+  if (!plan_ok(plan)) return DSA_ERR_PLAN;
+  if (plan->num_tokens == 0) return DSA_OK;
+  if (!q || !lse) return DSA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return DSA_ERR_INVALID_ARG;
+  if (q_stride_h < dsa::kD || q_stride_t < (int64_t)plan->num_heads * q_stride_h)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || q_stride_t % 8 != 0 || q_stride_h % 8 != 0) return DSA_ERR_ALIGNMENT;
+  if (!aligned(lse, 4)) return DSA_ERR_ALIGNMENT;
+  const bool has_extra = plan->extra_width > 0;
+  if (has_extra != (extra_cache != nullptr) || has_extra != (extra_idx != nullptr) ||
+      has_extra != (extra_lens != nullptr))
+    return DSA_ERR_INVALID_ARG;
+  if ((positions == nullptr) != (cos_sin == nullptr)) return DSA_ERR_INVALID_ARG;
+  if (cos_sin && (cos_sin_rows < 1 || !aligned(cos_sin, 16) || !aligned(positions, 8)))
+    return cos_sin_rows < 1 ? DSA_ERR_INVALID_ARG : DSA_ERR_ALIGNMENT;
+  if (sink && !aligned(sink, 4)) return DSA_ERR_ALIGNMENT;
+  if (!workspace || (int64_t)workspace_bytes < plan->workspace_bytes ||
+      !aligned(workspace, kAlignWs))
+    return DSA_ERR_WORKSPACE;
+
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  dsa_status s = fill_output(plan, positions, cos_sin, cos_sin_rows, rope_style, out, mx, p);
+  if (s != DSA_OK) return s;
+  s = fill_list(swa_cache, swa_idx, swa_idx_stride, swa_lens, plan->swa_width, p.list[0]);
+  if (s != DSA_OK) return s;
+  p.nlists = 1;
+  if (has_extra) {
+    s = fill_list(extra_cache, extra_idx, extra_idx_stride, extra_lens, plan->extra_width,
+                  p.list[1]);
+    if (s != DSA_OK) return s;
+    p.nlists = 2;
+  }
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.q_st = q_stride_t;
+  p.q_sh = q_stride_h;
+  p.sink = sink;
+  p.scale = scale;
+  p.scale_log2 = scale * dsa::kLog2e;
+  p.lse = lse;
+  fill_schedule(plan, workspace, p);
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, st);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  return cuda_status(plan->kernel == dsa::kKernelTc ? dsa_launch_tc(p, st)
+                                                    : dsa_launch_simt(p, st));
+}
+
+dsa_status combine_impl(const dsa_decode_plan_t *plan, void *workspace, size_t workspace_bytes,
+                        const float *sink, const int64_t *positions, const float *cos_sin,
+                        int64_t cos_sin_rows, int32_t rope_style, void *out,
+                        const dsa_mxfp8_out *mx, float *lse, dsa_stream_t stream) {
+  if (!plan_ok(plan)) return DSA_ERR_PLAN;
+  if (plan->num_tokens == 0 || plan->ctas_per_group <= 1) return DSA_OK;
+  if (!lse) return DSA_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || (sink && !aligned(sink, 4))) return DSA_ERR_ALIGNMENT;
+  if ((positions == nullptr) != (cos_sin == nullptr)) return DSA_ERR_INVALID_ARG;
+  if (cos_sin && (cos_sin_rows < 1 || !aligned(cos_sin, 16) || !aligned(positions, 8)))
+    return cos_sin_rows < 1 ? DSA_ERR_INVALID_ARG : DSA_ERR_ALIGNMENT;
+  if (!workspace || (int64_t)workspace_bytes < plan->workspace_bytes ||
+      !aligned(workspace, kAlignWs))
+    return DSA_ERR_WORKSPACE;
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  dsa_status s = fill_output(plan, positions, cos_sin, cos_sin_rows, rope_style, out, mx, p);
+  if (s != DSA_OK) return s;
+  fill_schedule(plan, workspace, p);
+  p.list[0].tiles = plan->tiles_swa;
+  p.list[1].tiles = plan->tiles_extra;
+  p.sink = sink;
+  p.lse = lse;
+  return cuda_status(dsa_launch_combine(p, reinterpret_cast<cudaStream_t>(stream)));
+}
 
 }  // namespace
 
@@ -206,56 +325,29 @@ dsa_status dsa_decode_run(const dsa_decode_plan_t *plan, void *workspace,
                           const int64_t *positions, const float *cos_sin,
                           int64_t cos_sin_rows, float scale, void *out, float *lse,
                           dsa_stream_t stream) {
-  if (!plan_ok(plan)) return DSA_ERR_PLAN;
-  if (plan->num_tokens == 0) return DSA_OK;
-  if (!q || !out || !lse) return DSA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return DSA_ERR_INVALID_ARG;
-  if (q_stride_h < dsa::kD || q_stride_t < (int64_t)plan->num_heads * q_stride_h)
-    return DSA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || q_stride_t % 8 != 0 || q_stride_h % 8 != 0) return DSA_ERR_ALIGNMENT;
-  if (!aligned(out, 16) || !aligned(lse, 4)) return DSA_ERR_ALIGNMENT;
-  const bool has_extra = plan->extra_width > 0;
-  if (has_extra != (extra_cache != nullptr) || has_extra != (extra_idx != nullptr) ||
-      has_extra != (extra_lens != nullptr))
-    return DSA_ERR_INVALID_ARG;
-  if ((positions == nullptr) != (cos_sin == nullptr)) return DSA_ERR_INVALID_ARG;
-  if (cos_sin && (cos_sin_rows < 1 || !aligned(cos_sin, 16) || !aligned(positions, 8)))
-    return cos_sin_rows < 1 ? DSA_ERR_INVALID_ARG : DSA_ERR_ALIGNMENT;
-  if (sink && !aligned(sink, 4)) return DSA_ERR_ALIGNMENT;
-  if (!workspace || (int64_t)workspace_bytes < plan->workspace_bytes ||
-      !aligned(workspace, kAlignWs))
-    return DSA_ERR_WORKSPACE;
+  if (!out) return plan_ok(plan) ? (plan->num_tokens == 0 ? DSA_OK : DSA_ERR_INVALID_ARG)
+                                 : DSA_ERR_PLAN;
+  return run_impl(plan, workspace, workspace_bytes, q, q_stride_t, q_stride_h, swa_cache,
+                  swa_idx, swa_idx_stride, swa_lens, extra_cache, extra_idx, extra_idx_stride,
+                  extra_lens, sink, positions, cos_sin, cos_sin_rows, DSA_ROPE_NEOX, scale, out,
+                  nullptr, lse, stream);
+}
 
-  Params p;
-  std::memset(&p, 0, sizeof(p));
-  dsa_status s = fill_list(swa_cache, swa_idx, swa_idx_stride, swa_lens, plan->swa_width,
-                           p.list[0]);
-  if (s != DSA_OK) return s;
-  p.nlists = 1;
-  if (has_extra) {
-    s = fill_list(extra_cache, extra_idx, extra_idx_stride, extra_lens, plan->extra_width,
-                  p.list[1]);
-    if (s != DSA_OK) return s;
-    p.nlists = 2;
-  }
-  p.q = static_cast<const __nv_bfloat16 *>(q);
-  p.q_st = q_stride_t;
-  p.q_sh = q_stride_h;
-  p.sink = sink;
-  p.positions = positions;
-  p.cos_sin = cos_sin;
-  p.cs_rows = cos_sin_rows;
-  p.scale = scale;
-  p.scale_log2 = scale * dsa::kLog2e;
-  p.out = static_cast<__nv_bfloat16 *>(out);
-  p.lse = lse;
-  fill_schedule(plan, workspace, p);
-
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, st);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
-  return cuda_status(plan->kernel == dsa::kKernelTc ? dsa_launch_tc(p, st)
-                                                    : dsa_launch_simt(p, st));
+dsa_status dsa_decode_run_v41(const dsa_decode_plan_t *plan, void *workspace,
+                              size_t workspace_bytes, const void *q, int64_t q_stride_t,
+                              int64_t q_stride_h, const dsa_cache_desc *swa_cache,
+                              const int32_t *swa_idx, int64_t swa_idx_stride,
+                              const int32_t *swa_lens, const dsa_cache_desc *extra_cache,
+                              const int32_t *extra_idx, int64_t extra_idx_stride,
+                              const int32_t *extra_lens, const float *sink,
+                              const int64_t *positions, const float *cos_sin,
+                              int64_t cos_sin_rows, int32_t rope_style, float scale,
+                              void *out, const dsa_mxfp8_out *mx, float *lse,
+                              dsa_stream_t stream) {
+  return run_impl(plan, workspace, workspace_bytes, q, q_stride_t, q_stride_h, swa_cache,
+                  swa_idx, swa_idx_stride, swa_lens, extra_cache, extra_idx, extra_idx_stride,
+                  extra_lens, sink, positions, cos_sin, cos_sin_rows, rope_style, scale, out, mx,
+                  lse, stream);
 }
 
 dsa_status dsa_decode_combine(const dsa_decode_plan_t *plan, void *workspace,
@@ -263,21 +355,18 @@ dsa_status dsa_decode_combine(const dsa_decode_plan_t *plan, void *workspace,
                               float *lse, dsa_stream_t stream) {
   if (!plan_ok(plan)) return DSA_ERR_PLAN;
   if (plan->num_tokens == 0 || plan->ctas_per_group <= 1) return DSA_OK;
-  if (!out || !lse) return DSA_ERR_INVALID_ARG;
-  if (!aligned(out, 16) || !aligned(lse, 4) || (sink && !aligned(sink, 4)))
-    return DSA_ERR_ALIGNMENT;
-  if (!workspace || (int64_t)workspace_bytes < plan->workspace_bytes ||
-      !aligned(workspace, kAlignWs))
-    return DSA_ERR_WORKSPACE;
-  Params p;
-  std::memset(&p, 0, sizeof(p));
-  fill_schedule(plan, workspace, p);
-  p.list[0].tiles = plan->tiles_swa;
-  p.list[1].tiles = plan->tiles_extra;
-  p.sink = sink;
-  p.out = static_cast<__nv_bfloat16 *>(out);
-  p.lse = lse;
-  return cuda_status(dsa_launch_combine(p, reinterpret_cast<cudaStream_t>(stream)));
+  if (!out) return DSA_ERR_INVALID_ARG;
+  return combine_impl(plan, workspace, workspace_bytes, sink, nullptr, nullptr, 0,
+                      DSA_ROPE_NEOX, out, nullptr, lse, stream);
+}
+
+dsa_status dsa_decode_combine_v41(const dsa_decode_plan_t *plan, void *workspace,
+                                  size_t workspace_bytes, const float *sink,
+                                  const int64_t *positions, const float *cos_sin,
+                                  int64_t cos_sin_rows, int32_t rope_style, void *out,
+                                  const dsa_mxfp8_out *mx, float *lse, dsa_stream_t stream) {
+  return combine_impl(plan, workspace, workspace_bytes, sink, positions, cos_sin, cos_sin_rows,
+                      rope_style, out, mx, lse, stream);
 }
 
 dsa_status dsa_decode_selection(const dsa_decode_plan_t *plan, const void *workspace,

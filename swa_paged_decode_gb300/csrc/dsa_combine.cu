@@ -143,10 +143,39 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
       }
     }
   }
+  // MXFP8 output: 8 consecutive lanes hold one 32-dim chunk of a head (the
+  // quarter's first dim is a multiple of 128); GPT-J pairs lie inside a
+  // thread's 4 dims.
+  const float *cs_row = p.mx_on ? mx_rope_row(p, t) : nullptr;
 #pragma unroll
   for (int k = 0; k < kItems; ++k) {
     const int e = tid + k * kCombineThreads, h = e / kQ4, d4 = dq + e % kQ4;
     const float inv = inv_s[h];
+    if (p.mx_on) {
+      const int d0 = 4 * d4;
+      float x[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv};
+      if (cs_row != nullptr && d0 >= kRopeStart) {
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+          const int i = (d0 - kRopeStart) / 2 + pr;
+          const float c = __ldg(cs_row + i), sn = __ldg(cs_row + kRopeHalf + i);
+          const float oe = x[2 * pr], oo = x[2 * pr + 1];
+          x[2 * pr] = fmaf(oe, c, sn * oo);
+          x[2 * pr + 1] = fmaf(oo, c, -(sn * oe));
+        }
+      }
+      float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+      for (int off = 4; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+      a = fmaxf(a, 1e-10f);
+      const uint32_t E = ue8m0_ceil(a * (1.0f / 448.0f));
+      const float sc = ue8m0_inverse(E);
+      const uint32_t codes = e4m3x2_rn_sat(x[0] * sc, x[1] * sc) | (e4m3x2_rn_sat(x[2] * sc, x[3] * sc) << 16);
+      const int hh = h0 + hb + h, c = d0 >> 5;
+      *reinterpret_cast<uint32_t *>(mx_chunk(p, t, hh, c) + (d0 & 31)) = codes;
+      if ((d0 & 31) == 0) *mx_scale_byte(p, t, hh, c) = (uint8_t)E;
+      continue;
+    }
     __nv_bfloat16 *o = p.out + ((int64_t)t * p.H + h0 + hb + h) * kD + 4 * d4;
     __nv_bfloat162 a = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
     __nv_bfloat162 c2 = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);

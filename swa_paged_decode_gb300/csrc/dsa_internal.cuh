@@ -50,8 +50,16 @@ struct Params {
   int64_t cs_rows;
   float scale;
   float scale_log2;            // scale * log2(e)
-  __nv_bfloat16 *out;          // [T, H, 512]
+  int32_t rope_gptj;           // RoPE pairing: 0 NeoX (448+i, 480+i), 1 GPT-J (448+2i, 449+2i)
+  __nv_bfloat16 *out;          // [T, H, 512] (bf16 output), or null with mx_on
   float *lse;                  // [T, H]
+  // MXFP8 output (V4.1 epilogue): codes and ue8m0 scales in the o-fused layout
+  int32_t mx_on;               // 1: write mx_* instead of out
+  int32_t mx_g;                // heads per output group
+  uint8_t *mx_data;            // code (t, h, d) at t*mx_st + (h/G)*mx_sg + (c*G + h%G)*32 + d%32, c = d/32
+  uint8_t *mx_scale;           // byte (t, h, c) at 4*(t*mx_sst + (h/G)*mx_ssg + (ka/4)*mx_ssw) + ka%4, ka = c*G + h%G
+  int64_t mx_st, mx_sg;        // bytes
+  int64_t mx_sst, mx_ssg, mx_ssw;   // int32 words
   // schedule (copied from the plan)
   int32_t T, H, hpg, HG, tpt, upc, C;
   int64_t U;
@@ -248,6 +256,14 @@ __device__ inline float e4m3_to_f32(uint32_t code) {
   return (code & 0x80u) ? -mag : mag;
 }
 
+// ue8m0 scale byte b -> 2^(b - 127) as fp32, exact (b = 0 is the fp32
+// subnormal 2^-127); b = 0xFF is NaN.
+__device__ inline float ue8m0_to_f32(uint32_t b) {
+  b &= 0xFFu;
+  if (b == 0xFFu) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float(b ? (b << 23) : 0x00400000u);
+}
+
 // e2m1 (bias 1, subnormal at exponent field 0) -> fp32, exact, same trick
 // with 2^126.
 __device__ inline float e2m1_to_f32(uint32_t nib) {
@@ -258,7 +274,8 @@ __device__ inline float e2m1_to_f32(uint32_t nib) {
 // One-time per-device kernel set-up (function attributes): `f` runs on the
 // first launch of kernel variant `bit` on the current device, later launches
 // skip it (they may be captured into a CUDA graph, where no set-up call is
-// wanted). Thread-safe.
+// wanted). Thread-safe. Bits in use: tensor-core kernels 0-2 (plain) and
+// 20-22 (V4.1 options), SIMT kernels 8-11, combine 16.
 cudaError_t dsa_configure_once(int bit, cudaError_t (*f)(void *), void *arg);
 
 // Programmatic dependent launch: the decode kernels let the combine grid be
@@ -273,6 +290,76 @@ __device__ __forceinline__ void pdl_wait_primary() {
 
 __device__ inline float bf16_bits_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
+}
+
+// ---------------------------------------------------------------- MXFP8 out
+// The V4.1 output epilogue (the swapab page's merge step): inverse GPT-J
+// RoPE on dims >= 448, then per head and 32-dim chunk an ue8m0 scale
+// E = ceil(log2(max(amax, 1e-10) * fp32(1/448))) + 127 and e4m3 codes of
+// x * 2^(127 - E), stored in the o-fused layout.
+
+// ue8m0 byte of the smallest power of two >= v, v a positive normal fp32
+// value: the biased exponent field, plus one unless the mantissa field is
+// zero (then v is that power of two); saturated at 254 (0xFF is NaN).
+__device__ __forceinline__ uint32_t ue8m0_ceil(float v) {
+  const uint32_t b = __float_as_uint(v);
+  const uint32_t e = ((b >> 23) & 0xFFu) + ((b & 0x7FFFFFu) != 0u ? 1u : 0u);
+  return e > 254u ? 254u : e;
+}
+// 2^(127 - E) for a scale byte E in [1, 254] (fp32 bits (254 - E) << 23).
+__device__ __forceinline__ float ue8m0_inverse(uint32_t E) { return __uint_as_float((254u - E) << 23); }
+
+// Two fp32 values -> e4m3 codes (round to nearest even, saturating to
+// +-448): lo in bits 0..7, hi in bits 8..15.
+__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// o-fused addresses of head h (absolute), 32-dim chunk c of token t.
+__device__ __forceinline__ uint8_t *mx_chunk(const Params &p, int64_t t, int h, int c) {
+  const int g = h / p.mx_g, ka = c * p.mx_g + (h - g * p.mx_g);
+  return p.mx_data + t * p.mx_st + (int64_t)g * p.mx_sg + (int64_t)ka * 32;
+}
+__device__ __forceinline__ uint8_t *mx_scale_byte(const Params &p, int64_t t, int h, int c) {
+  const int g = h / p.mx_g, ka = c * p.mx_g + (h - g * p.mx_g);
+  return p.mx_scale + 4 * (t * p.mx_sst + (int64_t)g * p.mx_ssg + (int64_t)(ka >> 2) * p.mx_ssw) +
+         (ka & 3);
+}
+
+// One lane per dim, one warp per 32-dim chunk (dim d = 32c + lane, c
+// warp-uniform): inverse GPT-J rotation when cs_row != null and the chunk
+// lies in dims >= 448 (the pair partner is the neighbouring lane), chunk
+// amax over the warp, cast, and the stores (lane 0 writes the scale byte).
+// All 32 lanes must call it together.
+__device__ __forceinline__ void mx_store_lane(const Params &p, float x, int64_t t, int h, int d,
+                                              const float *cs_row) {
+  const int lane = threadIdx.x & 31;
+  if (cs_row != nullptr && d >= kRopeStart) {
+    const float other = __shfl_xor_sync(0xffffffffu, x, 1);
+    const int i = (d - kRopeStart) >> 1;
+    const float c = __ldg(cs_row + i), s = __ldg(cs_row + kRopeHalf + i);
+    x = (d & 1) ? fmaf(x, c, -(s * other)) : fmaf(x, c, s * other);
+  }
+  float a = fabsf(x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  a = fmaxf(a, 1e-10f);
+  const uint32_t E = ue8m0_ceil(a * (1.0f / 448.0f));
+  const int c = d >> 5;
+  mx_chunk(p, t, h, c)[lane] = (uint8_t)(e4m3x2_rn_sat(x * ue8m0_inverse(E), 0.f) & 0xFFu);
+  if (lane == 0) *mx_scale_byte(p, t, h, c) = (uint8_t)E;
+}
+
+// Table row of token t for the inverse rotation (null without RoPE or for
+// NeoX, whose inverse the MXFP8 path does not take); a position outside the
+// table uses row 0, as the Q staging does.
+__device__ __forceinline__ const float *mx_rope_row(const Params &p, int64_t t) {
+  if (!p.cos_sin || !p.rope_gptj) return nullptr;
+  int64_t pos = __ldg(p.positions + t);
+  if (pos < 0 || pos >= p.cs_rows) pos = 0;
+  return p.cos_sin + pos * 64;
 }
 
 // Status word: first failure wins.

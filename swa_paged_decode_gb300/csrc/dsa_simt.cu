@@ -41,16 +41,19 @@ __device__ void load_subtile(const Params &p, SimtSmem &sm, int32_t lid, int32_t
   float *krow = sm.k + i * kD;
   if (!ok) {
     for (int d = j; d < kD; d += 8) krow[d] = 0.f;
-  } else if (L.fmt == DSA_REC_FP8_528) {
+  } else if (L.fmt != DSA_REC_NVFP4_288) {   // fp8: fp32 scales per 128 or ue8m0 per 32 dims
     const uint8_t *rec = record_ptr(L, sid);
-    const float4 sc = __ldg(reinterpret_cast<const float4 *>(rec + 512));
-    const float scl[4] = {sc.x, sc.y, sc.z, sc.w};
+    const bool ue = L.fmt == DSA_REC_FP8_528_UE8M0;
+    const uint4 sc = __ldg(reinterpret_cast<const uint4 *>(rec + 512));
+    const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const int c = j + 8 * kk;  // 16-byte chunk = dims [16c, 16c+16)
       const uint4 v = __ldg(reinterpret_cast<const uint4 *>(rec) + c);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      const float s = scl[c >> 3];
+      const int sb = c >> 1;     // ue8m0 scale byte of dims [32 sb, 32 sb + 32)
+      const float s = ue ? ue8m0_to_f32(scw[sb >> 2] >> (8 * (sb & 3)))
+                         : __uint_as_float(scw[c >> 3]);
 #pragma unroll
       for (int e = 0; e < 16; ++e)
         krow[16 * c + e] = e4m3_to_f32((w[e >> 2] >> (8 * (e & 3))) & 0xFFu) * s;
@@ -103,7 +106,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) 
 
   for (int32_t t = tf; t <= tl; ++t) {
     const Segment seg = make_segment(p, c, t, u0, u1);
-    // Q (fp32) with NeoX RoPE on dims 448..511.
+    // Q (fp32) with RoPE on dims 448..511 (NeoX or GPT-J pairs).
     int64_t pos = p.positions ? __ldg(p.positions + t) : 0;
     if (pos < 0 || (p.cos_sin && pos >= p.cs_rows)) {   // outside the table: flag, use row 0
       if (tid == 0) report_status(p.status, DSA_ERR_INVALID_ARG);
@@ -113,7 +116,12 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) 
       const int h = e / kD, d = e % kD;
       const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)(h0 + h) * p.q_sh;
       float x = __bfloat162float(qh[d]);
-      if (p.cos_sin && d >= kRopeStart) {
+      if (p.cos_sin && d >= kRopeStart && p.rope_gptj) {   // pair (448+2i, 449+2i)
+        const float *cs = p.cos_sin + pos * 64;
+        const int i = (d - kRopeStart) >> 1;
+        const float other = __bfloat162float(qh[d ^ 1]);
+        x = (d & 1) ? x * cs[i] + other * cs[kRopeHalf + i] : x * cs[i] - other * cs[kRopeHalf + i];
+      } else if (p.cos_sin && d >= kRopeStart) {
         const float *cs = p.cos_sin + pos * 64;
         if (d < kRopeStart + kRopeHalf) {
           const int i = d - kRopeStart;
@@ -224,6 +232,9 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) 
     }
 
     // Finalize: whole tokens -> out / lse with the sink; split -> partial slot.
+    // MXFP8 output: a warp holds one 32-dim chunk of a head (d = tid + 256 k).
+    const bool mx = seg.whole && p.mx_on;
+    const float *cs_row = mx ? mx_rope_row(p, t) : nullptr;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int h = i >> 1, d = tid + 256 * (i & 1);
@@ -238,7 +249,10 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) 
           }
           v = acc[i] / den;
         }
-        p.out[((int64_t)t * p.H + h0 + h) * kD + d] = __float2bfloat16_rn(v);
+        if (mx)
+          mx_store_lane(p, v, t, h0 + h, d, cs_row);
+        else
+          p.out[((int64_t)t * p.H + h0 + h) * kD + d] = __float2bfloat16_rn(v);
       } else {
         const int64_t slot = (int64_t)hg * 2 * p.C + seg.slot;
         p.part_o[(slot * HPG + h) * kD + d] = (l > 0.f) ? acc[i] / l : 0.f;

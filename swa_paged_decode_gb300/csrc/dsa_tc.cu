@@ -206,7 +206,7 @@ __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, in
   g.ok = slot_valid(L, g.r, lid == 0 ? c.lim0 : c.lim1, sid);
   const uint4 z = make_uint4(0, 0, 0, 0);
   g.pl = true;
-  if (L.fmt == DSA_REC_FP8_528) {
+  if (L.fmt != DSA_REC_NVFP4_288) {   // both 528-byte fp8 records
     if (g.ok) {
       const uint8_t *rec = record_ptr(L, sid);
       if ((reinterpret_cast<uintptr_t>(rec) & 31u) == 0) {   // chunk pairs are whole 32-byte sectors
@@ -272,8 +272,9 @@ __device__ __forceinline__ uint4 shfl_xor_u4(const uint4 v, int mask) {
 // Dequantize the two 64-dim k-blocks of M block mb for this thread's row
 // half. Called by all 32 lanes of the warp (fp8 rows in sector layout get the
 // missing half of each chunk pair from the other lane of their row).
-__device__ __forceinline__ void dequant_block(bool fp8, const Gather &g, const uint32_t (&scale2)[4],
-                                              int mb, int row, int j, uint32_t kv_base) {
+__device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g,
+                                              const uint32_t (&scale2)[4], int mb, int row, int j,
+                                              uint32_t kv_base) {
   if (fp8) {
     // chunks c = 4m + 2j + e of k-block m; M block mb = k-blocks {2mb, 2mb+1}
 #pragma unroll
@@ -281,7 +282,11 @@ __device__ __forceinline__ void dequant_block(bool fp8, const Gather &g, const u
       const int m = 2 * mb + mm;
       const uint4 recv = shfl_xor_u4(j == 0 ? g.d[2 * m + 2] : g.d[2 * m], 1);
       const uint4 pr[2] = {g.pl ? g.d[2 * m] : g.d[2 * m + 1], g.pl ? g.d[2 * m + 1] : recv};
-      const uint32_t sc = scale2[mb];
+      // fp32 scales: scale2[mb] is the block's f16 pair. ue8m0: scale2 holds
+      // the 16 raw scale bytes; this lane's 32 dims of k-block m (chunks
+      // 4m + 2j + e) take byte 2m + j.
+      const uint32_t sc =
+          ue ? scale_f16x2(ue8m0_to_f32(scale2[m >> 1] >> (16 * (m & 1) + 8 * j))) : scale2[mb];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int c = 4 * m + 2 * j + e;   // dims [16c, 16c+16), scale block mb
@@ -346,7 +351,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
                : "memory");
 }
 
-template <int HPG>
+// kExt: the V4.1 options (fp8 records with ue8m0 scales, GPT-J RoPE, MXFP8
+// output); the plain instantiation compiles none of their code.
+template <int HPG, bool kExt>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   using Cfg = TcCfg<HPG>;
   constexpr int NH = Cfg::kHalf;
@@ -453,15 +460,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const int32_t sid_n2 = cn2.u < u1 ? load_sid(p, cn2, row) : -1;
       const int32_t sid_next = sid_n1;
       const bool last_of_token = cn.u >= u1 || cn.t != t;
-      const bool fp8 = p.list[lid].fmt == DSA_REC_FP8_528;
+      const bool fp8 = p.list[lid].fmt != DSA_REC_NVFP4_288;
+      const bool ue = kExt && p.list[lid].fmt == DSA_REC_FP8_528_UE8M0;
       uint32_t scale2[4] = {0, 0, 0, 0};
       if (fp8) {   // sector layout: lane j = 1 takes the scales from lane j = 0
         const uint4 sp = shfl_xor_u4(g.d[17], 1);
         const uint4 sv = (!g.pl && j == 1) ? sp : g.d[17];
-        scale2[0] = scale_f16x2(__uint_as_float(sv.x));
-        scale2[1] = scale_f16x2(__uint_as_float(sv.y));
-        scale2[2] = scale_f16x2(__uint_as_float(sv.z));
-        scale2[3] = scale_f16x2(__uint_as_float(sv.w));
+        if (ue) {   // raw bytes, decoded per k-block
+          scale2[0] = sv.x;
+          scale2[1] = sv.y;
+          scale2[2] = sv.z;
+          scale2[3] = sv.w;
+        } else {
+          scale2[0] = scale_f16x2(__uint_as_float(sv.x));
+          scale2[1] = scale_f16x2(__uint_as_float(sv.y));
+          scale2[2] = scale_f16x2(__uint_as_float(sv.z));
+          scale2[3] = scale_f16x2(__uint_as_float(sv.w));
+        }
       }
       if (j == 0 && g.ok) {
         kept += 1;
@@ -486,7 +501,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       for (int mb = 0; mb < 4; ++mb) {
         if (!first) wait(kBarKvFree + mb, ph_free[mb]);
         if (mb == 0 && j == 0) row_ok_s[row] = g.ok ? 1.f : 0.f;
-        dequant_block(fp8, g, scale2, mb, row, j, kv_base);
+        dequant_block(fp8, ue, g, scale2, mb, row, j, kv_base);
       }
       // One hand-off per tile: the QK MMAs are issued once the whole tile is
       // in place, so per-block fences and arrives would only lengthen the
@@ -544,10 +559,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         qa[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane);
         qb[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane + 1);
       }
-      // NeoX: dim 448+i pairs with 480+i; lanes 28..31 hold dims 448..511
+      // Lanes 28..31 hold dims 448..511. NeoX: dim 448+i pairs with 480+i
+      // (two lanes apart); GPT-J: 448+2i with 449+2i (inside a lane, pair
+      // index 8 (lane - 28) + k for its values 2k, 2k+1).
       const bool rope = p.cos_sin != nullptr;
+      const bool gptj = kExt && p.rope_gptj != 0;
       const bool rlane = rope && lane >= 28, firsth = lane < 30;
-      const float *cs = p.cos_sin + (rope ? pos * 64 + (lane & 1) * 16 : 0);
+      const float *cs = p.cos_sin + (rope ? pos * 64 + (gptj ? 8 * (lane & 3) : (lane & 1) * 16) : 0);
 #pragma unroll
       for (int i = 0; i < kQH; ++i) {
         const int h = warp + kSmWarps * i;
@@ -558,7 +576,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           v[2 * k] = bf16_bits_to_f32(w[k] & 0xFFFFu);
           v[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
         }
-        if (rope) {   // branch-free: every lane reads a valid row entry, lanes 28..31 use it
+        if (rope && gptj) {   // every lane reads a valid row entry, lanes 28..31 use it
+          float c[8], sn[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            c[k] = __ldg(cs + k);
+            sn[k] = __ldg(cs + kRopeHalf + k);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float x1 = v[2 * k], x2 = v[2 * k + 1];
+            const float r1 = fmaf(x1, c[k], -(x2 * sn[k])), r2 = fmaf(x2, c[k], x1 * sn[k]);
+            v[2 * k] = rlane ? r1 : x1;
+            v[2 * k + 1] = rlane ? r2 : x2;
+          }
+        } else if (rope) {   // branch-free: every lane reads a valid row entry, lanes 28..31 use it
           float c[16], sn[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
@@ -654,9 +686,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       }
       if (seg_worked) ++sord;
       sm_bar();
+      const bool mx = kExt && seg.whole && p.mx_on;
+      const float *cs_row = mx ? mx_rope_row(p, seg.t) : nullptr;
 #pragma unroll 1
       for (int mb = 0; mb < 4; ++mb) {
         const int d = 128 * mb + prow;
+        if (mx) {   // a warp holds one 32-dim chunk (dims 128 mb + 32 q4 + lane)
+#pragma unroll 1
+          for (int g8 = 0; g8 < NH / 8; ++g8) {
+            float o[8];
+            if (seg_worked) tc::tmem_ld<8>(tl_lane + Cfg::kColO + mb * HPG + half * NH + 8 * g8, o);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int h = half * NH + 8 * g8 + i;
+              const float iv = red_s[256 - 64 + h];
+              mx_store_lane(p, (!seg_worked || iv == 0.f) ? 0.f : o[i] * iv, seg.t, h0 + h, d,
+                            cs_row);
+            }
+          }
+          continue;
+        }
 #pragma unroll
         for (int g8 = 0; g8 < NH / 8; ++g8) {
           float o[8];
@@ -872,14 +921,14 @@ bool dsa_tc_supports(int hpg) { return hpg == 16 || hpg == 32 || hpg == 64; }
 namespace {
 // Checks that the kernel kept exactly kLaunchRegs registers per thread (the
 // warpgroup register split assumes it) and raises its shared-memory limit.
-template <int N>
+template <int N, bool E>
 cudaError_t tc_setup(void *) {
   using namespace dsa;
   cudaFuncAttributes fa;
-  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N>);
+  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E>);
   if (err != cudaSuccess) return err;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(tc_decode_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(tc_decode_kernel<N, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)TcCfg<N>::kSmem);
 }
 }  // namespace
@@ -887,14 +936,22 @@ cudaError_t tc_setup(void *) {
 cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
   using namespace dsa;
   const dim3 grid((unsigned)(p.C * p.HG)), block(kTcThreads);
+  const bool ext = p.rope_gptj || p.mx_on || p.list[0].fmt == DSA_REC_FP8_528_UE8M0 ||
+                   (p.nlists > 1 && p.list[1].fmt == DSA_REC_FP8_528_UE8M0);
   cudaError_t err = cudaSuccess;
   switch (p.hpg) {
 #define DSA_TC_CASE(N, BIT)                                                              \
   case N: {                                                                              \
     const int smem = (int)TcCfg<N>::kSmem;                                               \
-    err = dsa_configure_once(BIT, &tc_setup<N>, nullptr);                                \
-    if (err != cudaSuccess) return err;                                                  \
-    tc_decode_kernel<N><<<grid, block, smem, stream>>>(p);                               \
+    if (ext) {                                                                           \
+      err = dsa_configure_once(BIT + 20, &tc_setup<N, true>, nullptr);                   \
+      if (err != cudaSuccess) return err;                                                \
+      tc_decode_kernel<N, true><<<grid, block, smem, stream>>>(p);                       \
+    } else {                                                                             \
+      err = dsa_configure_once(BIT, &tc_setup<N, false>, nullptr);                       \
+      if (err != cudaSuccess) return err;                                                \
+      tc_decode_kernel<N, false><<<grid, block, smem, stream>>>(p);                      \
+    }                                                                                    \
     break;                                                                               \
   }
     DSA_TC_CASE(16, 0)
