@@ -34,6 +34,7 @@ from swa_paged_decode_gb300 import workloads as W  # noqa: E402
 METRIC = "decode tokens/s; gathered-KV HBM GB/s as % of GB300 peak (1 GPU)"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20        # > 2x the 126 MB L2
+MX_GROUP = 8   # heads per o-fused output group of the V4.1 variant (open on the pages)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic of tc_decode_kernel<64> from one ncu capture
@@ -58,6 +59,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, help="workload 1..5")
+    ap.add_argument("--variant", choices=["base", "v41"], default="base",
+                    help="v41: ue8m0 fp8 records, GPT-J RoPE, MXFP8 o-fused output "
+                         f"({MX_GROUP} heads per group)")
     ap.add_argument("--tokens", type=int, default=None, help="batch size (default: config's)")
     ap.add_argument("--per-config", dest="per_config", action="store_true", default=True)
     ap.add_argument("--quick", dest="per_config", action="store_false",
@@ -93,13 +97,14 @@ def kept_rows(w: W.Workload) -> torch.Tensor:
     return cnt
 
 
-def algorithmic(w: W.Workload):
+def algorithmic(w: W.Workload, mx: bool = False):
     cnt = kept_rows(w)
     rows = sum(int(k.sum()) for k, _ in cnt)
     gathered = sum(int(k.sum()) * rb for k, rb in cnt)
     flops = 2 * 2 * W.HEAD_DIM * w.H * rows      # QK^T and PV, 2 flops per MAC
     ids_bytes = 4 * (w.swa.width + (0 if w.extra is None else w.extra.width)) * w.T
-    io_bytes = w.T * w.H * W.HEAD_DIM * 2 * 2 + w.T * w.H * 4   # q in, out, lse
+    out_bytes = w.T * w.H * (W.HEAD_DIM + W.HEAD_DIM // 32) if mx else w.T * w.H * W.HEAD_DIM * 2
+    io_bytes = w.T * w.H * W.HEAD_DIM * 2 + out_bytes + w.T * w.H * 4   # q in, out, lse
     return dict(rows=rows, gathered_bytes=gathered, flops=flops,
                 total_bytes=gathered + ids_bytes + io_bytes)
 
@@ -172,23 +177,34 @@ class ClockSampler:
 # ------------------------------------------------------------ GPU arm
 
 class Step:
-    def __init__(self, w: W.Workload, B):
+    def __init__(self, w: W.Workload, B, mx: bool = False):
         self.w = w
         self.B = B
-        self.dec = B.Decoder(w)
+        self.mx = mx
+        self.dec = B.Decoder(w, mx_group=MX_GROUP if mx else None)
         self.has_combine = self.dec.plan.ctas_per_group > 1
 
     def __call__(self, ev_k0=None, ev_k1=None):
         w, B, d = self.w, self.B, self.dec
+        ei = None if w.extra is None else w.extra.ids
+        el = None if w.extra is None else w.extra.lens
         if ev_k0 is not None:
             ev_k0.record()
-        B.dsa_decode_run(d.plan, d.workspace, w.q, w.swa_cache, w.swa.ids, w.swa.lens,
-                         w.extra_cache, None if w.extra is None else w.extra.ids,
-                         None if w.extra is None else w.extra.lens, w.sink, w.positions,
-                         w.cos_sin, w.scale, d.out, d.lse)
+        if self.mx:
+            B.dsa_decode_run_v41(d.plan, d.workspace, w.q, w.swa_cache, w.swa.ids, w.swa.lens,
+                                 w.extra_cache, ei, el, w.sink, w.positions, w.cos_sin,
+                                 w.rope_style, w.scale, None, d.mx, d.lse)
+        else:
+            B.dsa_decode_run(d.plan, d.workspace, w.q, w.swa_cache, w.swa.ids, w.swa.lens,
+                             w.extra_cache, ei, el, w.sink, w.positions, w.cos_sin, w.scale,
+                             d.out, d.lse)
         if ev_k1 is not None:
             ev_k1.record()
-        B.dsa_decode_combine(d.plan, d.workspace, w.sink, d.out, d.lse)
+        if self.mx:
+            B.dsa_decode_combine_v41(d.plan, d.workspace, w.sink, w.positions, w.cos_sin,
+                                     w.rope_style, None, d.mx, d.lse)
+        else:
+            B.dsa_decode_combine(d.plan, d.workspace, w.sink, d.out, d.lse)
 
 
 def rank_barrier(world: int):
@@ -240,7 +256,7 @@ class _Null:
         return False
 
 
-def e2e_steps(w: W.Workload, B, steps: int, warmup: int, flush: torch.Tensor):
+def e2e_steps(w: W.Workload, B, steps: int, warmup: int, flush: torch.Tensor, mx: bool = False):
     """Same step through the public API from pinned HOST buffers: per step the
     per-token inputs (Q, slot lists, lengths, positions) go host->device and
     out + lse come back device->host inside the timed region. The caches and
@@ -257,19 +273,26 @@ def e2e_steps(w: W.Workload, B, steps: int, warmup: int, flush: torch.Tensor):
            "extra_ids": None if w.extra is None else w.extra.ids,
            "extra_lens": None if w.extra is None else w.extra.lens, "positions": w.positions}
     host = {n: src[n].cpu().pin_memory() for n in names}
-    dec = B.Decoder(w)
+    dec = B.Decoder(w, mx_group=MX_GROUP if mx else None)
     comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     E = lambda: torch.cuda.Event()
+    pinned = lambda t: torch.empty(t.shape, dtype=t.dtype).pin_memory()
     sets = []
     for _ in range(2):
-        sets.append({"dev": {n: torch.empty_like(src[n]) for n in names},
-                     "out": torch.empty_like(dec.out), "lse": torch.empty_like(dec.lse),
-                     "out_h": torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory(),
-                     "lse_h": torch.empty(dec.lse.shape, dtype=dec.lse.dtype).pin_memory(),
-                     "in_ready": E(), "comp_done": E(), "out_done": E(), "used": False})
+        if mx:
+            m = B.MxOut(w.T, w.H, MX_GROUP, w.q.device)
+            outs = {"mx": m, "res": [m.data, m.scale]}
+        else:
+            o = torch.empty_like(dec.out)
+            outs = {"out": o, "res": [o]}
+        lse = torch.empty_like(dec.lse)
+        outs["res"].append(lse)
+        sets.append(dict(outs, dev={n: torch.empty_like(src[n]) for n in names}, lse=lse,
+                         res_h=[pinned(t) for t in outs["res"]],
+                         in_ready=E(), comp_done=E(), out_done=E(), used=False))
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = dec.out.numel() * 2 + dec.lse.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in sets[0]["res"])
 
     def step(k):
         b = sets[k % 2]
@@ -283,15 +306,24 @@ def e2e_steps(w: W.Workload, B, steps: int, warmup: int, flush: torch.Tensor):
         comp.wait_event(b["in_ready"])
         flush.zero_()
         d = b["dev"]
-        B.dsa_decode_run(dec.plan, dec.workspace, d["q"], w.swa_cache, d["swa_ids"],
-                         d["swa_lens"], w.extra_cache, d.get("extra_ids"), d.get("extra_lens"),
-                         w.sink, d.get("positions"), w.cos_sin, w.scale, b["out"], b["lse"], comp)
-        B.dsa_decode_combine(dec.plan, dec.workspace, w.sink, b["out"], b["lse"], comp)
+        if mx:
+            B.dsa_decode_run_v41(dec.plan, dec.workspace, d["q"], w.swa_cache, d["swa_ids"],
+                                 d["swa_lens"], w.extra_cache, d.get("extra_ids"),
+                                 d.get("extra_lens"), w.sink, d.get("positions"), w.cos_sin,
+                                 w.rope_style, w.scale, None, b["mx"], b["lse"], comp)
+            B.dsa_decode_combine_v41(dec.plan, dec.workspace, w.sink, d.get("positions"),
+                                     w.cos_sin, w.rope_style, None, b["mx"], b["lse"], comp)
+        else:
+            B.dsa_decode_run(dec.plan, dec.workspace, d["q"], w.swa_cache, d["swa_ids"],
+                             d["swa_lens"], w.extra_cache, d.get("extra_ids"),
+                             d.get("extra_lens"), w.sink, d.get("positions"), w.cos_sin, w.scale,
+                             b["out"], b["lse"], comp)
+            B.dsa_decode_combine(dec.plan, dec.workspace, w.sink, b["out"], b["lse"], comp)
         b["comp_done"].record(comp)
         s_out.wait_event(b["comp_done"])
         with torch.cuda.stream(s_out):
-            b["out_h"].copy_(b["out"], non_blocking=True)
-            b["lse_h"].copy_(b["lse"], non_blocking=True)
+            for hst, dv in zip(b["res_h"], b["res"]):
+                hst.copy_(dv, non_blocking=True)
             b["out_done"].record(s_out)
 
     for k in range(warmup):
@@ -308,7 +340,7 @@ def e2e_steps(w: W.Workload, B, steps: int, warmup: int, flush: torch.Tensor):
     return a.elapsed_time(e), h2d, d2h
 
 
-def roofline(w: W.Workload, alg, kern_ms_avg: float, peaks, peak_kind):
+def roofline(w: W.Workload, alg, kern_ms_avg: float, peaks, peak_kind, captured: bool = True):
     hbm = peaks["hbm_gbs"]
     tf = peaks["bf16_tflops"]
     intensity = alg["flops"] / max(alg["gathered_bytes"], 1)
@@ -321,7 +353,7 @@ def roofline(w: W.Workload, alg, kern_ms_avg: float, peaks, peak_kind):
     else:
         ach = alg["gathered_bytes"] / s / 1e9
         r = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
-    r["traffic"] = ncu_traffic(alg["rows"])
+    r["traffic"] = ncu_traffic(alg["rows"]) if captured else None
     r["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
     r["intensity_flop_per_byte"] = intensity
     r["kernel_ms"] = kern_ms_avg
@@ -350,16 +382,17 @@ def gpu_arm(args, rank, world, B, peaks, peak_kind):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    w = W.make_config(args.config, T=args.tokens, device=dev)
-    alg = algorithmic(w)
-    step = Step(w, B)
+    mx = args.variant == "v41"
+    w = W.make_config(args.config, T=args.tokens, device=dev, v41=mx)
+    alg = algorithmic(w, mx)
+    step = Step(w, B, mx)
     clocks = ClockSampler(dev.index)
     total_ms, step_ms, kern_ms = time_steps(step, args.steps, args.warmup, flush, clocks, world)
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     value = w.T * world / (ms_per_step * 1e-3)
     kern_avg = sum(kern_ms) / len(kern_ms)
-    e2e_ms, h2d, d2h = e2e_steps(w, B, max(3, args.steps // 2), args.warmup, flush)
+    e2e_ms, h2d, d2h = e2e_steps(w, B, max(3, args.steps // 2), args.warmup, flush, mx)
     e2e_value = w.T * world / (e2e_ms / max(3, args.steps // 2) * 1e-3)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -368,12 +401,14 @@ def gpu_arm(args, rank, world, B, peaks, peak_kind):
         "dtype": "bf16" if step.dec.plan.kernel == 1 else "fp32",
         "data": "synthetic (seeded N(0,1) rows quantized to fp8/NVFP4 records, random slot lists)",
         "config": {"workload": w.name, "T": w.T, "H": w.H,
-                   "swa": f"fp8_528 w{w.swa.width} page {w.swa_cache.page_size} "
-                          f"{w.swa_cache.num_slots} slots",
+                   "swa": f"{W.FMT_NAMES[w.swa_cache.fmt]} w{w.swa.width} page "
+                          f"{w.swa_cache.page_size} {w.swa_cache.num_slots} slots",
                    "extra": None if w.extra is None else
-                   f"{['fp8_528', 'nvfp4_288'][w.extra_cache.fmt]} w{w.extra.width} page "
+                   f"{W.FMT_NAMES[w.extra_cache.fmt]} w{w.extra.width} page "
                    f"{w.extra_cache.page_size} {w.extra_cache.num_slots} slots",
                    "sink": w.sink is not None, "rope": w.cos_sin is not None,
+                   "rope_style": ["neox", "gptj"][w.rope_style],
+                   "out": f"mxfp8 o-fused, {MX_GROUP} heads per group" if mx else "bf16",
                    "global_batch": w.T * world, "l2": "flushed (256 MiB write before every step)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "kernel": ["simt", "tcgen05"][step.dec.plan.kernel]},
@@ -381,10 +416,11 @@ def gpu_arm(args, rank, world, B, peaks, peak_kind):
                          "gbs": alg["gathered_bytes"] / (kern_avg * 1e-3) / 1e9,
                          "frac_of_peak": alg["gathered_bytes"] / (kern_avg * 1e-3) / 1e9 / peaks["hbm_gbs"],
                          "gbs_step": alg["gathered_bytes"] / (ms_per_step * 1e-3) / 1e9},
-        "roofline": roofline(w, alg, kern_avg, peaks, peak_kind),
+        "roofline": roofline(w, alg, kern_avg, peaks, peak_kind, captured=not mx),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (1 + (1 if step.has_combine else 0)),
+        # decode, combine (when a token is split), MXFP8 cast (V4.1 output)
+        "gpu_launches": args.steps * (1 + (1 if step.has_combine else 0) + (1 if mx else 0)),
         "clocks": clocks.summary(),
     }
     return res, w
@@ -415,27 +451,37 @@ def per_config_table(B, peaks, peak_kind, steps=20, warmup=3):
 
 # ------------------------------------------------------------ CPU (oracle) arm
 
-def oracle_timing(w: W.Workload, target_s: float, seed: int = 0):
+def oracle_run(a, tok, cores: int, mx: bool):
+    """The oracle on tokens `tok` (and, for the V4.1 variant, its MXFP8
+    output epilogue on the result)."""
+    import oracle
+    out = oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
+                        positions=a["positions"], cos_sin=a["cos_sin"],
+                        rope_style=a["rope_style"], tokens=tok, nthreads=cores)[0]
+    if mx:
+        pos = None if a["positions"] is None else a["positions"].cpu().numpy()[tok]
+        oracle.mxfp8_epilogue(out, group_size=MX_GROUP, positions=pos, cos_sin=a["cos_sin"],
+                              rope_style=a["rope_style"])
+
+
+def oracle_timing(w: W.Workload, target_s: float, seed: int = 0, mx: bool = False):
     """Time the fp64 oracle on a bounded token sample of workload w."""
     import numpy as np
 
-    import oracle
     a = W.oracle_args(w)
     cores = os.cpu_count() or 1
     rng = np.random.default_rng(seed)
     n = min(w.T, cores)
     tok = np.sort(rng.choice(w.T, size=n, replace=False))
     t0 = time.perf_counter()
-    oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
-                  positions=a["positions"], cos_sin=a["cos_sin"], rope_style=a["rope_style"], tokens=tok, nthreads=cores)
+    oracle_run(a, tok, cores, mx)
     dt = time.perf_counter() - t0
     per_tok = dt / n
     n2 = int(max(1, min(w.T, target_s / max(per_tok, 1e-9))))
     if n2 > n:
         tok = np.sort(rng.choice(w.T, size=n2, replace=False))
         t0 = time.perf_counter()
-        oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
-                      positions=a["positions"], cos_sin=a["cos_sin"], rope_style=a["rope_style"], tokens=tok, nthreads=cores)
+        oracle_run(a, tok, cores, mx)
         dt = time.perf_counter() - t0
         n = n2
     return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -447,8 +493,8 @@ def reference_arm(args):
     sample of the same workload, on this host's cores."""
     import numpy as np
 
-    import oracle
-    w = W.make_config(args.config, T=args.tokens, device="cpu")
+    mx = args.variant == "v41"
+    w = W.make_config(args.config, T=args.tokens, device="cpu", v41=mx)
     a = W.oracle_args(w)
     cores = os.cpu_count() or 1
     rng = np.random.default_rng(0)
@@ -456,8 +502,7 @@ def reference_arm(args):
     def one():
         tok = np.sort(rng.choice(w.T, size=n, replace=False))
         t0 = time.perf_counter()
-        oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
-                      positions=a["positions"], cos_sin=a["cos_sin"], rope_style=a["rope_style"], tokens=tok, nthreads=cores)
+        oracle_run(a, tok, cores, mx)
         return time.perf_counter() - t0
     for _ in range(args.warmup):
         one()
@@ -495,10 +540,10 @@ def main():
     peaks, peak_kind = load_peaks()
     res, w = gpu_arm(args, rank, world, B, peaks, peak_kind)
     if rank == 0 and world == 1:
-        if args.per_config:
+        if args.per_config and args.variant == "base":
             res["per_config"] = per_config_table(B, peaks, peak_kind)
         if args.cpu_baseline:
-            res["cpu_baseline"] = oracle_timing(w, args.cpu_seconds)
+            res["cpu_baseline"] = oracle_timing(w, args.cpu_seconds, mx=args.variant == "v41")
     if world > 1:
         import torch.distributed as dist
         dist.barrier()

@@ -127,7 +127,10 @@ typedef struct {
   int64_t balance_live;     /* 1: CTA boundaries balance live tiles (set when
                               a CTA covers >= 2 tokens on average); 0: even
                               split of the units, bounds[c] = c*units_per_cta */
-  int64_t reserved[14];
+  int64_t ws_stage_offset;  /* fp32 [T][H][512] staging of the MXFP8 output */
+  int64_t workspace_bytes_mx; /* workspace an MXFP8-output call needs
+                              (dsa_decode_run_v41 / combine_v41 with mx)     */
+  int64_t reserved[12];
 } dsa_decode_plan_t;
 
 /* Plan one decode call.
@@ -218,6 +221,9 @@ typedef struct {
  *               of the output are first rotated back (the inverse of the Q
  *               rotation, same table row); that inverse is implemented for
  *               DSA_ROPE_GPTJ only (NEOX with RoPE and mx: DSA_ERR_UNSUPPORTED).
+ *               With mx the workspace must hold plan->workspace_bytes_mx
+ *               bytes: run leaves each token's fp32 output in it and
+ *               dsa_decode_combine_v41 writes the MXFP8 output (required).
  * Every other argument as for dsa_decode_run. Split tokens get their output
  * from dsa_decode_combine_v41 (same rope_style, positions, cos_sin, out / mx). */
 dsa_status dsa_decode_run_v41(const dsa_decode_plan_t *plan, void *workspace,
@@ -233,7 +239,9 @@ dsa_status dsa_decode_run_v41(const dsa_decode_plan_t *plan, void *workspace,
                               dsa_stream_t stream);
 
 /* dsa_decode_combine for dsa_decode_run_v41: the same plan, workspace, sink,
- * positions, cos_sin, rope_style and output (out or mx) as given to run. */
+ * positions, cos_sin, rope_style and output (out or mx) as given to run.
+ * With mx it merges the split tokens into the staging area and then casts
+ * every token to MXFP8 (one more launch, also for plans that split nothing). */
 dsa_status dsa_decode_combine_v41(const dsa_decode_plan_t *plan, void *workspace,
                                   size_t workspace_bytes, const float *sink,
                                   const int64_t *positions, const float *cos_sin,

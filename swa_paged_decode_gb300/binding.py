@@ -48,8 +48,9 @@ class Plan(ctypes.Structure):
         "tiles_per_token", "units_per_cta", "ctas_per_group", "split_tokens", "kernel")] + \
         [(n, ctypes.c_int64) for n in (
             "total_units", "ws_sel_offset", "ws_part_lse_offset", "ws_part_sel_offset",
-            "ws_part_o_offset", "workspace_bytes", "ws_bounds_offset", "balance_live")] + \
-        [("reserved", ctypes.c_int64 * 14)]
+            "ws_part_o_offset", "workspace_bytes", "ws_bounds_offset", "balance_live",
+            "ws_stage_offset", "workspace_bytes_mx")] + \
+        [("reserved", ctypes.c_int64 * 12)]
 
 
 _lib = None
@@ -282,6 +283,8 @@ class Decoder:
         self.plan, nbytes = dsa_decode_plan(w.T, w.H, w.swa.width,
                                             0 if w.extra is None else w.extra.width, num_sms)
         dev = w.q.device
+        if mx_group is not None:
+            nbytes = self.plan.workspace_bytes_mx
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         self.mx = None if mx_group is None else MxOut(w.T, w.H, mx_group, dev)
         self.out = (torch.empty((w.T, w.H, W.HEAD_DIM), dtype=torch.bfloat16, device=dev)

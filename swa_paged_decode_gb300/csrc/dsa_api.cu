@@ -164,14 +164,15 @@ dsa_status run_impl(const dsa_decode_plan_t *plan, void *workspace, size_t works
   if (cos_sin && (cos_sin_rows < 1 || !aligned(cos_sin, 16) || !aligned(positions, 8)))
     return cos_sin_rows < 1 ? DSA_ERR_INVALID_ARG : DSA_ERR_ALIGNMENT;
   if (sink && !aligned(sink, 4)) return DSA_ERR_ALIGNMENT;
-  if (!workspace || (int64_t)workspace_bytes < plan->workspace_bytes ||
-      !aligned(workspace, kAlignWs))
+  const int64_t need = mx ? plan->workspace_bytes_mx : plan->workspace_bytes;
+  if (!workspace || (int64_t)workspace_bytes < need || !aligned(workspace, kAlignWs))
     return DSA_ERR_WORKSPACE;
 
   Params p;
   std::memset(&p, 0, sizeof(p));
   dsa_status s = fill_output(plan, positions, cos_sin, cos_sin_rows, rope_style, out, mx, p);
   if (s != DSA_OK) return s;
+  if (p.mx_on) p.stage = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan->ws_stage_offset);
   s = fill_list(swa_cache, swa_idx, swa_idx_stride, swa_lens, plan->swa_width, p.list[0]);
   if (s != DSA_OK) return s;
   p.nlists = 1;
@@ -202,14 +203,15 @@ dsa_status combine_impl(const dsa_decode_plan_t *plan, void *workspace, size_t w
                         int64_t cos_sin_rows, int32_t rope_style, void *out,
                         const dsa_mxfp8_out *mx, float *lse, dsa_stream_t stream) {
   if (!plan_ok(plan)) return DSA_ERR_PLAN;
-  if (plan->num_tokens == 0 || plan->ctas_per_group <= 1) return DSA_OK;
+  // bf16 output: only split tokens need this call; MXFP8: every token does
+  if (plan->num_tokens == 0 || (!mx && plan->ctas_per_group <= 1)) return DSA_OK;
   if (!lse) return DSA_ERR_INVALID_ARG;
   if (!aligned(lse, 4) || (sink && !aligned(sink, 4))) return DSA_ERR_ALIGNMENT;
   if ((positions == nullptr) != (cos_sin == nullptr)) return DSA_ERR_INVALID_ARG;
   if (cos_sin && (cos_sin_rows < 1 || !aligned(cos_sin, 16) || !aligned(positions, 8)))
     return cos_sin_rows < 1 ? DSA_ERR_INVALID_ARG : DSA_ERR_ALIGNMENT;
-  if (!workspace || (int64_t)workspace_bytes < plan->workspace_bytes ||
-      !aligned(workspace, kAlignWs))
+  const int64_t need = mx ? plan->workspace_bytes_mx : plan->workspace_bytes;
+  if (!workspace || (int64_t)workspace_bytes < need || !aligned(workspace, kAlignWs))
     return DSA_ERR_WORKSPACE;
   Params p;
   std::memset(&p, 0, sizeof(p));
@@ -220,7 +222,11 @@ dsa_status combine_impl(const dsa_decode_plan_t *plan, void *workspace, size_t w
   p.list[1].tiles = plan->tiles_extra;
   p.sink = sink;
   p.lse = lse;
-  return cuda_status(dsa_launch_combine(p, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (p.mx_on) p.stage = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan->ws_stage_offset);
+  cudaError_t e = dsa_launch_combine(p, st);
+  if (e == cudaSuccess && p.mx_on) e = dsa_launch_mx_epilogue(p, st);
+  return cuda_status(e);
 }
 
 }  // namespace
@@ -311,6 +317,10 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   plan->ws_bounds_offset = off;
   off = align_up(off + 8 * (ctas + 1), kAlignWs);
   plan->workspace_bytes = num_tokens == 0 ? 0 : off;
+  // MXFP8 output: every token's fp32 output is staged [T][H][512] after it
+  plan->ws_stage_offset = off;
+  plan->workspace_bytes_mx =
+      num_tokens == 0 ? 0 : off + 4 * (int64_t)num_tokens * num_heads * dsa::kD;
   *workspace_bytes = (size_t)plan->workspace_bytes;
   return DSA_OK;
 }

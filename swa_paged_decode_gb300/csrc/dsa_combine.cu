@@ -143,37 +143,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
       }
     }
   }
-  // MXFP8 output: 8 consecutive lanes hold one 32-dim chunk of a head (the
-  // quarter's first dim is a multiple of 128); GPT-J pairs lie inside a
-  // thread's 4 dims.
-  const float *cs_row = p.mx_on ? mx_rope_row(p, t) : nullptr;
 #pragma unroll
   for (int k = 0; k < kItems; ++k) {
     const int e = tid + k * kCombineThreads, h = e / kQ4, d4 = dq + e % kQ4;
     const float inv = inv_s[h];
-    if (p.mx_on) {
-      const int d0 = 4 * d4;
-      float x[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv};
-      if (cs_row != nullptr && d0 >= kRopeStart) {
-#pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-          const int i = (d0 - kRopeStart) / 2 + pr;
-          const float c = __ldg(cs_row + i), sn = __ldg(cs_row + kRopeHalf + i);
-          const float oe = x[2 * pr], oo = x[2 * pr + 1];
-          x[2 * pr] = fmaf(oe, c, sn * oo);
-          x[2 * pr + 1] = fmaf(oo, c, -(sn * oe));
-        }
-      }
-      float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-      for (int off = 4; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-      a = fmaxf(a, 1e-10f);
-      const uint32_t E = ue8m0_ceil(a * (1.0f / 448.0f));
-      const float sc = ue8m0_inverse(E);
-      const uint32_t codes = e4m3x2_rn_sat(x[0] * sc, x[1] * sc) | (e4m3x2_rn_sat(x[2] * sc, x[3] * sc) << 16);
-      const int hh = h0 + hb + h, c = d0 >> 5;
-      *reinterpret_cast<uint32_t *>(mx_chunk(p, t, hh, c) + (d0 & 31)) = codes;
-      if ((d0 & 31) == 0) *mx_scale_byte(p, t, hh, c) = (uint8_t)E;
+    if (p.stage) {   // MXFP8 output: fp32 to the staging area, cast later
+      *reinterpret_cast<float4 *>(p.stage + ((int64_t)t * p.H + h0 + hb + h) * kD + 4 * d4) =
+          make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
       continue;
     }
     __nv_bfloat16 *o = p.out + ((int64_t)t * p.H + h0 + hb + h) * kD + 4 * d4;
@@ -184,6 +160,49 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
     pk.y = *reinterpret_cast<uint32_t *>(&c2);
     *reinterpret_cast<uint2 *>(o) = pk;
   }
+}
+
+// ------------------------------------------------------------ MXFP8 cast
+// The V4.1 output epilogue (the swapab page's merge step): per token, head
+// and 32-dim chunk, the inverse GPT-J rotation of dims >= 448 (table row of
+// the token's position; pairs lie inside a thread's 4 dims), an ue8m0 scale
+// E = ceil(log2(max(amax, 1e-10) * fp32(1/448))) + 127 and e4m3 codes of
+// x * 2^(127 - E) (round to nearest even, saturating), o-fused layout.
+// Warp = one (token, head, 128-dim quarter); 8 lanes = one 32-dim chunk.
+constexpr int kMxThreads = 256;
+
+__global__ void __launch_bounds__(kMxThreads) mx_epilogue_kernel(Params p) {
+  pdl_wait_primary();   // the staged outputs are complete and visible
+  const int64_t unit = (int64_t)blockIdx.x * (kMxThreads / 32) + (threadIdx.x >> 5);
+  if (unit >= (int64_t)p.T * p.H * 4) return;   // whole warps leave together
+  const int lane = threadIdx.x & 31, quarter = (int)(unit & 3);
+  const int64_t th = unit >> 2;
+  const int64_t t = th / p.H;
+  const int h = (int)(th - t * p.H);
+  const int d0 = 128 * quarter + 4 * lane;
+  const float4 v = __ldg(reinterpret_cast<const float4 *>(p.stage + th * kD + d0));
+  float x[4] = {v.x, v.y, v.z, v.w};
+  const float *cs_row = mx_rope_row(p, t);
+  if (cs_row != nullptr && d0 >= kRopeStart) {
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      const int i = (d0 - kRopeStart) / 2 + pr;
+      const float c = __ldg(cs_row + i), sn = __ldg(cs_row + kRopeHalf + i);
+      const float oe = x[2 * pr], oo = x[2 * pr + 1];
+      x[2 * pr] = fmaf(oe, c, sn * oo);
+      x[2 * pr + 1] = fmaf(oo, c, -(sn * oe));
+    }
+  }
+  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  const uint32_t E = ue8m0_ceil(fmaxf(a, 1e-10f) * (1.0f / 448.0f));
+  const float sc = ue8m0_inverse(E);
+  const uint32_t codes =
+      e4m3x2_rn_sat(x[0] * sc, x[1] * sc) | (e4m3x2_rn_sat(x[2] * sc, x[3] * sc) << 16);
+  const int c = d0 >> 5;
+  *reinterpret_cast<uint32_t *>(mx_chunk(p, t, h, c) + (d0 & 31)) = codes;
+  if ((d0 & 31) == 0) *mx_scale_byte(p, t, h, c) = (uint8_t)E;
 }
 
 }  // namespace dsa
@@ -221,4 +240,25 @@ cudaError_t dsa_launch_combine(const dsa::Params &p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+}
+
+cudaError_t dsa_launch_mx_epilogue(const dsa::Params &p, cudaStream_t stream) {
+  using namespace dsa;
+  const int64_t units = (int64_t)p.T * p.H * 4;
+  if (units == 0) return cudaSuccess;
+  const int64_t blocks = (units + kMxThreads / 32 - 1) / (kMxThreads / 32);
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  // Programmatic dependent of the kernel before it (combine, or the decode
+  // kernel when nothing was split): it waits for that grid's completion.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kMxThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mx_epilogue_kernel, p);
 }

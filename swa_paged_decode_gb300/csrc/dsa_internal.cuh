@@ -53,7 +53,10 @@ struct Params {
   int32_t rope_gptj;           // RoPE pairing: 0 NeoX (448+i, 480+i), 1 GPT-J (448+2i, 449+2i)
   __nv_bfloat16 *out;          // [T, H, 512] (bf16 output), or null with mx_on
   float *lse;                  // [T, H]
-  // MXFP8 output (V4.1 epilogue): codes and ue8m0 scales in the o-fused layout
+  // MXFP8 output (V4.1 epilogue): the decode and combine kernels leave each
+  // token's fp32 output in `stage`; the epilogue kernel casts it into the
+  // codes and ue8m0 scales of the o-fused layout
+  float *stage;                // [T, H, 512] in the workspace, with mx_on
   int32_t mx_on;               // 1: write mx_* instead of out
   int32_t mx_g;                // heads per output group
   uint8_t *mx_data;            // code (t, h, d) at t*mx_st + (h/G)*mx_sg + (c*G + h%G)*32 + d%32, c = d/32
@@ -328,30 +331,6 @@ __device__ __forceinline__ uint8_t *mx_scale_byte(const Params &p, int64_t t, in
          (ka & 3);
 }
 
-// One lane per dim, one warp per 32-dim chunk (dim d = 32c + lane, c
-// warp-uniform): inverse GPT-J rotation when cs_row != null and the chunk
-// lies in dims >= 448 (the pair partner is the neighbouring lane), chunk
-// amax over the warp, cast, and the stores (lane 0 writes the scale byte).
-// All 32 lanes must call it together.
-__device__ __forceinline__ void mx_store_lane(const Params &p, float x, int64_t t, int h, int d,
-                                              const float *cs_row) {
-  const int lane = threadIdx.x & 31;
-  if (cs_row != nullptr && d >= kRopeStart) {
-    const float other = __shfl_xor_sync(0xffffffffu, x, 1);
-    const int i = (d - kRopeStart) >> 1;
-    const float c = __ldg(cs_row + i), s = __ldg(cs_row + kRopeHalf + i);
-    x = (d & 1) ? fmaf(x, c, -(s * other)) : fmaf(x, c, s * other);
-  }
-  float a = fabsf(x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-  a = fmaxf(a, 1e-10f);
-  const uint32_t E = ue8m0_ceil(a * (1.0f / 448.0f));
-  const int c = d >> 5;
-  mx_chunk(p, t, h, c)[lane] = (uint8_t)(e4m3x2_rn_sat(x * ue8m0_inverse(E), 0.f) & 0xFFu);
-  if (lane == 0) *mx_scale_byte(p, t, h, c) = (uint8_t)E;
-}
-
 // Table row of token t for the inverse rotation (null without RoPE or for
 // NeoX, whose inverse the MXFP8 path does not take); a position outside the
 // table uses row 0, as the Q staging does.
@@ -374,3 +353,4 @@ cudaError_t dsa_launch_simt(const dsa::Params &p, cudaStream_t stream);
 cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream);
 bool dsa_tc_supports(int heads_per_group);
 cudaError_t dsa_launch_combine(const dsa::Params &p, cudaStream_t stream);
+cudaError_t dsa_launch_mx_epilogue(const dsa::Params &p, cudaStream_t stream);

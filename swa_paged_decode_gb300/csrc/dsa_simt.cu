@@ -232,9 +232,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) 
     }
 
     // Finalize: whole tokens -> out / lse with the sink; split -> partial slot.
-    // MXFP8 output: a warp holds one 32-dim chunk of a head (d = tid + 256 k).
-    const bool mx = seg.whole && p.mx_on;
-    const float *cs_row = mx ? mx_rope_row(p, t) : nullptr;
+    // MXFP8 output: whole tokens go to the fp32 staging area (cast later).
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int h = i >> 1, d = tid + 256 * (i & 1);
@@ -249,8 +247,8 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_decode_kernel(Params p) 
           }
           v = acc[i] / den;
         }
-        if (mx)
-          mx_store_lane(p, v, t, h0 + h, d, cs_row);
+        if (p.stage)
+          p.stage[((int64_t)t * p.H + h0 + h) * kD + d] = v;
         else
           p.out[((int64_t)t * p.H + h0 + h) * kD + d] = __float2bfloat16_rn(v);
       } else {

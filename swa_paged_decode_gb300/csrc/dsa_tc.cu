@@ -686,26 +686,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       }
       if (seg_worked) ++sord;
       sm_bar();
-      const bool mx = kExt && seg.whole && p.mx_on;
-      const float *cs_row = mx ? mx_rope_row(p, seg.t) : nullptr;
+      // MXFP8 output: whole tokens go to the fp32 staging area (cast later)
+      float *const stage = kExt ? p.stage : nullptr;
 #pragma unroll 1
       for (int mb = 0; mb < 4; ++mb) {
         const int d = 128 * mb + prow;
-        if (mx) {   // a warp holds one 32-dim chunk (dims 128 mb + 32 q4 + lane)
-#pragma unroll 1
-          for (int g8 = 0; g8 < NH / 8; ++g8) {
-            float o[8];
-            if (seg_worked) tc::tmem_ld<8>(tl_lane + Cfg::kColO + mb * HPG + half * NH + 8 * g8, o);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int h = half * NH + 8 * g8 + i;
-              const float iv = red_s[256 - 64 + h];
-              mx_store_lane(p, (!seg_worked || iv == 0.f) ? 0.f : o[i] * iv, seg.t, h0 + h, d,
-                            cs_row);
-            }
-          }
-          continue;
-        }
 #pragma unroll
         for (int g8 = 0; g8 < NH / 8; ++g8) {
           float o[8];
@@ -715,7 +700,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
             const int h = half * NH + 8 * g8 + i;
             const float iv = red_s[256 - 64 + h];
             const float v = (!seg_worked || iv == 0.f) ? 0.f : o[i] * iv;
-            if (seg.whole)
+            if (seg.whole && stage != nullptr)
+              stage[((int64_t)seg.t * p.H + h0 + h) * kD + d] = v;
+            else if (seg.whole)
               p.out[((int64_t)seg.t * p.H + h0 + h) * kD + d] = __float2bfloat16_rn(v);
             else
               p.part_o[(((int64_t)hg * 2 * p.C + seg.slot) * HPG + h) * kD + d] = v;

@@ -293,11 +293,20 @@ CONFIG5_BATCHES = (1, 8, 64, 256, 1024)
 
 
 def make_config(k: int, *, T: Optional[int] = None, device="cpu",
-                seed: Optional[int] = None, page_pad: int = 0) -> Workload:
+                seed: Optional[int] = None, page_pad: int = 0, v41: bool = False) -> Workload:
+    """Measured configuration k. ``v41``: the same shapes and draws in the
+    V4.1 form -- every fp8-528 list holds ue8m0-scaled records, RoPE pairs
+    dims GPT-J style."""
     c = dict(CONFIGS[k])
     if T is not None:
         c["T"] = T
     name = f"config{k}_T{c['T']}_H{c['H']}"
+    if v41:
+        for key in ("swa", "extra"):
+            if c[key] is not None and c[key]["fmt"] == FMT_FP8_528:
+                c[key] = dict(c[key], fmt=FMT_FP8_528_UE8M0)
+        c["rope_style"] = ROPE_GPTJ
+        name += "_v41"
     return make_workload(seed=(k - 1) if seed is None else seed, device=device,
                          name=name, page_pad=page_pad, **c)
 

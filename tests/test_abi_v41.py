@@ -20,6 +20,8 @@ def mx_desc(**over):
 
 def run_v41(lib, a, rope_style=B.DSA_ROPE_GPTJ, out=None, mx=None, **over):
     k = dict(a.kw)
+    if mx is not None:   # an MXFP8 call needs the plan's larger workspace
+        k["ws_bytes"] = a.plan.workspace_bytes_mx
     k.update(over)
     swa = over.get("swa_desc", a.swa)
     extra = over.get("extra_desc", a.extra)
@@ -90,15 +92,38 @@ def test_combine_v41_validation(lib):
     assert a.plan.ctas_per_group > 1
     p = ctypes.byref(a.plan)
     f = lib.dsa_decode_combine_v41
-    assert f(p, FAKE, a.nbytes, None, None, None, 0, 1, None, None, FAKE, None) == -1
+    nb, nm = a.nbytes, a.plan.workspace_bytes_mx
+    assert f(p, FAKE, nb, None, None, None, 0, 1, None, None, FAKE, None) == -1
     m = mx_desc()
-    assert f(p, FAKE, a.nbytes, None, None, None, 0, 1, FAKE, ctypes.byref(m), FAKE, None) == -1
-    assert f(p, FAKE, a.nbytes, None, FAKE, FAKE, 16, 0, None, ctypes.byref(m), FAKE, None) == -2
-    assert f(p, FAKE, a.nbytes, None, FAKE, None, 16, 1, None, ctypes.byref(m), FAKE, None) == -1
+    assert f(p, FAKE, nm, None, None, None, 0, 1, FAKE, ctypes.byref(m), FAKE, None) == -1
+    assert f(p, FAKE, nm, None, FAKE, FAKE, 16, 0, None, ctypes.byref(m), FAKE, None) == -2
+    assert f(p, FAKE, nm, None, FAKE, None, 16, 1, None, ctypes.byref(m), FAKE, None) == -1
     assert f(p, None, 0, None, None, None, 0, 1, None, ctypes.byref(m), FAKE, None) == -4
-    assert f(p, FAKE, a.nbytes, None, None, None, 0, 7, FAKE, None, FAKE, None) == -1
+    assert f(p, FAKE, nb, None, None, None, 0, 7, FAKE, None, FAKE, None) == -1
     bad = mx_desc(group_size=5)
-    assert f(p, FAKE, a.nbytes, None, None, None, 0, 1, None, ctypes.byref(bad), FAKE, None) == -1
+    assert f(p, FAKE, nm, None, None, None, 0, 1, None, ctypes.byref(bad), FAKE, None) == -1
+
+
+def test_mxfp8_workspace_size(lib):
+    a = Args(T=4, H=16)
+    p = a.plan
+    assert p.ws_stage_offset >= p.workspace_bytes and p.ws_stage_offset % 256 == 0
+    assert p.workspace_bytes_mx == p.ws_stage_offset + 4 * 4 * 16 * 512
+    # the bf16 workspace is too small for an MXFP8 call (a later check would give -2)
+    assert run_v41(lib, a, mx=mx_desc(), ws_bytes=a.nbytes, swa_desc=FMT7) == -4
+    assert run_v41(lib, a, mx=mx_desc(), swa_desc=FMT7) == -2
+    c = Args(T=64, we=512)
+    f = lib.dsa_decode_combine_v41
+    m = mx_desc()
+    assert f(ctypes.byref(c.plan), FAKE, c.nbytes, None, None, None, 0, 1, None, ctypes.byref(m),
+             FAKE, None) == -4
+    # with bf16 output, a plan that splits nothing needs no combine; MXFP8 does
+    d = Args(T=1, we=0)
+    assert d.plan.ctas_per_group == 1
+    g = lib.dsa_decode_combine_v41
+    assert g(ctypes.byref(d.plan), None, 0, None, None, None, 0, 1, FAKE, None, FAKE, None) == 0
+    assert g(ctypes.byref(d.plan), None, 0, None, None, None, 0, 1, None, ctypes.byref(m), FAKE,
+             None) == -4
 
 
 def test_zero_tokens_v41_is_a_no_op(lib):
