@@ -306,17 +306,24 @@ __device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g
   } else {
     // chunk c = 4m + 2j + e holds dims [32c, 32c+32) of k-block 2m + j;
     // M block mb is m = mb, e in {0, 1}; its 4 scales are word 2mb + j of
-    // the scale bytes (d[8] words 0..3, d[9] words 4..7)
+    // the scale bytes (d[8] words 0..3, d[9] words 4..7). The two lanes of a
+    // row write the same swizzle positions of two k-blocks; the odd lane
+    // takes its halves in the other order (e = ee ^ j), so the 8 lanes of a
+    // quarter-warp store to 8 different bank groups. Its chunk position
+    // (4e + i) ^ (r % 8) is (4ee + i) ^ r7j with r7j = (r % 8) ^ 4j.
     const uint4 sq = mb < 2 ? g.d[8] : g.d[9];
-    const uint32_t sw = j == 0 ? ((mb & 1) ? sq.z : sq.x) : ((mb & 1) ? sq.w : sq.y);
+    const uint32_t sw0 = j == 0 ? ((mb & 1) ? sq.z : sq.x) : ((mb & 1) ? sq.w : sq.y);
+    const uint32_t sw = j == 0 ? sw0 : __funnelshift_l(sw0, sw0, 16);
+    const uint32_t rb = kv_base + (uint32_t)(2 * mb + j) * 16384u + (uint32_t)(row >> 3) * 1024u +
+                        (uint32_t)(row & 7) * 128u;
+    const int r7j = (row & 7) ^ (4 * j);
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int k = 2 * mb + e;
-      const int c = 4 * mb + 2 * j + e;
-      const uint32_t pair = (sw >> (16 * e)) & 0xFFFFu;
+    for (int ee = 0; ee < 2; ++ee) {
+      const uint4 src = (ee == j) ? g.d[2 * mb] : g.d[2 * mb + 1];
+      const uint32_t pair = (sw >> (16 * ee)) & 0xFFFFu;
       const uint32_t s2 = tc::e4m3x2_to_f16x2(pair);
       const uint32_t sa = __byte_perm(s2, s2, 0x1010), sb = __byte_perm(s2, s2, 0x3232);
-      const uint32_t w[4] = {g.d[k].x, g.d[k].y, g.d[k].z, g.d[k].w};
+      const uint32_t w[4] = {src.x, src.y, src.z, src.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {  // word i = dims [32c + 8i, +8)
         uint32_t f[4];
@@ -324,8 +331,7 @@ __device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g
         const uint32_t sc = i < 2 ? sa : sb;
 #pragma unroll
         for (int q = 0; q < 4; ++q) f[q] = tc::hmul2(f[q], sc);
-        const int kb = c >> 1, ci = (4 * c + i) & 7;
-        tc::st_shared_v4(kv_base + sw128_off(row, kb, ci, 16384), f[0], f[1], f[2], f[3]);
+        tc::st_shared_v4(rb + ((uint32_t)((4 * ee + i) ^ r7j) << 4), f[0], f[1], f[2], f[3]);
       }
     }
   }
