@@ -43,9 +43,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # while the kernel sources hash to `sources`. The capture is summarised under
 # profiles/ with the command that made it.
 NCU_TRAFFIC = {
-    "sources": "3bfa6a593ccef033",
+    "sources": "0f9adf19eec334c3",
     "workload": "config5_T256_H64",
-    "bytes_per_launch": 426152704 + 25781248,
+    "bytes_per_launch": 426228736 + 25545984,
     "rows_per_launch": 256 * (128 + 4096),
 }
 KERNEL_SOURCES = ("swa_paged_decode_gb300/csrc/dsa_tc.cu", "swa_paged_decode_gb300/csrc/tc_ptx.cuh",
