@@ -34,3 +34,27 @@ def test_graph_replay_matches_direct_call():
         assert torch.equal(dec.out.view(torch.int16), ref_out.view(torch.int16))
         assert torch.equal(dec.lse.view(torch.int32), ref_lse.view(torch.int32))
         assert B.dsa_decode_read_status(dec.workspace) == 0
+
+
+def test_graph_replay_v41_mxfp8():
+    # run_v41 + combine_v41 + the MXFP8 cast, captured and replayed
+    BLD.build()
+    B.load()
+    w = W.make_config(3, device="cuda", v41=True)
+    dec = B.Decoder(w, mx_group=8)
+    assert dec.plan.ctas_per_group > 1
+    mx, lse = dec(w)
+    torch.cuda.synchronize()
+    ref = (mx.data.clone(), mx.scale.clone(), lse.clone())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dec(w)
+    for _ in range(2):
+        mx.data.fill_(0x7F)
+        mx.scale.fill_(-1)
+        dec.lse.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(mx.data, ref[0]) and torch.equal(mx.scale, ref[1])
+        assert torch.equal(dec.lse.view(torch.int32), ref[2].view(torch.int32))
+        assert B.dsa_decode_read_status(dec.workspace) == 0
