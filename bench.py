@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # while the kernel sources hash to `sources`. The capture is summarised under
 # profiles/ with the command that made it.
 NCU_TRAFFIC = {
-    "sources": "0f9adf19eec334c3",
+    "sources": "785b2e910b26d3bf",
     "workload": "config5_T256_H64",
     "bytes_per_launch": 426228736 + 25545984,
     "rows_per_launch": 256 * (128 + 4096),

@@ -3,15 +3,19 @@
 // One persistent CTA per SM walks a contiguous range of (token, 128-row tile)
 // units with three warp-specialised roles joined by mbarriers:
 //
-//   producers (warps 8-15)  gather: predicated 16-byte loads of the tile's
-//            128 records, one tile ahead, held in registers (thread = one row
-//            and one half of its 32-byte sectors); dequant: records -> f16
-//            K-major tile in shared memory, 128-byte swizzle (16-byte chunk c
-//            of row r at chunk c ^ (r % 8)), written one 128-dim block at a
-//            time as soon as the PV MMAs of the previous tile release it.
-//            NVFP4: e2m1 * e4m3 scale (exact in f16). fp8: e4m3 * the fp32
-//            block scale rounded to f16, the product rounded to f16
-//            (relative error <= 2^-11 per element).
+//   producers (warps 8-15)  gather: the tile's 128 records, one tile ahead,
+//            held in registers (the two halves of a row in adjacent lanes;
+//            32-byte loads where a record starts on a 32-byte boundary, the
+//            aligned 32-byte sectors around fp8 records 16 bytes off that
+//            grid, predicated 16-byte loads otherwise); dequant: records ->
+//            f16 K-major tile in shared memory, 128-byte swizzle (16-byte
+//            chunk c of row r at chunk c ^ (r % 8)), written one 128-dim block
+//            at a time as soon as the PV MMAs of the previous tile release
+//            it. NVFP4: e2m1 * e4m3 scale (exact in f16). fp8: e4m3 * the
+//            fp32 block scale rounded to f16, the product rounded to f16
+//            (relative error <= 2^-11 per element). fp8 with ue8m0 scales
+//            (the V4.1 record): e4m3 * 2^(b - 127), exact in f16 for scale
+//            exponents in [-15, 7].
 //   MMA issue (one thread of warp 0)  swap-AB tcgen05.mma kind::f16:
 //            S[128 rows, H] = K[128, 512] . Q[H, 512]^T into TMEM, issued back
 //            to back once the tile has landed; then O^T[512, H] += K^T . P in four
@@ -21,11 +25,16 @@
 //            per thread; scores x = S * scale * log2e;
 //            base-2 running max per head that moves only when a score passes
 //            it by 2^8 (then O in TMEM and the partial sums are rescaled);
-//            P = 2^(x - m) as f16. Also stages Q (NeoX RoPE,
+//            P = 2^(x - m) as f16. Also stages Q (NeoX or GPT-J RoPE,
 //            per-head power-of-two prescale into f16) and, per token,
 //            reduces the sums, folds the sink into the denominator and writes
-//            out (bf16) and lse (fp32) -- or an fp32 partial for a token split
-//            over CTAs, merged later by the combine kernel.
+//            out (bf16) and lse (fp32) -- or, for MXFP8 output, the fp32
+//            output to a staging area that a separate kernel casts -- or an
+//            fp32 partial for a token split over CTAs, merged later by the
+//            combine kernel.
+//
+// The V4.1 options (ue8m0 records, GPT-J RoPE, MXFP8 staging) exist only in
+// the kExt instantiation; the plain one compiles without them.
 //
 // Tiles whose first row lies past min(len, width) are skipped by every role
 // (each evaluates the same predicate from the lengths), so all roles walk the
