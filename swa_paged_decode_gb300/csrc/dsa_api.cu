@@ -303,6 +303,7 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   plan->balance_live = (num_tokens >= 16 && plan->tiles_per_token >= 8) ? 1 : 0;
   // Workspace: status | sel[T][2] | part_lse[HG][2C][hpg] | part_sel[2C][2] |
   //            part_o[HG][2C][hpg][512] | bounds[C+1]
+  //            (| stage[T][H][512] fp32, for MXFP8 output only)
   const int64_t slots = 2 * ctas;
   int64_t off = kStatusBytes;
   plan->ws_sel_offset = off;

@@ -1,4 +1,5 @@
-// dsa_combine.cu -- split-KV LSE combine.
+// dsa_combine.cu -- split-KV LSE combine, and the MXFP8 output cast of the
+// V4.1 form (mx_epilogue_kernel, below).
 //
 // A token whose units the schedule spreads over CTAs c0..c1 left one
 // normalised partial (O_i, lse_i) per CTA. This kernel merges them in CTA
