@@ -64,6 +64,12 @@ constexpr int kTcThreads = 32 * (kSmWarps + kPrWarps);
 constexpr int kLaunchRegs = 128;
 constexpr long long kWaitBudget = 4000000000ll;  // SM cycles (~2 s) per wait
 constexpr float kRescaleSlack = 8.0f;            // log2 headroom of the running max
+// Row exponents: an fp8 row is written to the f16 tile as k * 2^-e, e the
+// exponent of its largest block scale (so its largest scale lies in [1, 2)),
+// clamped to [-kRowExpMax, kRowExpMax]; the softmax puts 2^e back exactly.
+constexpr int kRowExpMax = 48;
+constexpr int32_t kRowInvalid = INT32_MIN;       // row record of a row that is not kept
+constexpr float kMaxInit = -1e30f;               // running max before any kept row
 
 template <int HPG>
 struct TcCfg {
@@ -75,7 +81,7 @@ struct TcCfg {
   static constexpr uint32_t kKV = 0;                     // 128 x 512 f16 = 128 KiB
   static constexpr uint32_t kQ = 131072;                 // HPG x 512 f16
   static constexpr uint32_t kP = kQ + HPG * 1024;        // [128 x HPG] f16
-  static constexpr uint32_t kRho = kP + kPBytes;         // [128] f32 row flag: 1 kept, 0 not
+  static constexpr uint32_t kRho = kP + kPBytes;         // [128] int32 row exponent, kRowInvalid: not kept
   static constexpr uint32_t kHeadF = kRho + 1024;        // [64] f32 per-head score factor
   static constexpr uint32_t kM = kHeadF + 256;           // [64] running max (log2)
   static constexpr uint32_t kRed = kM + 256;             // [4][64] f32
@@ -186,6 +192,16 @@ __device__ __forceinline__ uint32_t scale_f16x2(float s) {
   return hb | (hb << 16);
 }
 
+// 2^e as fp32 for an integer e in [-126, 127] (exact).
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// Row exponent from the largest biased exponent field (8 bits, bias 127) of
+// a row's block scales: e = field - 127, clamped to [-kRowExpMax, kRowExpMax].
+__device__ __forceinline__ int row_exp(uint32_t field) {
+  const int e = (int)field - 127;
+  return e < -kRowExpMax ? -kRowExpMax : (e > kRowExpMax ? kRowExpMax : e);
+}
+
 // ---------------------------------------------------------------- producer
 // Thread (producer warp pw, lane l): row 32*(pw%4) + l, half j = pw/4 of the
 // record's 16-byte chunks: c = 4m + 2j + e (e in {0,1}) -- whole sectors.
@@ -282,8 +298,8 @@ __device__ __forceinline__ uint4 shfl_xor_u4(const uint4 v, int mask) {
 // half. Called by all 32 lanes of the warp (fp8 rows in sector layout get the
 // missing half of each chunk pair from the other lane of their row).
 __device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g,
-                                              const uint32_t (&scale2)[4], int mb, int row, int j,
-                                              uint32_t kv_base) {
+                                              const uint32_t (&scale2)[4], float rnorm, int mb,
+                                              int row, int j, uint32_t kv_base) {
   if (fp8) {
     // chunks c = 4m + 2j + e of k-block m; M block mb = k-blocks {2mb, 2mb+1}
 #pragma unroll
@@ -291,11 +307,12 @@ __device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g
       const int m = 2 * mb + mm;
       const uint4 recv = shfl_xor_u4(j == 0 ? g.d[2 * m + 2] : g.d[2 * m], 1);
       const uint4 pr[2] = {g.pl ? g.d[2 * m] : g.d[2 * m + 1], g.pl ? g.d[2 * m + 1] : recv};
-      // fp32 scales: scale2[mb] is the block's f16 pair. ue8m0: scale2 holds
-      // the 16 raw scale bytes; this lane's 32 dims of k-block m (chunks
-      // 4m + 2j + e) take byte 2m + j.
+      // fp32 scales: scale2[mb] is the block's normalized f16 pair. ue8m0:
+      // scale2 holds the 16 raw scale bytes; this lane's 32 dims of k-block m
+      // (chunks 4m + 2j + e) take byte 2m + j, times the row's 2^-e (rnorm).
       const uint32_t sc =
-          ue ? scale_f16x2(ue8m0_to_f32(scale2[m >> 1] >> (16 * (m & 1) + 8 * j))) : scale2[mb];
+          ue ? scale_f16x2(ue8m0_to_f32(scale2[m >> 1] >> (16 * (m & 1) + 8 * j)) * rnorm)
+             : scale2[mb];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int c = 4 * m + 2 * j + e;   // dims [16c, 16c+16), scale block mb
@@ -385,7 +402,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   const uint32_t kv_base = sbase + Cfg::kKV;
   const uint32_t q_base = sbase + Cfg::kQ;
   const uint32_t p_base = sbase + Cfg::kP;
-  float *row_ok_s = reinterpret_cast<float *>(smem + Cfg::kRho);
+  int32_t *row_e_s = reinterpret_cast<int32_t *>(smem + Cfg::kRho);
   float *m_s = reinterpret_cast<float *>(smem + Cfg::kM);
   float *headf_s = reinterpret_cast<float *>(smem + Cfg::kHeadF);
   float *red_s = reinterpret_cast<float *>(smem + Cfg::kRed);
@@ -478,21 +495,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const bool fp8 = p.list[lid].fmt != DSA_REC_NVFP4_288;
       const bool ue = kExt && p.list[lid].fmt == DSA_REC_FP8_528_UE8M0;
       uint32_t scale2[4] = {0, 0, 0, 0};
+      // Row exponent e (fp8 rows): the tile holds k * 2^-e, so the row's
+      // largest block scale lies in [1, 2) and every block within 2^14 of it
+      // keeps f16 precision, whatever the row's magnitude. NVFP4 rows (e2m1
+      // times an e4m3 scale: exact f16 normals) keep e = 0.
+      int erow = 0;
       if (fp8) {   // sector layout: lane j = 1 takes the scales from lane j = 0
         const uint4 sp = shfl_xor_u4(g.d[17], 1);
         const uint4 sv = (!g.pl && j == 1) ? sp : g.d[17];
-        if (ue) {   // raw bytes, decoded per k-block
-          scale2[0] = sv.x;
-          scale2[1] = sv.y;
-          scale2[2] = sv.z;
-          scale2[3] = sv.w;
-        } else {
-          scale2[0] = scale_f16x2(__uint_as_float(sv.x));
-          scale2[1] = scale_f16x2(__uint_as_float(sv.y));
-          scale2[2] = scale_f16x2(__uint_as_float(sv.z));
-          scale2[3] = scale_f16x2(__uint_as_float(sv.w));
+        scale2[0] = sv.x;
+        scale2[1] = sv.y;
+        scale2[2] = sv.z;
+        scale2[3] = sv.w;
+        if (ue) {   // raw bytes, decoded per k-block; e from the largest byte
+          uint32_t mx = __vmaxu4(__vmaxu4(sv.x, sv.y), __vmaxu4(sv.z, sv.w));
+          mx = max(max(mx & 0xFFu, (mx >> 8) & 0xFFu), max((mx >> 16) & 0xFFu, mx >> 24));
+          erow = row_exp(mx);
+        } else {    // e from the largest exponent field of the 4 fp32 scales
+          const uint32_t f = max(max((sv.x >> 23) & 0xFFu, (sv.y >> 23) & 0xFFu),
+                                 max((sv.z >> 23) & 0xFFu, (sv.w >> 23) & 0xFFu));
+          erow = row_exp(f);
+          const float rn = pow2i(-erow);
+#pragma unroll
+          for (int b = 0; b < 4; ++b) scale2[b] = scale_f16x2(__uint_as_float(scale2[b]) * rn);
         }
       }
+      const float rnorm = pow2i(-erow);
       if (j == 0 && g.ok) {
         kept += 1;
         chk += row_hash(g.sid, g.r, lid);
@@ -515,8 +543,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 #pragma unroll
       for (int mb = 0; mb < 4; ++mb) {
         if (!first) wait(kBarKvFree + mb, ph_free[mb]);
-        if (mb == 0 && j == 0) row_ok_s[row] = g.ok ? 1.f : 0.f;
-        dequant_block(fp8, ue, g, scale2, mb, row, j, kv_base);
+        if (mb == 0 && j == 0) row_e_s[row] = g.ok ? erow : kRowInvalid;
+        dequant_block(fp8, ue, g, scale2, rnorm, mb, row, j, kv_base);
       }
       // One hand-off per tile: the QK MMAs are issued once the whole tile is
       // in place, so per-block fences and arrives would only lengthen the
@@ -635,7 +663,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         tc::st_shared_v4(q_base + sw128_off(h, kb, ci, HPG * 128), f[0], f[1], f[2], f[3]);
         tc::st_shared_v4(q_base + sw128_off(h, kb, ci + 1, HPG * 128), f[4], f[5], f[6], f[7]);
       }
-      if (tid < HPG) m_s[tid] = -INFINITY;
+      if (tid < HPG) m_s[tid] = kMaxInit;
       tc::fence_async_smem();
       sm_bar();   // Q (async proxy), head factors and m_s visible
     };
@@ -774,7 +802,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         // the row flags are written with block 0 of the tile
         wait(kBarKvFull, ph_kv);
       }
-      const bool rv = row_ok_s[prow] != 0.f;
+      // This thread's row: kept or not, and its exponent e (the tile holds
+      // k * 2^-e). In log2 units the row's score is x = S * hf * 2^e; the
+      // running max m and P work on y = x + e, so P = 2^(y - m) carries the
+      // factor 2^e that PV needs to rebuild k from the tile, while the row
+      // sums take P * 2^-e = 2^(x - m): out = O / l and lse = m + log2 l
+      // keep their form. Rows that are not kept get y = -inf (P = 0).
+      const int32_t ei = row_e_s[prow];
+      const bool rv = ei != kRowInvalid;
+      const float er = rv ? (float)ei : -INFINITY;
+      const float rs = rv ? pow2i(ei) : 0.f;
+      const float rinv = rv ? pow2i(-ei) : 0.f;
       wait(kBarSFull, ph_s);
       tc::tc_fence_after();
       // S of this thread's row and head half (TMEM -> registers)
@@ -819,9 +857,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float &xv = x[4 * g4 + i];
-          const float xs = rv ? xv * hf[i] : -INFINITY;
-          need |= xs > mm[i] + kRescaleSlack;
-          xv = (xs == -INFINITY) ? 0.f : tc::ex2(xs - mm[i]);
+          const float t = fmaf(xv, hf[i] * rs, er - mm[i]);   // y - m (-inf if not kept)
+          need |= t > kRescaleSlack;
+          xv = tc::ex2(t);
         }
       }
       store_p(x);
@@ -832,7 +870,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         tc::tc_fence_after();
         load_s(x);
 #pragma unroll
-        for (int j = 0; j < NH; ++j) x[j] = rv ? x[j] * headf_s[half * NH + j] : -INFINITY;
+        for (int j = 0; j < NH; ++j) x[j] = fmaf(x[j], headf_s[half * NH + j] * rs, er);   // y
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
           float v = x[j];
@@ -845,7 +883,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           const float tm = fmaxf(fmaxf(red_s[tid], red_s[64 + tid]), fmaxf(red_s[128 + tid], red_s[192 + tid]));
           const float mo = m_s[tid];
           const float mn = fmaxf(mo, tm);
-          red_s[tid] = (mn == -INFINITY) ? 1.f : (mo == -INFINITY ? 0.f : tc::ex2(mo - mn));
+          red_s[tid] = tc::ex2(mo - mn);   // 0 when mo is still kMaxInit
           m_s[tid] = mn;
         }
         sm_bar();
@@ -872,7 +910,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float &xv = x[4 * g4 + i];
-            xv = (xv == -INFINITY) ? 0.f : tc::ex2(xv - mm[i]);
+            xv = tc::ex2(xv - mm[i]);   // y = -inf (row not kept): 0
           }
         }
         store_p(x);
@@ -881,7 +919,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         sm_bar();   // P, O and red_s settled before PV
       }
 #pragma unroll
-      for (int j = 0; j < NH; ++j) l_reg[j] += x[j];
+      for (int j = 0; j < NH; ++j) l_reg[j] = fmaf(x[j], rinv, l_reg[j]);   // += 2^(x - m)
       // ---- O^T += K^T . P
       if (issuer && !*abort_s) {
         tc::tc_fence_after();

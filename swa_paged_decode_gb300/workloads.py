@@ -167,9 +167,11 @@ def encode_nvfp4_records(x: torch.Tensor) -> torch.Tensor:
 
 
 def make_cache(num_slots: int, page_size: int, fmt: int, gen: torch.Generator,
-               device, page_pad: int = 0, chunk: int = 1 << 18) -> PagedCache:
+               device, page_pad: int = 0, chunk: int = 1 << 18, mag=(0,)) -> PagedCache:
     """N(0,1) source rows, quantized to records, laid out in pages.
-    ``page_pad`` extra bytes (multiple of 16) separate consecutive pages."""
+    ``page_pad`` extra bytes (multiple of 16) separate consecutive pages.
+    ``mag``: powers of two; the source row of slot s is scaled by
+    2^mag[s % len(mag)] before it is quantized (default: unit rows)."""
     assert num_slots % page_size == 0 and page_pad % 16 == 0
     rb = RECORD_BYTES[fmt]
     num_pages = num_slots // page_size
@@ -182,6 +184,10 @@ def make_cache(num_slots: int, page_size: int, fmt: int, gen: torch.Generator,
     for s0 in range(0, num_slots, chunk):
         s1 = min(num_slots, s0 + chunk)          # both multiples of page_size
         x = torch.randn((s1 - s0, HEAD_DIM), generator=gen, device=device)
+        if tuple(mag) != (0,):
+            m = torch.tensor([float(k) for k in mag], dtype=torch.float32, device=device)
+            sl = torch.arange(s0, s1, device=device) % len(mag)
+            x = x * torch.exp2(m[sl])[:, None]
         recs[s0 // page_size: s1 // page_size] = enc(x).view(-1, page_size, rb)
     return PagedCache(data, page_size, fmt)
 
@@ -230,18 +236,24 @@ def _lens(T, width, lens, gen, device):
 def make_workload(*, T: int, H: int, swa: dict, extra: Optional[dict] = None,
                   sink: bool = False, rope: bool = False, seed: int = 0,
                   device="cpu", name: str = "custom", page_pad: int = 0,
-                  scale: Optional[float] = None, rope_style: int = ROPE_NEOX) -> Workload:
+                  scale: Optional[float] = None, rope_style: int = ROPE_NEOX,
+                  q_log2: int = 0) -> Workload:
     """Build a workload.
 
     swa / extra: dict(width, lens=(lo, hi) inclusive or "full", fmt, page,
-    slots, invalid=fraction of in-range entries replaced by -1 (default 0)).
+    slots, invalid=fraction of in-range entries replaced by -1 (default 0),
+    mag=powers of two scaling the source rows per slot, see make_cache).
+    q_log2: Q is drawn N(0,1) and scaled by 2^q_log2 (exact in bf16).
     """
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     specs = [swa] + ([extra] if extra is not None else [])
-    caches = [make_cache(s["slots"], s["page"], s["fmt"], gen, device, page_pad)
-              for s in specs]
-    q = torch.randn((T, H, HEAD_DIM), generator=gen, device=device).to(torch.bfloat16)
+    caches = [make_cache(s["slots"], s["page"], s["fmt"], gen, device, page_pad,
+                         mag=s.get("mag", (0,))) for s in specs]
+    q = torch.randn((T, H, HEAD_DIM), generator=gen, device=device)
+    if q_log2:
+        q = q * 2.0 ** q_log2
+    q = q.to(torch.bfloat16)
     lens = [_lens(T, s["width"], s.get("lens", "full"), gen, device) for s in specs]
     ids = [sample_distinct(T, s["width"], s["slots"], gen, device) for s in specs]
     lists = []
