@@ -62,11 +62,17 @@ typedef enum {
  *            i), then 32 e4m3 scales (one per 16 dims); value = code * scale.
  * FP8_528_UE8M0: 512 e4m3 codes, then 16 ue8m0 scale bytes (one per 32
  *            dims); value = code * 2^(byte - 127) (the V4.1 record of the
- *            swapab page, stage_inputs fp8 branch). The kernels compute in
- *            f16 tiles: values are exact while every scale exponent
- *            byte - 127 lies in [-15, 7]; outside that range they are rounded
- *            to f16 (a scale byte of 0xFF, NaN in E8M0, gives non-finite
- *            values).
+ *            swapab page, stage_inputs fp8 branch). A scale byte of 0xFF
+ *            (NaN in E8M0) gives non-finite values.
+ * Precision of the tensor-core kernels: every row is written to an f16 tile
+ * as value * 2^-e, e the exponent of the row's largest block scale (clamped
+ * to [-48, 48]), and 2^e is applied again in fp32 after the products, so a
+ * row's magnitude does not matter. NVFP4 and FP8_528_UE8M0 values are then
+ * exact (UE8M0: blocks within 2^15 of the row's largest scale, and block
+ * exponents in [-63, 55]; smaller blocks are rounded, relative to the row's
+ * largest, below 2^-24); FP8_528 values are code * (scale * 2^-e rounded to
+ * f16), rounded to f16 (relative error <= 2^-11 for blocks within 2^14 of
+ * the row's largest scale; scales up to 2^55).
  * Source: the swapab page (record sizes 528 and 288, NVFP4 block of 16 with
  * e4m3 scales) with the fp32-per-128 scale layout of FlashMLA's V3.2 record
  * (sparse_decode.h, bytes_per_token = 512 + ... + (512/128)*4).            */
@@ -134,6 +140,11 @@ typedef struct {
 } dsa_decode_plan_t;
 
 /* Plan one decode call.
+ * Defined by: FlashMLA's sparse_decode.h page, the scheduling metadata made
+ * before the decode launch (get_decoding_sched_meta, run with num_sm_parts =
+ * max(num_sms / s_q, 1) parts in get_meta): here the work of all tokens is
+ * cut into (token, 128-row tile) units, spread over the SMs, and the split
+ * tokens' partial buffers sized (cf. lse_accum / o_accum there).
  * num_tokens >= 0; num_heads in {16, 32, 48, 64, 96, 128}; swa_width >= 1;
  * extra_width >= 0 (0 = no extra list). num_sms: SM count to spread the
  * work over (0 = query the current device). On success fills *plan and
@@ -147,6 +158,13 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
 /* Run the fused gather + dequant + attention kernel (argument order after the
  * plan and workspace follows the problem statement: q, sliding-window cache
  * and list, extra cache and list, sink, positions, cos_sin, scale, out, lse).
+ * Defined by: the swapab page, SwapABDecodeKernel.__call__ (its docstring
+ * gives the arguments: paged uint8 caches whose pages may lie further apart
+ * than page * record bytes, [s_q, width] int32 slot lists with -1 invalid,
+ * [s_q] int32 lengths, int64 positions, the cos/sin table, the sink) and
+ * FlashMLA's sparse_decode.h page, sparse_attn_decode_interface (MQA with
+ * one KV head, d_v = 512, an optional extra cache with its own indices and
+ * lengths, an optional attention sink, out and lse returned).
  *
  * q          : bf16 [T, H, 512], element (t, h, d) at q + t*q_stride_t +
  *              h*q_stride_h + d (strides in elements); 16-byte aligned rows.
@@ -179,7 +197,11 @@ dsa_status dsa_decode_run(const dsa_decode_plan_t *plan, void *workspace,
                           int64_t cos_sin_rows, float scale, void *out, float *lse,
                           dsa_stream_t stream);
 
-/* Merge the split-KV partials left in the workspace by dsa_decode_run:
+/* Defined by: FlashMLA's sparse_decode.h page, the combine launch after the
+ * decode (run_flash_mla_combine_kernel over lse_accum / o_accum with the
+ * attention sink), and the production.py page's Python KV merge
+ * (O = sum_i exp(lse_i) O_i / sum_i exp(lse_i), lse = log sum_i exp(lse_i)).
+ * Merge the split-KV partials left in the workspace by dsa_decode_run:
  * out = sum_i e^{lse_i} O_i / (sum_i e^{lse_i} + e^{sink}), lse = log sum_i
  * e^{lse_i}, in a fixed split order (bitwise deterministic). `sink` must be
  * the pointer given to run (or NULL). Launches nothing when the plan splits
@@ -214,7 +236,10 @@ typedef struct {
   int32_t reserved;
 } dsa_mxfp8_out;
 
-/* dsa_decode_run with the V4.1 options (the swapab page's mega-kernel call):
+/* Defined by: the swapab page, SwapABDecodeKernel (stage_inputs: fp8 records
+ * with ue8m0 scales per 32 dims and GPT-J RoPE of Q; the merge step: inverse
+ * RoPE, MXFP8 cast with ue8m0 scales per 32 dims, o-fused store).
+ * dsa_decode_run with the V4.1 options (the swapab page's mega-kernel call):
  *   rope_style: DSA_ROPE_NEOX or DSA_ROPE_GPTJ (used when RoPE is on).
  *   out / mx  : exactly one non-NULL. out: bf16 [T, H, 512] as in
  *               dsa_decode_run. mx: MXFP8 output; with RoPE on, dims >= 448
@@ -238,7 +263,11 @@ dsa_status dsa_decode_run_v41(const dsa_decode_plan_t *plan, void *workspace,
                               void *out, const dsa_mxfp8_out *mx, float *lse,
                               dsa_stream_t stream);
 
-/* dsa_decode_combine for dsa_decode_run_v41: the same plan, workspace, sink,
+/* Defined by: the swapab page's merge step (steps 8-9 of
+ * SwapABDecodeKernel: fixed-order merge of the partials, sink folded once,
+ * then the inverse RoPE / MXFP8 / o-fused epilogue) and FlashMLA's combine
+ * launch.
+ * dsa_decode_combine for dsa_decode_run_v41: the same plan, workspace, sink,
  * positions, cos_sin, rope_style and output (out or mx) as given to run.
  * With mx it merges the split tokens into the staging area and then casts
  * every token to MXFP8 (one more launch, also for plans that split nothing). */
@@ -248,7 +277,11 @@ dsa_status dsa_decode_combine_v41(const dsa_decode_plan_t *plan, void *workspace
                                   int64_t cos_sin_rows, int32_t rope_style, void *out,
                                   const dsa_mxfp8_out *mx, float *lse, dsa_stream_t stream);
 
-/* Row-selection record of the last run+combine on this workspace: per token
+/* Defined by: the swapab page, stage_inputs (a list position names a row iff
+ * it lies below min(length, width) and its slot id is a cache slot; invalid
+ * rows read nothing). This call exports that selection for checking; the
+ * pages have no call of their own for it.
+ * Row-selection record of the last run+combine on this workspace: per token
  * the number of kept rows (kept[T], int32, device) and the sum mod 2^32 over
  * kept rows of fmix32(id * 0x9E3779B1 + 2*position + list) (checksum[T],
  * uint32, device; list 0 = sliding window, 1 = extra; fmix32 = MurmurHash3's
@@ -256,8 +289,12 @@ dsa_status dsa_decode_combine_v41(const dsa_decode_plan_t *plan, void *workspace
 dsa_status dsa_decode_selection(const dsa_decode_plan_t *plan, const void *workspace,
                                 int32_t *kept, uint32_t *checksum, dsa_stream_t stream);
 
-/* Device status word of the workspace (DSA_OK, or DSA_ERR_TIMEOUT when a
- * bounded device wait gave up). SYNCHRONIZES `stream` to read it. */
+/* Defined by: the argument checks of FlashMLA's sparse_attn_decode_interface
+ * (TORCH_CHECK) and the swapab page's dispatch asserts, for the conditions
+ * only the device sees: the device status word of the workspace (DSA_OK;
+ * DSA_ERR_INVALID_ARG when a position lies outside the cos/sin table;
+ * DSA_ERR_TIMEOUT when a bounded device wait gave up). SYNCHRONIZES `stream`
+ * to read it. */
 dsa_status dsa_decode_read_status(const void *workspace, dsa_stream_t stream,
                                   int32_t *device_status);
 
@@ -282,7 +319,8 @@ dsa_status dsa_decode_read_status(const void *workspace, dsa_stream_t stream,
  *   device_status: optional int32 device pointer (4-byte aligned). When
  *         non-NULL, it receives an asynchronous copy of the device status
  *         word (DSA_OK, or what the kernels recorded, as
- *         dsa_decode_read_status reports it).
+ *         dsa_decode_read_status reports it); DSA_OK for a plan of 0 tokens.
+ *         Each call starts from a cleared status word.
  * Set-up: the first call on each device, with that device current, looks
  * the array up (cudaGetSymbolAddress, which may load the module); make that
  * first call before any stream capture. The array is shared: calls that
@@ -299,10 +337,11 @@ dsa_status dsa_decode_run_noalloc(const dsa_decode_plan_t *plan, const void *q,
                                   void *out, float *lse, int32_t *device_status,
                                   dsa_stream_t stream);
 
-/* Static description of a status code. */
+/* Static description of a status code (no counterpart on the pages). */
 const char *dsa_decode_status_string(dsa_status s);
 
-/* ABI version of this header (bumped on any layout change). */
+/* ABI version of this header (bumped on any layout change; no counterpart
+ * on the pages). */
 int32_t dsa_decode_abi_version(void);
 
 #define DSA_DECODE_ABI_VERSION 3

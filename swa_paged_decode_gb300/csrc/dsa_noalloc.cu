@@ -56,9 +56,14 @@ dsa_status dsa_decode_run_noalloc(const dsa_decode_plan_t *plan, const void *q,
     return DSA_ERR_PLAN;
   // Checked before any CUDA call: plans needing more than the array are refused.
   if (plan->workspace_bytes > (int64_t)DSA_NOALLOC_MAX_WORKSPACE) return DSA_ERR_WORKSPACE;
-  if (plan->num_tokens == 0) return DSA_OK;
   if (device_status && (reinterpret_cast<uintptr_t>(device_status) % 4) != 0)
     return DSA_ERR_ALIGNMENT;
+  if (plan->num_tokens == 0) {   // nothing to launch; the status word still says DSA_OK
+    if (device_status &&
+        cudaMemsetAsync(device_status, 0, 4, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    return DSA_OK;
+  }
   void *ws = nullptr;
   dsa_status s = scratch_for_current_device(&ws);
   if (s != DSA_OK) return s;

@@ -35,6 +35,24 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def test_every_declared_call_cites_its_definition():
+    """Each entry point's comment block (the comment right before its
+    declaration) names the passage of the pages that defines the operation
+    ("Defined by: ...", with a page and an identifier on it), or says that
+    the pages have no counterpart."""
+    src = open(HEADER).read()
+    pages = ("swapab page", "sparse_decode.h page", "production.py page")
+    for name in declared_functions():
+        m = re.search(r"(/\*(?:(?!\*/).)*\*/)\s*[\w\s\*]*?\b" + name + r"\s*\(", src, flags=re.S)
+        assert m, f"{name}: no comment before its declaration"
+        doc = " ".join(m.group(1).split())
+        if "counterpart" in doc:
+            continue
+        assert "Defined by:" in doc, f"{name}: no citation"
+        cited = doc.split("Defined by:", 1)[1]
+        assert any(p in cited for p in pages), f"{name}: citation names no page"
+
+
 def test_abi_version_matches_header(lib):
     m = re.search(r"#define DSA_DECODE_ABI_VERSION (\d+)", open(HEADER).read())
     assert lib.dsa_decode_abi_version() == int(m.group(1))

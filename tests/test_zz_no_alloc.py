@@ -14,7 +14,7 @@ from swa_paged_decode_gb300 import build as BLD
 from swa_paged_decode_gb300 import workloads as W
 
 MAX_BYTES = 48 * 1024 * 1024
-DSA_ERR_WORKSPACE, DSA_ERR_PLAN = -4, -7
+DSA_ERR_INVALID_ARG, DSA_ERR_WORKSPACE, DSA_ERR_PLAN = -1, -4, -7
 
 
 @pytest.fixture(scope="module")
@@ -99,3 +99,35 @@ def test_noalloc_repeated_calls_same_inputs(lib):
         assert status == B.DSA_OK
         assert torch.equal(out.view(torch.int16), ro.view(torch.int16))
         assert torch.equal(lse.view(torch.int32), rl.view(torch.int32))
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_kernel_status_then_clears_it(lib):
+    """A condition the kernel records (a position outside the cos/sin table:
+    DSA_ERR_INVALID_ARG) reaches the caller's status word through the shared
+    scratch, and the next valid call reports DSA_OK again (the word is
+    cleared per call, not left from the last one)."""
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    w = W.make_config(5, T=8, device="cuda")
+    ro, rl, plan = _reference(w)
+    good = w.positions.clone()
+    w.positions[3] = w.cos_sin.shape[0] + 5
+    _, _, status = _noalloc(w, plan)
+    assert status == DSA_ERR_INVALID_ARG
+    w.positions.copy_(good)
+    out, lse, status = _noalloc(w, plan)
+    assert status == B.DSA_OK
+    assert torch.equal(out.view(torch.int16), ro.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), rl.view(torch.int32))
+
+
+@pytest.mark.gpu
+def test_noalloc_zero_tokens_writes_ok_status(lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    plan, _ = B.dsa_decode_plan(0, 64, 128, 0)
+    st = torch.full((1,), -99, dtype=torch.int32, device="cuda")
+    rc = lib.dsa_decode_run_noalloc(ctypes.byref(plan), None, 0, 0, None, None, 0, None, None,
+                                    None, 0, None, None, None, None, 0, 1.0, None, None,
+                                    ctypes.c_void_p(st.data_ptr()), None)
+    torch.cuda.synchronize()
+    assert rc == B.DSA_OK and int(st.item()) == B.DSA_OK
