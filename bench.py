@@ -398,7 +398,10 @@ def gpu_arm(args, rank, world, B, peaks, peak_kind):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if step.dec.plan.kernel == 1 else "fp32",
+        "dtype": "f16" if step.dec.plan.kernel == 1 else "fp32",
+        "dtype_detail": ("tcgen05 kind::f16 MMAs on f16 tiles (fp8 rows normalized per row "
+                         "by a power of two), fp32 accumulate and softmax, bf16 out"
+                         if step.dec.plan.kernel == 1 else "CUDA-core fp32, bf16 out"),
         "data": "synthetic (seeded N(0,1) rows quantized to fp8/NVFP4 records, random slot lists)",
         "config": {"workload": w.name, "T": w.T, "H": w.H,
                    "swa": f"{W.FMT_NAMES[w.swa_cache.fmt]} w{w.swa.width} page "
@@ -423,7 +426,7 @@ def gpu_arm(args, rank, world, B, peaks, peak_kind):
         "gpu_launches": args.steps * (1 + (1 if step.has_combine else 0) + (1 if mx else 0)),
         "clocks": clocks.summary(),
     }
-    return res, w
+    return res, w, step
 
 
 def per_config_table(B, peaks, peak_kind, steps=20, warmup=3):
@@ -453,19 +456,28 @@ def per_config_table(B, peaks, peak_kind, steps=20, warmup=3):
 
 def oracle_run(a, tok, cores: int, mx: bool):
     """The oracle on tokens `tok` (and, for the V4.1 variant, its MXFP8
-    output epilogue on the result)."""
+    output epilogue on the result); returns (out, lse, kept, checksum)."""
     import oracle
-    out = oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
+    res = oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
                         positions=a["positions"], cos_sin=a["cos_sin"],
-                        rope_style=a["rope_style"], tokens=tok, nthreads=cores)[0]
+                        rope_style=a["rope_style"], tokens=tok, nthreads=cores)
     if mx:
         pos = None if a["positions"] is None else a["positions"].cpu().numpy()[tok]
-        oracle.mxfp8_epilogue(out, group_size=MX_GROUP, positions=pos, cos_sin=a["cos_sin"],
+        oracle.mxfp8_epilogue(res[0], group_size=MX_GROUP, positions=pos, cos_sin=a["cos_sin"],
                               rope_style=a["rope_style"])
+    return res
 
 
-def oracle_timing(w: W.Workload, target_s: float, seed: int = 0, mx: bool = False):
-    """Time the fp64 oracle on a bounded token sample of workload w."""
+def oracle_timing(w: W.Workload, target_s: float, seed: int = 0, mx: bool = False,
+                  max_s: float = 90.0):
+    """Time the fp64 oracle on workload w, on every host core and on one.
+
+    All cores: every token of the workload when that fits in ``max_s``
+    seconds (estimated from a first sample of one token per core), else a
+    seeded sample of about ``target_s`` seconds. The oracle's results on
+    these tokens are returned for the parity record. One core: a seeded
+    sample of about target_s / 3 seconds.
+    Returns (cpu_baseline dict, (tokens, oracle out, lse, kept, checksum))."""
     import numpy as np
 
     a = W.oracle_args(w)
@@ -475,17 +487,83 @@ def oracle_timing(w: W.Workload, target_s: float, seed: int = 0, mx: bool = Fals
     tok = np.sort(rng.choice(w.T, size=n, replace=False))
     t0 = time.perf_counter()
     oracle_run(a, tok, cores, mx)
+    per_tok = (time.perf_counter() - t0) / n
+    n2 = w.T if w.T * per_tok <= max_s else int(max(1, min(w.T, target_s / max(per_tok, 1e-9))))
+    tok = np.arange(w.T) if n2 == w.T else np.sort(rng.choice(w.T, size=n2, replace=False))
+    t0 = time.perf_counter()
+    res = oracle_run(a, tok, cores, mx)
     dt = time.perf_counter() - t0
-    per_tok = dt / n
-    n2 = int(max(1, min(w.T, target_s / max(per_tok, 1e-9))))
-    if n2 > n:
-        tok = np.sort(rng.choice(w.T, size=n2, replace=False))
-        t0 = time.perf_counter()
-        oracle_run(a, tok, cores, mx)
-        dt = time.perf_counter() - t0
-        n = n2
-    return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {w.T} tokens of {w.name} (fp64 C oracle, {cores} threads), {dt:.1f} s"}
+    n1 = int(max(1, min(w.T, target_s / 3 / max(per_tok * cores, 1e-9))))
+    tok1 = np.sort(rng.choice(w.T, size=n1, replace=False))
+    t0 = time.perf_counter()
+    oracle_run(a, tok1, 1, mx)
+    dt1 = time.perf_counter() - t0
+    base = {"value": n2 / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n2} of {w.T} tokens of {w.name} (fp64 C oracle, {cores} threads), {dt:.1f} s",
+            "one_core": {"value": n1 / dt1, "unit": UNIT, "cores": 1,
+                         "sample": f"{n1} of {w.T} tokens, 1 thread, {dt1:.1f} s"}}
+    return base, (tok, *res)
+
+
+def parity_record(step: "Step", ref, mx: bool):
+    """GPU output of the timed workload (the buffers of the last timed step;
+    every step decodes the same inputs) against the oracle on the tokens it
+    evaluated, with the decode tolerances: out max |err| <= 2e-2 and
+    per-(token, head) cosine >= 0.9999 against the fp64 oracle, |dlse| <=
+    1e-3, row selection (kept count, checksum) bit-exact. For MXFP8 output
+    each dequantized value must lie within 2e-2 plus half an e4m3 step of
+    the oracle epilogue's input (and its scale byte within 1)."""
+    import numpy as np
+
+    tok, r_out, r_lse, r_kept, r_chk = ref
+    d = step.dec
+    kept, chk = d.selection()
+    if d.lse.is_cuda:
+        torch.cuda.synchronize()
+    ti = torch.as_tensor(tok, device=d.lse.device, dtype=torch.long)
+    lse = d.lse.index_select(0, ti).double().cpu().numpy()
+    k = kept.index_select(0, ti).cpu().numpy()
+    c = chk.index_select(0, ti).cpu().numpy().view(np.uint32)
+    fin = np.isfinite(r_lse)
+    rec = {"tokens_checked": int(len(tok)), "of_tokens": int(step.w.T),
+           "selection_exact": bool(np.array_equal(k, r_kept) and np.array_equal(c, r_chk)),
+           "lse_inf_pattern_exact": bool(np.array_equal(np.isfinite(lse), fin)),
+           "max_abs_dlse": float(np.abs(lse[fin] - r_lse[fin]).max()) if fin.any() else 0.0}
+    if not mx:
+        o = d.out.index_select(0, ti).double().cpu().numpy()
+        rec["max_abs_err"] = float(np.abs(o - r_out).max())
+        rn, on = np.linalg.norm(r_out, axis=-1), np.linalg.norm(o, axis=-1)
+        nz = rn > 0
+        cos = (o * r_out).sum(-1)[nz] / np.maximum(on[nz] * rn[nz], 1e-300)
+        rec["min_cosine"] = float(cos.min()) if cos.size else 1.0
+        rec["zero_rows_exact"] = bool(np.all(o[~nz] == 0))
+        ok_out = rec["max_abs_err"] <= 2e-2 and rec["min_cosine"] >= 0.9999 and rec["zero_rows_exact"]
+    else:
+        import oracle
+        w = step.w
+        G = d.mx.group_size
+        pos = None if w.positions is None else w.positions.cpu().numpy()[tok]
+        _, r_sc, x = oracle.mxfp8_epilogue(r_out, group_size=G, positions=pos,
+                                           cos_sin=None if w.cos_sin is None else w.cos_sin.cpu(),
+                                           rope_style=w.rope_style)
+        table = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+        sc = d.mx.scale_bytes().index_select(0, ti).cpu().numpy().astype(np.int64)
+        got = table[d.mx.data.index_select(0, ti).cpu().numpy()] * \
+            np.repeat(np.ldexp(1.0, sc - 127), 32, axis=-1)
+        n, H = x.shape[:2]
+        want = x.astype(np.float64).reshape(n, H // G, G, 16, 32).transpose(0, 1, 3, 2, 4)
+        want = want.reshape(n, H // G, G * 512)
+        err = np.abs(got - want)
+        rec["max_abs_err"] = float(err.max())
+        rec["mx_values_within_bound"] = bool(np.all(err <= 2e-2 + np.abs(want) * 2.0 ** -4 * 1.001))
+        rec["mx_scale_bytes_within_1"] = bool(np.all(np.abs(sc - r_sc) <= 1))
+        ok_out = rec["mx_values_within_bound"] and rec["mx_scale_bytes_within_1"]
+    rec["pass"] = bool(ok_out and rec["selection_exact"] and rec["lse_inf_pattern_exact"]
+                       and rec["max_abs_dlse"] <= 1e-3)
+    rec["tolerance"] = ("out max|err| <= 2e-2, cosine >= 0.9999, |dlse| <= 1e-3, selection exact"
+                        if not mx else "MXFP8 values within 2e-2 + half an e4m3 step, scale bytes "
+                        "within 1, |dlse| <= 1e-3, selection exact")
+    return rec
 
 
 def reference_arm(args):
@@ -538,12 +616,14 @@ def main():
         dist.barrier()
     B.load()
     peaks, peak_kind = load_peaks()
-    res, w = gpu_arm(args, rank, world, B, peaks, peak_kind)
+    res, w, step = gpu_arm(args, rank, world, B, peaks, peak_kind)
     if rank == 0 and world == 1:
         if args.per_config and args.variant == "base":
             res["per_config"] = per_config_table(B, peaks, peak_kind)
         if args.cpu_baseline:
-            res["cpu_baseline"] = oracle_timing(w, args.cpu_seconds, mx=args.variant == "v41")
+            mx = args.variant == "v41"
+            res["cpu_baseline"], ref = oracle_timing(w, args.cpu_seconds, mx=mx)
+            res["parity"] = parity_record(step, ref, mx)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()

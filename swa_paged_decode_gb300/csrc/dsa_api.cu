@@ -11,6 +11,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "dsa_internal.cuh"
 
 using dsa::Params;
@@ -34,6 +36,13 @@ cudaError_t dsa::dsa_configure_once(int bit, cudaError_t (*f)(void *), void *arg
 }
 
 namespace {
+
+// NVTX range over one entry point (host side: argument checks and launches),
+// so a profiler timeline shows each run / combine call.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 constexpr int64_t kAlignWs = 256;
 constexpr int64_t kStatusBytes = 256;
@@ -336,6 +345,7 @@ dsa_status dsa_decode_run(const dsa_decode_plan_t *plan, void *workspace,
                           const int64_t *positions, const float *cos_sin,
                           int64_t cos_sin_rows, float scale, void *out, float *lse,
                           dsa_stream_t stream) {
+  NvtxRange range("dsa_decode_run");
   if (!out) return plan_ok(plan) ? (plan->num_tokens == 0 ? DSA_OK : DSA_ERR_INVALID_ARG)
                                  : DSA_ERR_PLAN;
   return run_impl(plan, workspace, workspace_bytes, q, q_stride_t, q_stride_h, swa_cache,
@@ -355,6 +365,7 @@ dsa_status dsa_decode_run_v41(const dsa_decode_plan_t *plan, void *workspace,
                               int64_t cos_sin_rows, int32_t rope_style, float scale,
                               void *out, const dsa_mxfp8_out *mx, float *lse,
                               dsa_stream_t stream) {
+  NvtxRange range("dsa_decode_run_v41");
   return run_impl(plan, workspace, workspace_bytes, q, q_stride_t, q_stride_h, swa_cache,
                   swa_idx, swa_idx_stride, swa_lens, extra_cache, extra_idx, extra_idx_stride,
                   extra_lens, sink, positions, cos_sin, cos_sin_rows, rope_style, scale, out, mx,
@@ -364,6 +375,7 @@ dsa_status dsa_decode_run_v41(const dsa_decode_plan_t *plan, void *workspace,
 dsa_status dsa_decode_combine(const dsa_decode_plan_t *plan, void *workspace,
                               size_t workspace_bytes, const float *sink, void *out,
                               float *lse, dsa_stream_t stream) {
+  NvtxRange range("dsa_decode_combine");
   if (!plan_ok(plan)) return DSA_ERR_PLAN;
   if (plan->num_tokens == 0 || plan->ctas_per_group <= 1) return DSA_OK;
   if (!out) return DSA_ERR_INVALID_ARG;
@@ -376,6 +388,7 @@ dsa_status dsa_decode_combine_v41(const dsa_decode_plan_t *plan, void *workspace
                                   const int64_t *positions, const float *cos_sin,
                                   int64_t cos_sin_rows, int32_t rope_style, void *out,
                                   const dsa_mxfp8_out *mx, float *lse, dsa_stream_t stream) {
+  NvtxRange range("dsa_decode_combine_v41");
   return combine_impl(plan, workspace, workspace_bytes, sink, positions, cos_sin, cos_sin_rows,
                       rope_style, out, mx, lse, stream);
 }

@@ -55,3 +55,45 @@ def test_v41_form_draws_the_same_inputs():
         assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
                            y.view(torch.int16) if y.dtype == torch.bfloat16 else y)
     assert a.swa_cache.data.shape == b.swa_cache.data.shape
+
+
+class _FakeDec:
+    """CPU stand-in for the decoder buffers the parity record reads."""
+
+    def __init__(self, out, lse, kept, chk):
+        self.out, self.lse, self._k, self._c = out, lse, kept, chk
+
+    def selection(self):
+        return self._k, self._c
+
+
+class _FakeStep:
+    def __init__(self, w, dec):
+        self.w, self.dec = w, dec
+
+
+def test_parity_record_passes_on_oracle_output_and_catches_errors():
+    import numpy as np
+
+    import oracle
+    w = tiny()
+    a = W.oracle_args(w)
+    res = oracle.decode(a["q"], a["caches"], a["lists"], scale=a["scale"], sink=a["sink"],
+                        positions=a["positions"], cos_sin=a["cos_sin"], rope_style=a["rope_style"])
+    tok = np.arange(w.T)
+    ref = (tok, *res)
+    out = torch.from_numpy(res[0]).to(torch.bfloat16)
+    lse = torch.from_numpy(res[1]).float()
+    kept = torch.from_numpy(res[2])
+    chk = torch.from_numpy(res[3].view(np.int32))
+    rec = bench.parity_record(_FakeStep(w, _FakeDec(out, lse, kept, chk)), ref, mx=False)
+    assert rec["pass"] and rec["tokens_checked"] == w.T and rec["selection_exact"]
+    bad = out.clone()
+    bad[1, 2, 7] += 0.05                       # one element past the 2e-2 bound
+    assert not bench.parity_record(_FakeStep(w, _FakeDec(bad, lse, kept, chk)), ref, False)["pass"]
+    kb = kept.clone()
+    kb[0] += 1                                 # selection off by one row
+    assert not bench.parity_record(_FakeStep(w, _FakeDec(out, lse, kb, chk)), ref, False)["pass"]
+    lb = lse.clone()
+    lb[2, 0] += 2e-3
+    assert not bench.parity_record(_FakeStep(w, _FakeDec(out, lb, kept, chk)), ref, False)["pass"]
