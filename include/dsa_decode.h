@@ -136,7 +136,13 @@ typedef struct {
   int64_t ws_stage_offset;  /* fp32 [T][H][512] staging of the MXFP8 output */
   int64_t workspace_bytes_mx; /* workspace an MXFP8-output call needs
                               (dsa_decode_run_v41 / combine_v41 with mx)     */
-  int64_t reserved[12];
+  int64_t wait_budget_cycles; /* SM clock cycles a device wait may take before
+                              the kernel gives up (DSA_ERR_TIMEOUT); 0 = the
+                              default of about 2 s. Set only from the
+                              DSA_DECODE_WAIT_BUDGET environment variable at
+                              planning time, so tests can make a wait run
+                              out on purpose                                 */
+  int64_t reserved[11];
 } dsa_decode_plan_t;
 
 /* Plan one decode call.

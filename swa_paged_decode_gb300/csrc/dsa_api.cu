@@ -110,6 +110,7 @@ void fill_schedule(const dsa_decode_plan_t *plan, void *ws, Params &p) {
   p.part_o = reinterpret_cast<float *>(w + plan->ws_part_o_offset);
   p.bounds = reinterpret_cast<int64_t *>(w + plan->ws_bounds_offset);
   p.balance = (int32_t)plan->balance_live;
+  p.wait_budget = plan->wait_budget_cycles > 0 ? (long long)plan->wait_budget_cycles : 0;
 }
 
 dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
@@ -345,6 +346,12 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   plan->ws_stage_offset = off;
   plan->workspace_bytes_mx =
       num_tokens == 0 ? 0 : off + 4 * (int64_t)num_tokens * num_heads * dsa::kD;
+  // Test knob, read only here: a shorter budget for every bounded device wait
+  // (a wait that runs out sets DSA_ERR_TIMEOUT in the status word).
+  if (const char *wb = std::getenv("DSA_DECODE_WAIT_BUDGET")) {
+    const long long v = std::atoll(wb);
+    if (v > 0) plan->wait_budget_cycles = v;
+  }
   *workspace_bytes = (size_t)plan->workspace_bytes;
   return DSA_OK;
 }

@@ -69,6 +69,7 @@ struct Params {
   // workspace
   int64_t *bounds;             // [C+1]: CTA c owns units [bounds[c], bounds[c+1])
   int32_t balance;             // 1: live-tile balanced ranges, 0: c*upc
+  long long wait_budget;       // SM cycles per bounded device wait (0: the kernel's default)
   int32_t *status;             // device status word
   int32_t *sel;                // [T][2]: kept rows, checksum
   float *part_lse;             // [HG][2C][hpg]
@@ -277,8 +278,8 @@ __device__ inline float e2m1_to_f32(uint32_t nib) {
 // One-time per-device kernel set-up (function attributes): `f` runs on the
 // first launch of kernel variant `bit` on the current device, later launches
 // skip it (they may be captured into a CUDA graph, where no set-up call is
-// wanted). Thread-safe. Bits in use: tensor-core kernels 0-2 (plain) and
-// 20-22 (V4.1 options), SIMT kernels 8-11, combine 16.
+// wanted). Thread-safe. Bits in use: tensor-core kernels 0-2 (plain), 20-22
+// (V4.1 options) and 24-26 (exact-budget waits), SIMT kernels 8-11, combine 16.
 cudaError_t dsa_configure_once(int bit, cudaError_t (*f)(void *), void *arg);
 
 // Programmatic dependent launch: the decode kernels let the combine grid be

@@ -103,7 +103,8 @@ enum Bar : int {
   kBarKvFree = 1,   // [4] MMA commit -> producers: 128-dim block no longer read
   kBarSFull = 5,    // MMA commit -> softmax: S ready (and every earlier MMA done)
   kBarOFinal = 6,   // MMA commit -> softmax: last PV of a token done
-  kNumBars = 7
+  kBarDrain = 7,    // MMA commit -> issuer: every MMA issued so far done (abort path)
+  kNumBars = 8
 };
 constexpr uint32_t kMiscAbort = 8 * kNumBars;        // int32
 constexpr uint32_t kMiscTmem = kMiscAbort + 4;       // uint32
@@ -385,7 +386,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 
 // kExt: the V4.1 options (fp8 records with ue8m0 scales, GPT-J RoPE, MXFP8
 // output); the plain instantiation compiles none of their code.
-template <int HPG, bool kExt>
+// kStrict: the plan carries a wait budget (a test knob); only that
+// instantiation compiles the exact-budget waits.
+template <int HPG, bool kExt, bool kStrict>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   using Cfg = TcCfg<HPG>;
   constexpr int NH = Cfg::kHalf;
@@ -438,9 +441,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   // Bounded wait on a barrier phase. After any timeout (here or in another
   // warp) it returns at once; callers keep their control flow unchanged.
   // Waits off the MMA-issue path sleep between polls; the issuing warp spins.
+  // A budget from the plan (a test knob, kStrict) is kept exactly: its polls
+  // do not suspend (try_wait may suspend the thread for longer than a short
+  // budget).
   auto wait = [&](int b, uint32_t &phase) {
     if (!*abort_s) {
-      const bool done = tc::mbar_wait(&bars[b], phase, kWaitBudget, warp == 0 ? 0u : 2000u);
+      bool done;
+      if constexpr (kStrict)
+        done = tc::mbar_wait_strict(&bars[b], phase, p.wait_budget);
+      else
+        done = tc::mbar_wait(&bars[b], phase, kWaitBudget, warp == 0 ? 0u : 2000u);
       if (!done && !*abort_s) {
         *abort_s = 1;
         report_status(p.status, DSA_ERR_TIMEOUT);
@@ -946,6 +956,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     if (cur_t >= 0) finalize(seg);
   }
 
+  // After a wait gave up, MMAs issued before it may still be running: the
+  // issuer commits once more and waits (with the full default budget, MMAs
+  // always finish) until every one of them is done, so TMEM is never freed
+  // under a running MMA.
+  if (tid == 0 && *abort_s) {
+    tc::mma_commit(&bars[kBarDrain]);
+    tc::mbar_wait(&bars[kBarDrain], 0u, kWaitBudget);
+  }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -961,15 +979,15 @@ bool dsa_tc_supports(int hpg) { return hpg == 16 || hpg == 32 || hpg == 64; }
 namespace {
 // Checks that the kernel kept exactly kLaunchRegs registers per thread (the
 // warpgroup register split assumes it) and raises its shared-memory limit.
-template <int N, bool E>
+template <int N, bool E, bool S>
 cudaError_t tc_setup(void *) {
   using namespace dsa;
   cudaFuncAttributes fa;
-  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E>);
+  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E, S>);
   if (err != cudaSuccess) return err;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(tc_decode_kernel<N, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)TcCfg<N>::kSmem);
+  return cudaFuncSetAttribute(tc_decode_kernel<N, E, S>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<N>::kSmem);
 }
 }  // namespace
 
@@ -978,19 +996,25 @@ cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
   const dim3 grid((unsigned)(p.C * p.HG)), block(kTcThreads);
   const bool ext = p.rope_gptj || p.mx_on || p.list[0].fmt == DSA_REC_FP8_528_UE8M0 ||
                    (p.nlists > 1 && p.list[1].fmt == DSA_REC_FP8_528_UE8M0);
+  // exact-budget waits (a plan with a wait budget) exist for the plain form
+  const bool strict = !ext && p.wait_budget > 0;
   cudaError_t err = cudaSuccess;
   switch (p.hpg) {
 #define DSA_TC_CASE(N, BIT)                                                              \
   case N: {                                                                              \
     const int smem = (int)TcCfg<N>::kSmem;                                               \
     if (ext) {                                                                           \
-      err = dsa_configure_once(BIT + 20, &tc_setup<N, true>, nullptr);                   \
+      err = dsa_configure_once(BIT + 20, &tc_setup<N, true, false>, nullptr);            \
       if (err != cudaSuccess) return err;                                                \
-      tc_decode_kernel<N, true><<<grid, block, smem, stream>>>(p);                       \
+      tc_decode_kernel<N, true, false><<<grid, block, smem, stream>>>(p);                \
+    } else if (strict) {                                                                 \
+      err = dsa_configure_once(BIT + 24, &tc_setup<N, false, true>, nullptr);            \
+      if (err != cudaSuccess) return err;                                                \
+      tc_decode_kernel<N, false, true><<<grid, block, smem, stream>>>(p);                \
     } else {                                                                             \
-      err = dsa_configure_once(BIT, &tc_setup<N, false>, nullptr);                       \
+      err = dsa_configure_once(BIT, &tc_setup<N, false, false>, nullptr);                \
       if (err != cudaSuccess) return err;                                                \
-      tc_decode_kernel<N, false><<<grid, block, smem, stream>>>(p);                      \
+      tc_decode_kernel<N, false, false><<<grid, block, smem, stream>>>(p);               \
     }                                                                                    \
     break;                                                                               \
   }

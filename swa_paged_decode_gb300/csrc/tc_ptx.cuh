@@ -31,6 +31,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of a phase (mbarrier.try_wait may suspend the thread
+// until the phase completes or a hardware time limit passes; test_wait
+// returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait whose budget is exact in SM cycles: polls without suspending.
+__device__ __forceinline__ bool mbar_wait_strict(uint64_t *bar, uint32_t parity, long long budget) {
+  const long long t0 = clock64();
+  while (!mbar_test_wait(bar, parity))
+    if (clock64() - t0 > budget) return false;
+  return true;
+}
 // try_wait that lets the thread sleep (up to `ns` nanoseconds, woken early
 // when the phase completes) instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
