@@ -31,7 +31,8 @@ _lib = None
 FMT_FP8_528 = 0
 FMT_NVFP4_288 = 1
 FMT_FP8_528_UE8M0 = 2
-RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288, FMT_FP8_528_UE8M0: 528}
+FMT_MODEL1_584 = 3
+RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288, FMT_FP8_528_UE8M0: 528, FMT_MODEL1_584: 584}
 ROPE_NEOX = 0
 ROPE_GPTJ = 1
 

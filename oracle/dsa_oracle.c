@@ -31,6 +31,15 @@
  *      meaning 2^(b-127); the NVFP4 record holds 256 bytes of e2m1 nibbles
  *      then 32 e4m3 scales, one per 16 dims, element 2i in the low nibble of
  *      byte i and 2i+1 in the high one). k[d] = code(d) * scale(d).
+ *      The MODEL1 record of FlashMLA's sparse_decode.h page (the check
+ *      bytes_per_token = 448 + 64*2 + (448/64)*1 + 1 for d_qk = d_v = 512;
+ *      the page gives only these byte counts, read here in the order they
+ *      are summed): bytes 0..447 are the e4m3 codes of dims 0..447, bytes
+ *      448..575 dims 448..511 as little-endian bf16 values, bytes 576..582
+ *      one ue8m0 scale byte per 64 fp8 dims (dim d takes byte 576 + d/64,
+ *      meaning 2^(b-127)), byte 583 unused: k[d] = e4m3(byte d) *
+ *      2^(byte[576 + d/64] - 127) for d < 448, k[d] = bf16 value for
+ *      d >= 448.
  *   4. Q.  q = bf16 value of q[t, h, :] in fp64. With RoPE on, the last 64
  *      dims are rotated by the fp32 table row cos_sin[positions[t]] =
  *      [cos(32) | sin(32)], pair i taking c = cos[i], s = sin[i]:
@@ -66,7 +75,12 @@
 #define ORACLE_ROPE_START 448
 #define ORACLE_ROPE_HALF 32
 
-enum { ORACLE_FMT_FP8_528 = 0, ORACLE_FMT_NVFP4_288 = 1, ORACLE_FMT_FP8_528_UE8M0 = 2 };
+enum {
+  ORACLE_FMT_FP8_528 = 0,
+  ORACLE_FMT_NVFP4_288 = 1,
+  ORACLE_FMT_FP8_528_UE8M0 = 2,
+  ORACLE_FMT_MODEL1_584 = 3
+};
 enum { ORACLE_ROPE_NEOX = 0, ORACLE_ROPE_GPTJ = 1 };
 
 typedef struct {
@@ -133,7 +147,8 @@ static double bf16_value(uint16_t u) {
 }
 
 static int record_bytes(int32_t format) {
-  return format == ORACLE_FMT_NVFP4_288 ? 288 : 528;
+  if (format == ORACLE_FMT_NVFP4_288) return 288;
+  return format == ORACLE_FMT_MODEL1_584 ? 584 : 528;
 }
 
 /* Step 3: one record -> 512 fp64 values. */
@@ -144,6 +159,13 @@ void oracle_dequant_record(const uint8_t *rec, int32_t format, double *k) {
   } else if (format == ORACLE_FMT_FP8_528_UE8M0) {
     for (int d = 0; d < ORACLE_D; ++d)
       k[d] = oracle_e4m3_value(rec[d]) * oracle_ue8m0_value(rec[512 + d / 32]);
+  } else if (format == ORACLE_FMT_MODEL1_584) {
+    for (int d = 0; d < 448; ++d)
+      k[d] = oracle_e4m3_value(rec[d]) * oracle_ue8m0_value(rec[576 + d / 64]);
+    for (int d = 448; d < ORACLE_D; ++d) {
+      const uint8_t *b = rec + 448 + 2 * (d - 448);
+      k[d] = bf16_value((uint16_t)(b[0] | (b[1] << 8)));
+    }
   } else {
     for (int d = 0; d < ORACLE_D; ++d) {
       uint8_t byte = rec[d / 2];

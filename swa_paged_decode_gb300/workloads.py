@@ -20,6 +20,11 @@ workloads of this method):
     absmax / 448)) (the page's rule for its MXFP8 output, taken for the cache
     too), byte = exponent + 127, code = e4m3 round-to-nearest-even of
     x / scale.
+  * MODEL1-584 (FlashMLA's sparse_decode.h page gives the byte counts
+    448 + 64*2 + 448/64 + 1 for d_qk = d_v = 512; read in that order): the
+    e4m3 codes of dims 0..447 with one ue8m0 scale per 64 dims (same rule as
+    above, per 64 dims), dims 448..511 (the RoPE part) as little-endian bf16
+    (round to nearest even), the 7 scale bytes, one zero pad byte.
 
 The five named workloads follow the configurations the method is measured on
 (T tokens, H query heads, one shared 512-dim KV row per slot). Seeds: workload
@@ -38,9 +43,11 @@ HEAD_DIM = 512
 FMT_FP8_528 = 0
 FMT_NVFP4_288 = 1
 FMT_FP8_528_UE8M0 = 2
-RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288, FMT_FP8_528_UE8M0: 528}
+FMT_MODEL1_584 = 3
+RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288, FMT_FP8_528_UE8M0: 528,
+                FMT_MODEL1_584: 584}
 FMT_NAMES = {FMT_FP8_528: "fp8_528", FMT_NVFP4_288: "nvfp4_288",
-             FMT_FP8_528_UE8M0: "fp8_528_ue8m0"}
+             FMT_FP8_528_UE8M0: "fp8_528_ue8m0", FMT_MODEL1_584: "model1_584"}
 ROPE_NEOX = 0   # dim 448+i pairs with 480+i
 ROPE_GPTJ = 1   # dim 448+2i pairs with 449+2i
 ROPE_TABLE_ROWS = 131072
@@ -140,6 +147,21 @@ def encode_fp8_ue8m0_records(x: torch.Tensor) -> torch.Tensor:
     return torch.cat([codes, sbytes], dim=1)
 
 
+def encode_model1_records(x: torch.Tensor) -> torch.Tensor:
+    """[n, 512] float -> [n, 584] uint8 MODEL1 records."""
+    n = x.shape[0]
+    xb = x[:, :448].float().reshape(n, 7, 64)
+    amax = xb.abs().amax(dim=-1).double()                       # [n, 7]
+    ex = torch.where(amax > 0, torch.ceil(torch.log2(amax / 448.0)), torch.zeros_like(amax))
+    ex = ex.clamp(-127, 127)
+    y = (xb.double() / torch.exp2(ex)[..., None]).clamp(-448.0, 448.0).float()
+    codes = y.to(torch.float8_e4m3fn).view(torch.uint8).reshape(n, 448)
+    rope = x[:, 448:].float().to(torch.bfloat16).contiguous().view(torch.uint8).reshape(n, 128)
+    sbytes = (ex + 127).to(torch.uint8)
+    pad = torch.zeros((n, 1), dtype=torch.uint8, device=x.device)
+    return torch.cat([codes, rope, sbytes, pad], dim=1)
+
+
 def _e2m1_codes(y: torch.Tensor) -> torch.Tensor:
     """Round-to-nearest-even onto e2m1 magnitudes {0,.5,1,1.5,2,3,4,6}, saturating
     at 6; returns 4-bit codes (sign in bit 3) as uint8."""
@@ -179,7 +201,8 @@ def make_cache(num_slots: int, page_size: int, fmt: int, gen: torch.Generator,
     data = torch.zeros((num_pages, stride), dtype=torch.uint8, device=device)
     recs = data[:, :page_size * rb].view(num_pages, page_size, rb)
     enc = {FMT_FP8_528: encode_fp8_records, FMT_NVFP4_288: encode_nvfp4_records,
-           FMT_FP8_528_UE8M0: encode_fp8_ue8m0_records}[fmt]
+           FMT_FP8_528_UE8M0: encode_fp8_ue8m0_records,
+           FMT_MODEL1_584: encode_model1_records}[fmt]
     chunk = max(page_size, chunk - chunk % page_size)
     for s0 in range(0, num_slots, chunk):
         s1 = min(num_slots, s0 + chunk)          # both multiples of page_size
