@@ -64,19 +64,28 @@ typedef enum {
  *            dims); value = code * 2^(byte - 127) (the V4.1 record of the
  *            swapab page, stage_inputs fp8 branch). A scale byte of 0xFF
  *            (NaN in E8M0) gives non-finite values.
+ * MODEL1_584: FlashMLA's MODEL1 record (sparse_decode.h page: bytes_per_token
+ *            = 448 + 64*2 + (448/64)*1 + 1 for d_qk = d_v = 512; the page
+ *            gives only the byte counts, read in the order they are summed):
+ *            the e4m3 codes of dims 0..447, dims 448..511 (the RoPE part)
+ *            as 64 little-endian bf16 values, 7 ue8m0 scale bytes (dim
+ *            d < 448 takes byte 576 + d/64), 1 unused byte. Records are
+ *            8-byte aligned within a page (584 = 8 * 73).
  * Precision of the tensor-core kernels: every row is written to an f16 tile
  * as value * 2^-e, e the exponent of the row's largest block scale (clamped
  * to [-48, 48]), and 2^e is applied again in fp32 after the products, so a
- * row's magnitude does not matter. NVFP4 and FP8_528_UE8M0 values are then
- * exact (UE8M0: blocks within 2^15 of the row's largest scale, and block
- * exponents in [-63, 55]; smaller blocks are rounded, relative to the row's
- * largest, below 2^-24); FP8_528 values are code * (scale * 2^-e rounded to
- * f16), rounded to f16 (relative error <= 2^-11 for blocks within 2^14 of
- * the row's largest scale; scales up to 2^55).
+ * row's magnitude does not matter. NVFP4, FP8_528_UE8M0 and MODEL1_584
+ * values are then exact (ue8m0 blocks within 2^15 of the row's largest
+ * scale, and block exponents in [-63, 55]; smaller blocks are rounded,
+ * relative to the row's largest, below 2^-24; MODEL1's bf16 part is exact
+ * down to 2^-26 of the row's largest value, e taking that part into
+ * account); FP8_528 values are code * (scale * 2^-e rounded to f16),
+ * rounded to f16 (relative error <= 2^-11 for blocks within 2^14 of the
+ * row's largest scale; scales up to 2^55).
  * Source: the swapab page (record sizes 528 and 288, NVFP4 block of 16 with
  * e4m3 scales) with the fp32-per-128 scale layout of FlashMLA's V3.2 record
  * (sparse_decode.h, bytes_per_token = 512 + ... + (512/128)*4).            */
-enum { DSA_REC_FP8_528 = 0, DSA_REC_NVFP4_288 = 1, DSA_REC_FP8_528_UE8M0 = 2 };
+enum { DSA_REC_FP8_528 = 0, DSA_REC_NVFP4_288 = 1, DSA_REC_FP8_528_UE8M0 = 2, DSA_REC_MODEL1_584 = 3 };
 
 /* RoPE pairings of q dims 448..511 with a table row [cos(32) | sin(32)]:
  * NEOX pairs dim 448+i with 480+i, GPTJ pairs 448+2i with 449+2i (the swapab

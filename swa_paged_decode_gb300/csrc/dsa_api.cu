@@ -52,6 +52,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 bool pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 int record_bytes(int32_t fmt) {
   if (fmt == DSA_REC_FP8_528 || fmt == DSA_REC_FP8_528_UE8M0) return 528;
+  if (fmt == DSA_REC_MODEL1_584) return 584;
   return fmt == DSA_REC_NVFP4_288 ? 288 : -1;
 }
 

@@ -41,6 +41,27 @@ __device__ void load_subtile(const Params &p, SimtSmem &sm, int32_t lid, int32_t
   float *krow = sm.k + i * kD;
   if (!ok) {
     for (int d = j; d < kD; d += 8) krow[d] = 0.f;
+  } else if (L.fmt == DSA_REC_MODEL1_584) {   // 8-byte aligned records: 8-byte loads
+    const uint8_t *rec = record_ptr(L, sid);
+    const uint2 sc = __ldg(reinterpret_cast<const uint2 *>(rec + 576));   // 7 ue8m0 + 1 unused
+#pragma unroll
+    for (int kk = 0; kk < 7; ++kk) {
+      const int w = j + 8 * kk;   // 8-byte word = dims [8w, 8w+8), in 64-dim block kk
+      const uint2 v = __ldg(reinterpret_cast<const uint2 *>(rec) + w);
+      const float s = ue8m0_to_f32((kk < 4 ? sc.x : sc.y) >> (8 * (kk & 3)));
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        krow[8 * w + e] = e4m3_to_f32(((e < 4 ? v.x : v.y) >> (8 * (e & 3))) & 0xFFu) * s;
+    }
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const int w = j + 8 * kk;   // bf16 dims 448 + [4w, 4w+4)
+      const uint2 v = __ldg(reinterpret_cast<const uint2 *>(rec + 448) + w);
+      krow[448 + 4 * w + 0] = bf16_bits_to_f32(v.x & 0xFFFFu);
+      krow[448 + 4 * w + 1] = bf16_bits_to_f32(v.x >> 16);
+      krow[448 + 4 * w + 2] = bf16_bits_to_f32(v.y & 0xFFFFu);
+      krow[448 + 4 * w + 3] = bf16_bits_to_f32(v.y >> 16);
+    }
   } else if (L.fmt != DSA_REC_NVFP4_288) {   // fp8: fp32 scales per 128 or ue8m0 per 32 dims
     const uint8_t *rec = record_ptr(L, sid);
     const bool ue = L.fmt == DSA_REC_FP8_528_UE8M0;

@@ -214,14 +214,19 @@ __device__ __forceinline__ int row_exp(uint32_t field) {
 // the record (sector s holds chunks 2s-1 and 2s); lane j = 0 also holds
 // sector 16 (chunk 31 and the scales) in d[16], d[17]. The two lanes of a
 // row rebuild their pairs with one shuffle per pair (dequant_block).
+// MODEL1 records (kExt): d[2m], d[2m+1] = chunks 4m+2j, 4m+2j+1 of the fp8
+// dims (k-blocks m = 0..6), d[14..17] = chunks 28+4j .. 31+4j (this lane's
+// 32 bf16 dims 448+32j ..), sc8 = the 7 scale bytes and the unused byte.
 struct Gather {
   uint4 d[18];
+  uint2 sc8;
   int32_t sid;
   int32_t r;
   bool ok;
   bool pl;
 };
 
+template <bool kExt>
 __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, int32_t sid, int row,
                                             int j, Gather &g) {
   int32_t lid, row0;
@@ -232,6 +237,29 @@ __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, in
   g.ok = slot_valid(L, g.r, lid == 0 ? c.lim0 : c.lim1, sid);
   const uint4 z = make_uint4(0, 0, 0, 0);
   g.pl = true;
+  if (kExt && L.fmt == DSA_REC_MODEL1_584) {   // 584-byte records, 8-byte aligned
+    if (g.ok) {
+      const uint8_t *rec = record_ptr(L, sid);
+      auto chunk = [&](int c) -> uint4 {
+        if ((reinterpret_cast<uintptr_t>(rec) & 15u) == 0) return tc::ldg_nc_v4(rec + 16 * c);
+        const uint2 a = tc::ldg_nc_v2(rec + 16 * c), b = tc::ldg_nc_v2(rec + 16 * c + 8);
+        return make_uint4(a.x, a.y, b.x, b.y);
+      };
+#pragma unroll
+      for (int m = 0; m < 7; ++m) {
+        g.d[2 * m] = chunk(4 * m + 2 * j);
+        g.d[2 * m + 1] = chunk(4 * m + 2 * j + 1);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) g.d[14 + q] = chunk(28 + 4 * j + q);
+      g.sc8 = tc::ldg_nc_v2(rec + 576);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 18; ++k) g.d[k] = z;
+      g.sc8 = make_uint2(0, 0);
+    }
+    return;
+  }
   if (L.fmt != DSA_REC_NVFP4_288) {   // both 528-byte fp8 records
     if (g.ok) {
       const uint8_t *rec = record_ptr(L, sid);
@@ -364,6 +392,48 @@ __device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g
   }
 }
 
+// MODEL1 rows (kExt): M block mb = k-blocks 2mb, 2mb+1. k-blocks 0..6 hold
+// e4m3 codes times ue8m0 byte m of sc8 (one per 64 dims), k-block 7 the bf16
+// RoPE dims; every value times the row's 2^-e (rnorm), as f16.
+__device__ __forceinline__ void dequant_block_model1(const Gather &g, float rnorm, int mb, int row,
+                                                     int j, uint32_t kv_base) {
+#pragma unroll
+  for (int mm = 0; mm < 2; ++mm) {
+    const int m = 2 * mb + mm;
+    if (m < 7) {
+      const uint32_t sb = (m < 4 ? g.sc8.x : g.sc8.y) >> (8 * (m & 3));
+      const uint32_t sc = scale_f16x2(ue8m0_to_f32(sb) * rnorm);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint4 src = g.d[2 * m + e];
+        const uint32_t w[4] = {src.x, src.y, src.z, src.w};
+        uint32_t f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          tc::e4m3x4_to_f16x4(w[i], f[2 * i], f[2 * i + 1]);
+          f[2 * i] = tc::hmul2(f[2 * i], sc);
+          f[2 * i + 1] = tc::hmul2(f[2 * i + 1], sc);
+        }
+        const int ci = 4 * j + 2 * e;   // dims 64m + 32j + 16e .. +16
+        tc::st_shared_v4(kv_base + sw128_off(row, m, ci, 16384), f[0], f[1], f[2], f[3]);
+        tc::st_shared_v4(kv_base + sw128_off(row, m, ci + 1, 16384), f[4], f[5], f[6], f[7]);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {   // dims 448 + 32j + 8q .. +8
+        const uint4 src = g.d[14 + q];
+        const uint32_t w[4] = {src.x, src.y, src.z, src.w};
+        uint32_t f[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          f[i] = tc::pack_f16x2(bf16_bits_to_f32(w[i] & 0xFFFFu) * rnorm,
+                                bf16_bits_to_f32(w[i] >> 16) * rnorm);
+        tc::st_shared_v4(kv_base + sw128_off(row, 7, 4 * j + q, 16384), f[0], f[1], f[2], f[3]);
+      }
+    }
+  }
+}
+
 // Named barrier 1 among the 256 softmax threads (optionally OR-reducing).
 __device__ __forceinline__ int sm_bar_or(int pred) {
   int r;
@@ -478,8 +548,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       int32_t lid2, row02;
       cursor_tile(p, c, lid2, row02);
       const ListArgs &L = p.list[lid2];
-      if (slot_valid(L, row02 + row, lid2 == 0 ? c.lim0 : c.lim1, sid))
-        tc::prefetch_l2_bulk(record_ptr(L, sid), (uint32_t)L.rec);
+      if (slot_valid(L, row02 + row, lid2 == 0 ? c.lim0 : c.lim1, sid)) {
+        const uint8_t *rec = record_ptr(L, sid);
+        if (kExt && L.fmt == DSA_REC_MODEL1_584) {   // 16-byte aligned span around the record
+          const uintptr_t a0 = reinterpret_cast<uintptr_t>(rec) & ~(uintptr_t)15;
+          const uintptr_t a1 = (reinterpret_cast<uintptr_t>(rec) + 584 + 15) & ~(uintptr_t)15;
+          tc::prefetch_l2_bulk(reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0));
+        } else {
+          tc::prefetch_l2_bulk(rec, (uint32_t)L.rec);
+        }
+      }
     };
     Cursor cu = cursor_at(p, u0);       // tile being dequantized
     cursor_first_live(p, cu, u1);
@@ -491,7 +569,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const int32_t sid0 = load_sid(p, cu, row);
       prefetch(cu, sid0);
       prefetch(cn, sid_n1);
-      issue_loads(p, cu, sid0, row, j, g);
+      issue_loads<kExt>(p, cu, sid0, row, j, g);
     }
     while (cu.u < u1) {
       const int32_t t = cu.t;
@@ -502,7 +580,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const int32_t sid_n2 = cn2.u < u1 ? load_sid(p, cn2, row) : -1;
       const int32_t sid_next = sid_n1;
       const bool last_of_token = cn.u >= u1 || cn.t != t;
-      const bool fp8 = p.list[lid].fmt != DSA_REC_NVFP4_288;
+      const bool m1 = kExt && p.list[lid].fmt == DSA_REC_MODEL1_584;
+      const bool fp8 = !m1 && p.list[lid].fmt != DSA_REC_NVFP4_288;
       const bool ue = kExt && p.list[lid].fmt == DSA_REC_FP8_528_UE8M0;
       uint32_t scale2[4] = {0, 0, 0, 0};
       // Row exponent e (fp8 rows): the tile holds k * 2^-e, so the row's
@@ -530,6 +609,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           for (int b = 0; b < 4; ++b) scale2[b] = scale_f16x2(__uint_as_float(scale2[b]) * rn);
         }
       }
+      if (m1) {
+        // e from the largest scale byte and from the bf16 part's largest
+        // magnitude (its exponent field minus 8), so the f16 values stay
+        // below 2^9 either way
+        uint32_t mx = __vmaxu4(g.sc8.x, g.sc8.y & 0x00FFFFFFu);
+        mx = max(max(mx & 0xFFu, (mx >> 8) & 0xFFu), max((mx >> 16) & 0xFFu, mx >> 24));
+        uint32_t bm = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = g.d[14 + q];
+          bm = __vmaxu2(bm, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                     __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+        }
+        bm = max(bm & 0xFFFFu, bm >> 16);
+        bm = max(bm, (uint32_t)__shfl_xor_sync(0xffffffffu, bm, 1));   // the row's other half
+        const int eb = (int)(bm >> 7) - 8;   // bf16 exponent field - 8 (biased)
+        erow = row_exp(max((int)mx, eb));
+      }
       const float rnorm = pow2i(-erow);
       if (j == 0 && g.ok) {
         kept += 1;
@@ -554,7 +651,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       for (int mb = 0; mb < 4; ++mb) {
         if (!first) wait(kBarKvFree + mb, ph_free[mb]);
         if (mb == 0 && j == 0) row_e_s[row] = g.ok ? erow : kRowInvalid;
-        dequant_block(fp8, ue, g, scale2, rnorm, mb, row, j, kv_base);
+        if (m1)
+          dequant_block_model1(g, rnorm, mb, row, j, kv_base);
+        else
+          dequant_block(fp8, ue, g, scale2, rnorm, mb, row, j, kv_base);
       }
       // One hand-off per tile: the QK MMAs are issued once the whole tile is
       // in place, so per-block fences and arrives would only lengthen the
@@ -568,7 +668,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       cu = cn;
       cn = cn2;
       sid_n1 = sid_n2;
-      if (cu.u < u1) issue_loads(p, cu, sid_next, row, j, g);
+      if (cu.u < u1) issue_loads<kExt>(p, cu, sid_next, row, j, g);
     }
   } else {
     // ======================================================== softmax / epilogue / MMA
@@ -994,8 +1094,9 @@ cudaError_t tc_setup(void *) {
 cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
   using namespace dsa;
   const dim3 grid((unsigned)(p.C * p.HG)), block(kTcThreads);
-  const bool ext = p.rope_gptj || p.mx_on || p.list[0].fmt == DSA_REC_FP8_528_UE8M0 ||
-                   (p.nlists > 1 && p.list[1].fmt == DSA_REC_FP8_528_UE8M0);
+  auto ext_fmt = [](int32_t f) { return f == DSA_REC_FP8_528_UE8M0 || f == DSA_REC_MODEL1_584; };
+  const bool ext = p.rope_gptj || p.mx_on || ext_fmt(p.list[0].fmt) ||
+                   (p.nlists > 1 && ext_fmt(p.list[1].fmt));
   // exact-budget waits (a plan with a wait budget) exist for the plain form
   const bool strict = !ext && p.wait_budget > 0;
   cudaError_t err = cudaSuccess;
