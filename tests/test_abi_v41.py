@@ -84,7 +84,20 @@ def test_ue8m0_record_format_is_accepted(lib):
     bad_extra = B.CacheDesc(FAKE + 8, 64, 64 * 288, 64, 1)
     assert run_v41(lib, a, out=FAKE, swa_desc=ue, extra_desc=bad_extra) == -3
     assert a.call(lib, swa_desc=ue, extra_desc=bad_extra) == -3
-    assert a.call(lib, swa_desc=B.CacheDesc(FAKE, 64, 64 * 528, 64, 3)) == -2
+    assert a.call(lib, swa_desc=B.CacheDesc(FAKE, 64, 64 * 528, 64, 4)) == -2   # no format 4
+
+
+def test_model1_record_format_is_accepted(lib):
+    # MODEL1 (584-byte records): accepted in either list (the refusal comes
+    # from the misaligned other list); its page stride is checked against 584
+    a = Args(we=256)
+    m1 = B.CacheDesc(FAKE, 64, 64 * 584, 64, 3)
+    bad_extra = B.CacheDesc(FAKE + 8, 64, 64 * 288, 64, 1)
+    assert a.call(lib, swa_desc=m1, extra_desc=bad_extra) == -3
+    assert run_v41(lib, a, out=FAKE, swa_desc=m1, extra_desc=bad_extra) == -3
+    bad_swa = B.CacheDesc(FAKE + 8, 64, 64 * 528, 64, 0)
+    assert a.call(lib, swa_desc=bad_swa, extra_desc=B.CacheDesc(FAKE, 64, 64 * 584, 64, 3)) == -3
+    assert a.call(lib, swa_desc=B.CacheDesc(FAKE, 64, 64 * 528, 64, 3)) == -1   # stride < 64 * 584
 
 
 def test_combine_v41_validation(lib):
