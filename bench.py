@@ -59,9 +59,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, help="workload 1..5")
-    ap.add_argument("--variant", choices=["base", "v41"], default="base",
+    ap.add_argument("--variant", choices=["base", "v41", "model1"], default="base",
                     help="v41: ue8m0 fp8 records, GPT-J RoPE, MXFP8 o-fused output "
-                         f"({MX_GROUP} heads per group)")
+                         f"({MX_GROUP} heads per group); model1: MODEL1 (584 B) records "
+                         "in place of the fp8-528 lists")
     ap.add_argument("--tokens", type=int, default=None, help="batch size (default: config's)")
     ap.add_argument("--per-config", dest="per_config", action="store_true", default=True)
     ap.add_argument("--quick", dest="per_config", action="store_false",
@@ -383,7 +384,8 @@ def gpu_arm(args, rank, world, B, peaks, peak_kind):
     torch.cuda.set_device(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     mx = args.variant == "v41"
-    w = W.make_config(args.config, T=args.tokens, device=dev, v41=mx)
+    w = W.make_config(args.config, T=args.tokens, device=dev, v41=mx,
+                      model1=args.variant == "model1")
     alg = algorithmic(w, mx)
     step = Step(w, B, mx)
     clocks = ClockSampler(dev.index)
@@ -419,7 +421,7 @@ def gpu_arm(args, rank, world, B, peaks, peak_kind):
                          "gbs": alg["gathered_bytes"] / (kern_avg * 1e-3) / 1e9,
                          "frac_of_peak": alg["gathered_bytes"] / (kern_avg * 1e-3) / 1e9 / peaks["hbm_gbs"],
                          "gbs_step": alg["gathered_bytes"] / (ms_per_step * 1e-3) / 1e9},
-        "roofline": roofline(w, alg, kern_avg, peaks, peak_kind, captured=not mx),
+        "roofline": roofline(w, alg, kern_avg, peaks, peak_kind, captured=args.variant == "base"),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         # decode, combine (when a token is split), MXFP8 cast (V4.1 output)
@@ -572,7 +574,8 @@ def reference_arm(args):
     import numpy as np
 
     mx = args.variant == "v41"
-    w = W.make_config(args.config, T=args.tokens, device="cpu", v41=mx)
+    w = W.make_config(args.config, T=args.tokens, device="cpu", v41=mx,
+                      model1=args.variant == "model1")
     a = W.oracle_args(w)
     cores = os.cpu_count() or 1
     rng = np.random.default_rng(0)

@@ -328,14 +328,21 @@ CONFIG5_BATCHES = (1, 8, 64, 256, 1024)
 
 
 def make_config(k: int, *, T: Optional[int] = None, device="cpu",
-                seed: Optional[int] = None, page_pad: int = 0, v41: bool = False) -> Workload:
+                seed: Optional[int] = None, page_pad: int = 0, v41: bool = False,
+                model1: bool = False) -> Workload:
     """Measured configuration k. ``v41``: the same shapes and draws in the
     V4.1 form -- every fp8-528 list holds ue8m0-scaled records, RoPE pairs
-    dims GPT-J style."""
+    dims GPT-J style. ``model1``: every fp8-528 list holds MODEL1 records
+    instead (same draws, same RoPE)."""
     c = dict(CONFIGS[k])
     if T is not None:
         c["T"] = T
     name = f"config{k}_T{c['T']}_H{c['H']}"
+    if model1:
+        for key in ("swa", "extra"):
+            if c[key] is not None and c[key]["fmt"] == FMT_FP8_528:
+                c[key] = dict(c[key], fmt=FMT_MODEL1_584)
+        name += "_model1"
     if v41:
         for key in ("swa", "extra"):
             if c[key] is not None and c[key]["fmt"] == FMT_FP8_528:
