@@ -279,7 +279,8 @@ __device__ inline float e2m1_to_f32(uint32_t nib) {
 // first launch of kernel variant `bit` on the current device, later launches
 // skip it (they may be captured into a CUDA graph, where no set-up call is
 // wanted). Thread-safe. Bits in use: tensor-core kernels 0-2 (plain), 20-22
-// (V4.1 options) and 24-26 (exact-budget waits), SIMT kernels 8-11, combine 16.
+// (V4.1 options), 24-26 (exact-budget waits), 28-30 and 32-34 (MODEL1 records),
+// SIMT kernels 8-11, combine 16.
 cudaError_t dsa_configure_once(int bit, cudaError_t (*f)(void *), void *arg);
 
 // Programmatic dependent launch: the decode kernels let the combine grid be

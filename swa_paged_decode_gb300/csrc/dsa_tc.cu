@@ -214,19 +214,22 @@ __device__ __forceinline__ int row_exp(uint32_t field) {
 // the record (sector s holds chunks 2s-1 and 2s); lane j = 0 also holds
 // sector 16 (chunk 31 and the scales) in d[16], d[17]. The two lanes of a
 // row rebuild their pairs with one shuffle per pair (dequant_block).
-// MODEL1 records (kExt): d[2m], d[2m+1] = chunks 4m+2j, 4m+2j+1 of the fp8
-// dims (k-blocks m = 0..6), d[14..17] = chunks 28+4j .. 31+4j (this lane's
-// 32 bf16 dims 448+32j ..), sc8 = the 7 scale bytes and the unused byte.
+// MODEL1 records (kM1): d[i] = chunk A[2i + j], i = 0..17, of the 16-byte
+// grid that starts at the record (pl: the record is 16-byte aligned) or 8
+// bytes before it (odd slots of a 16-byte aligned page); record chunk c
+// (bytes 16c .. 16c+16) is A[c], or off the grid the upper half of A[c] and
+// the lower half of A[c+1], which the row's other lane holds. tail = record
+// bytes 568..583: the last two bf16 words, the 7 scale bytes, the unused one.
 struct Gather {
   uint4 d[18];
-  uint2 sc8;
+  uint4 tail;
   int32_t sid;
   int32_t r;
   bool ok;
   bool pl;
 };
 
-template <bool kExt>
+template <bool kM1>
 __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, int32_t sid, int row,
                                             int j, Gather &g) {
   int32_t lid, row0;
@@ -237,26 +240,21 @@ __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, in
   g.ok = slot_valid(L, g.r, lid == 0 ? c.lim0 : c.lim1, sid);
   const uint4 z = make_uint4(0, 0, 0, 0);
   g.pl = true;
-  if (kExt && L.fmt == DSA_REC_MODEL1_584) {   // 584-byte records, 8-byte aligned
+  if (kM1 && L.fmt == DSA_REC_MODEL1_584) {   // 584-byte records, 8-byte aligned
     if (g.ok) {
       const uint8_t *rec = record_ptr(L, sid);
-      auto chunk = [&](int c) -> uint4 {
-        if ((reinterpret_cast<uintptr_t>(rec) & 15u) == 0) return tc::ldg_nc_v4(rec + 16 * c);
-        const uint2 a = tc::ldg_nc_v2(rec + 16 * c), b = tc::ldg_nc_v2(rec + 16 * c + 8);
-        return make_uint4(a.x, a.y, b.x, b.y);
-      };
+      g.pl = (reinterpret_cast<uintptr_t>(rec) & 15u) == 0;
+      // off the grid the record is an odd slot, so the 8 bytes before it
+      // belong to the previous slot of the same page
+      const uint8_t *a = g.pl ? rec : rec - 8;
 #pragma unroll
-      for (int m = 0; m < 7; ++m) {
-        g.d[2 * m] = chunk(4 * m + 2 * j);
-        g.d[2 * m + 1] = chunk(4 * m + 2 * j + 1);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) g.d[14 + q] = chunk(28 + 4 * j + q);
-      g.sc8 = tc::ldg_nc_v2(rec + 576);
+      for (int i = 0; i < 18; ++i) g.d[i] = tc::ldg_nc_v4(a + 16 * (2 * i + j));
+      const uint2 t0 = tc::ldg_nc_v2(rec + 568), t1 = tc::ldg_nc_v2(rec + 576);
+      g.tail = make_uint4(t0.x, t0.y, t1.x, t1.y);
     } else {
 #pragma unroll
       for (int k = 0; k < 18; ++k) g.d[k] = z;
-      g.sc8 = make_uint2(0, 0);
+      g.tail = z;
     }
     return;
   }
@@ -392,20 +390,31 @@ __device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g
   }
 }
 
-// MODEL1 rows (kExt): M block mb = k-blocks 2mb, 2mb+1. k-blocks 0..6 hold
-// e4m3 codes times ue8m0 byte m of sc8 (one per 64 dims), k-block 7 the bf16
-// RoPE dims; every value times the row's 2^-e (rnorm), as f16.
+// MODEL1 rows (kM1): M block mb = k-blocks 2mb, 2mb+1. k-blocks 0..6 hold
+// e4m3 codes times ue8m0 byte m (one per 64 dims; this lane's record chunks
+// c = 2i + j, i = 2m, 2m+1), k-block 7 the bf16 RoPE dims (i = 14..17);
+// every value times the row's 2^-e (rnorm), as f16. Called by all 32 lanes
+// (the realignment trades halves between the two lanes of a row).
+__device__ __forceinline__ uint4 model1_chunk(const Gather &g, int i, int j) {
+  // off the grid: chunk 2i + j = A[2i+j].zw ++ A[2i+j+1].xy, where A[2i+j+1]
+  // is the other lane's d[i] (j = 0) or d[i+1] (j = 1), and A[36].xy = tail.xy
+  const uint4 send = (j == 0 && i < 17) ? g.d[i + 1] : g.d[i];
+  const uint4 recv = shfl_xor_u4(send, 1);
+  const uint4 nx = (j == 1 && i == 17) ? g.tail : recv;
+  const uint4 own = g.d[i];
+  return g.pl ? own : make_uint4(own.z, own.w, nx.x, nx.y);
+}
 __device__ __forceinline__ void dequant_block_model1(const Gather &g, float rnorm, int mb, int row,
                                                      int j, uint32_t kv_base) {
 #pragma unroll
   for (int mm = 0; mm < 2; ++mm) {
     const int m = 2 * mb + mm;
     if (m < 7) {
-      const uint32_t sb = (m < 4 ? g.sc8.x : g.sc8.y) >> (8 * (m & 3));
+      const uint32_t sb = (m < 4 ? g.tail.z : g.tail.w) >> (8 * (m & 3));
       const uint32_t sc = scale_f16x2(ue8m0_to_f32(sb) * rnorm);
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const uint4 src = g.d[2 * m + e];
+        const uint4 src = model1_chunk(g, 2 * m + e, j);   // dims 64m + 16(2e + j) .. +16
         const uint32_t w[4] = {src.x, src.y, src.z, src.w};
         uint32_t f[8];
 #pragma unroll
@@ -414,21 +423,21 @@ __device__ __forceinline__ void dequant_block_model1(const Gather &g, float rnor
           f[2 * i] = tc::hmul2(f[2 * i], sc);
           f[2 * i + 1] = tc::hmul2(f[2 * i + 1], sc);
         }
-        const int ci = 4 * j + 2 * e;   // dims 64m + 32j + 16e .. +16
+        const int ci = 2 * (2 * e + j);
         tc::st_shared_v4(kv_base + sw128_off(row, m, ci, 16384), f[0], f[1], f[2], f[3]);
         tc::st_shared_v4(kv_base + sw128_off(row, m, ci + 1, 16384), f[4], f[5], f[6], f[7]);
       }
     } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {   // dims 448 + 32j + 8q .. +8
-        const uint4 src = g.d[14 + q];
+      for (int e = 0; e < 4; ++e) {   // dims 448 + 8(2e + j) .. +8
+        const uint4 src = model1_chunk(g, 14 + e, j);
         const uint32_t w[4] = {src.x, src.y, src.z, src.w};
         uint32_t f[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           f[i] = tc::pack_f16x2(bf16_bits_to_f32(w[i] & 0xFFFFu) * rnorm,
                                 bf16_bits_to_f32(w[i] >> 16) * rnorm);
-        tc::st_shared_v4(kv_base + sw128_off(row, 7, 4 * j + q, 16384), f[0], f[1], f[2], f[3]);
+        tc::st_shared_v4(kv_base + sw128_off(row, 7, 2 * e + j, 16384), f[0], f[1], f[2], f[3]);
       }
     }
   }
@@ -455,10 +464,11 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 }
 
 // kExt: the V4.1 options (fp8 records with ue8m0 scales, GPT-J RoPE, MXFP8
-// output); the plain instantiation compiles none of their code.
+// output); the plain instantiation compiles none of their code. kM1: MODEL1
+// records as well, in instantiations of their own (with or without kExt).
 // kStrict: the plan carries a wait budget (a test knob); only that
 // instantiation compiles the exact-budget waits.
-template <int HPG, bool kExt, bool kStrict>
+template <int HPG, bool kExt, bool kStrict, bool kM1>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   using Cfg = TcCfg<HPG>;
   constexpr int NH = Cfg::kHalf;
@@ -550,7 +560,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const ListArgs &L = p.list[lid2];
       if (slot_valid(L, row02 + row, lid2 == 0 ? c.lim0 : c.lim1, sid)) {
         const uint8_t *rec = record_ptr(L, sid);
-        if (kExt && L.fmt == DSA_REC_MODEL1_584) {   // 16-byte aligned span around the record
+        if (kM1 && L.fmt == DSA_REC_MODEL1_584) {   // 16-byte aligned span around the record
           const uintptr_t a0 = reinterpret_cast<uintptr_t>(rec) & ~(uintptr_t)15;
           const uintptr_t a1 = (reinterpret_cast<uintptr_t>(rec) + 584 + 15) & ~(uintptr_t)15;
           tc::prefetch_l2_bulk(reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0));
@@ -569,7 +579,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const int32_t sid0 = load_sid(p, cu, row);
       prefetch(cu, sid0);
       prefetch(cn, sid_n1);
-      issue_loads<kExt>(p, cu, sid0, row, j, g);
+      issue_loads<kM1>(p, cu, sid0, row, j, g);
     }
     while (cu.u < u1) {
       const int32_t t = cu.t;
@@ -580,7 +590,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const int32_t sid_n2 = cn2.u < u1 ? load_sid(p, cn2, row) : -1;
       const int32_t sid_next = sid_n1;
       const bool last_of_token = cn.u >= u1 || cn.t != t;
-      const bool m1 = kExt && p.list[lid].fmt == DSA_REC_MODEL1_584;
+      const bool m1 = kM1 && p.list[lid].fmt == DSA_REC_MODEL1_584;
       const bool fp8 = !m1 && p.list[lid].fmt != DSA_REC_NVFP4_288;
       const bool ue = kExt && p.list[lid].fmt == DSA_REC_FP8_528_UE8M0;
       uint32_t scale2[4] = {0, 0, 0, 0};
@@ -612,14 +622,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       if (m1) {
         // e from the largest scale byte and from the bf16 part's largest
         // magnitude (its exponent field minus 8), so the f16 values stay
-        // below 2^9 either way
-        uint32_t mx = __vmaxu4(g.sc8.x, g.sc8.y & 0x00FFFFFFu);
+        // below 2^9 either way. The bf16 words: tail.xy and d[14..17], except
+        // that off the grid lane 0's d[14] starts 8 bytes early (fp8 codes).
+        uint32_t mx = __vmaxu4(g.tail.z, g.tail.w & 0x00FFFFFFu);
         mx = max(max(mx & 0xFFu, (mx >> 8) & 0xFFu), max((mx >> 16) & 0xFFu, mx >> 24));
-        uint32_t bm = 0;
+        uint32_t bm = __vmaxu2(g.tail.x & 0x7FFF7FFFu, g.tail.y & 0x7FFF7FFFu);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint4 v = g.d[14 + q];
-          bm = __vmaxu2(bm, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+          const bool lo_fp8 = q == 0 && !g.pl && j == 0;
+          const uint32_t vx = lo_fp8 ? 0u : v.x, vy = lo_fp8 ? 0u : v.y;
+          bm = __vmaxu2(bm, __vmaxu2(__vmaxu2(vx & 0x7FFF7FFFu, vy & 0x7FFF7FFFu),
                                      __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
         }
         bm = max(bm & 0xFFFFu, bm >> 16);
@@ -668,7 +681,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       cu = cn;
       cn = cn2;
       sid_n1 = sid_n2;
-      if (cu.u < u1) issue_loads<kExt>(p, cu, sid_next, row, j, g);
+      if (cu.u < u1) issue_loads<kM1>(p, cu, sid_next, row, j, g);
     }
   } else {
     // ======================================================== softmax / epilogue / MMA
@@ -1079,14 +1092,14 @@ bool dsa_tc_supports(int hpg) { return hpg == 16 || hpg == 32 || hpg == 64; }
 namespace {
 // Checks that the kernel kept exactly kLaunchRegs registers per thread (the
 // warpgroup register split assumes it) and raises its shared-memory limit.
-template <int N, bool E, bool S>
+template <int N, bool E, bool S, bool M>
 cudaError_t tc_setup(void *) {
   using namespace dsa;
   cudaFuncAttributes fa;
-  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E, S>);
+  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E, S, M>);
   if (err != cudaSuccess) return err;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(tc_decode_kernel<N, E, S>,
+  return cudaFuncSetAttribute(tc_decode_kernel<N, E, S, M>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<N>::kSmem);
 }
 }  // namespace
@@ -1094,9 +1107,11 @@ cudaError_t tc_setup(void *) {
 cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
   using namespace dsa;
   const dim3 grid((unsigned)(p.C * p.HG)), block(kTcThreads);
-  auto ext_fmt = [](int32_t f) { return f == DSA_REC_FP8_528_UE8M0 || f == DSA_REC_MODEL1_584; };
-  const bool ext = p.rope_gptj || p.mx_on || ext_fmt(p.list[0].fmt) ||
-                   (p.nlists > 1 && ext_fmt(p.list[1].fmt));
+  auto has_fmt = [&](int32_t f) {
+    return p.list[0].fmt == f || (p.nlists > 1 && p.list[1].fmt == f);
+  };
+  const bool m1 = has_fmt(DSA_REC_MODEL1_584);
+  const bool ext = p.rope_gptj || p.mx_on || has_fmt(DSA_REC_FP8_528_UE8M0);
   // exact-budget waits (a plan with a wait budget) exist for the plain form
   const bool strict = !ext && p.wait_budget > 0;
   cudaError_t err = cudaSuccess;
@@ -1104,18 +1119,26 @@ cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
 #define DSA_TC_CASE(N, BIT)                                                              \
   case N: {                                                                              \
     const int smem = (int)TcCfg<N>::kSmem;                                               \
-    if (ext) {                                                                           \
-      err = dsa_configure_once(BIT + 20, &tc_setup<N, true, false>, nullptr);            \
+    if (m1 && ext) {                                                                     \
+      err = dsa_configure_once(BIT + 28, &tc_setup<N, true, false, true>, nullptr);      \
       if (err != cudaSuccess) return err;                                                \
-      tc_decode_kernel<N, true, false><<<grid, block, smem, stream>>>(p);                \
+      tc_decode_kernel<N, true, false, true><<<grid, block, smem, stream>>>(p);          \
+    } else if (m1) {                                                                     \
+      err = dsa_configure_once(BIT + 32, &tc_setup<N, false, false, true>, nullptr);     \
+      if (err != cudaSuccess) return err;                                                \
+      tc_decode_kernel<N, false, false, true><<<grid, block, smem, stream>>>(p);         \
+    } else if (ext) {                                                                    \
+      err = dsa_configure_once(BIT + 20, &tc_setup<N, true, false, false>, nullptr);     \
+      if (err != cudaSuccess) return err;                                                \
+      tc_decode_kernel<N, true, false, false><<<grid, block, smem, stream>>>(p);         \
     } else if (strict) {                                                                 \
-      err = dsa_configure_once(BIT + 24, &tc_setup<N, false, true>, nullptr);            \
+      err = dsa_configure_once(BIT + 24, &tc_setup<N, false, true, false>, nullptr);     \
       if (err != cudaSuccess) return err;                                                \
-      tc_decode_kernel<N, false, true><<<grid, block, smem, stream>>>(p);                \
+      tc_decode_kernel<N, false, true, false><<<grid, block, smem, stream>>>(p);         \
     } else {                                                                             \
-      err = dsa_configure_once(BIT, &tc_setup<N, false, false>, nullptr);                \
+      err = dsa_configure_once(BIT, &tc_setup<N, false, false, false>, nullptr);         \
       if (err != cudaSuccess) return err;                                                \
-      tc_decode_kernel<N, false, false><<<grid, block, smem, stream>>>(p);               \
+      tc_decode_kernel<N, false, false, false><<<grid, block, smem, stream>>>(p);        \
     }                                                                                    \
     break;                                                                               \
   }
