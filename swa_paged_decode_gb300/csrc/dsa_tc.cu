@@ -731,7 +731,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const bool rope = p.cos_sin != nullptr;
       const bool gptj = kExt && p.rope_gptj != 0;
       const bool rlane = rope && lane >= 28, firsth = lane < 30;
-      const float *cs = p.cos_sin + (rope ? pos * 64 + (gptj ? 8 * (lane & 3) : (lane & 1) * 16) : 0);
+      // The token's table row, copied once into this warp's slice of the P
+      // buffer (free while Q is staged: the previous token's last PV has
+      // completed), read from there for each head.
+      float *const csw = reinterpret_cast<float *>(smem + Cfg::kP) + 64 * warp;
+      if (rope) {
+        if (lane < 16)
+          reinterpret_cast<float4 *>(csw)[lane] =
+              __ldg(reinterpret_cast<const float4 *>(p.cos_sin + pos * 64) + lane);
+        __syncwarp();
+      }
+      const float *cs = csw + (gptj ? 8 * (lane & 3) : (lane & 1) * 16);
 #pragma unroll
       for (int i = 0; i < kQH; ++i) {
         const int h = warp + kSmWarps * i;
@@ -746,8 +756,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           float c[8], sn[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            c[k] = __ldg(cs + k);
-            sn[k] = __ldg(cs + kRopeHalf + k);
+            c[k] = cs[k];
+            sn[k] = cs[kRopeHalf + k];
           }
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -760,8 +770,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           float c[16], sn[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            c[k] = __ldg(cs + k);   // the row stays in L1 across the heads
-            sn[k] = __ldg(cs + kRopeHalf + k);
+            c[k] = cs[k];
+            sn[k] = cs[kRopeHalf + k];
           }
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
