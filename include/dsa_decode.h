@@ -126,7 +126,8 @@ typedef struct {
   int32_t tiles_per_token;
   int32_t units_per_cta;   /* units per CTA of an even split (grid sizing)   */
   int32_t ctas_per_group;  /* CTAs per head group                            */
-  int32_t split_tokens;    /* upper bound on tokens split over CTAs          */
+  int32_t split_tokens;    /* upper bound on tokens split over CTAs (0: every
+                              token is whole in one CTA, combine is a no-op)  */
   int32_t kernel;          /* internal kernel variant                        */
   int64_t total_units;     /* T * tiles_per_token                            */
   int64_t ws_sel_offset;   /* workspace byte offsets                         */

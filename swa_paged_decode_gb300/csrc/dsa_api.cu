@@ -215,7 +215,7 @@ dsa_status combine_impl(const dsa_decode_plan_t *plan, void *workspace, size_t w
                         const dsa_mxfp8_out *mx, float *lse, dsa_stream_t stream) {
   if (!plan_ok(plan)) return DSA_ERR_PLAN;
   // bf16 output: only split tokens need this call; MXFP8: every token does
-  if (plan->num_tokens == 0 || (!mx && plan->ctas_per_group <= 1)) return DSA_OK;
+  if (plan->num_tokens == 0 || (!mx && plan->split_tokens == 0)) return DSA_OK;
   if (!lse) return DSA_ERR_INVALID_ARG;
   if (!aligned(lse, 4) || (sink && !aligned(sink, 4))) return DSA_ERR_ALIGNMENT;
   if ((positions == nullptr) != (cos_sin == nullptr)) return DSA_ERR_INVALID_ARG;
@@ -320,12 +320,15 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   if (upc > INT32_MAX || ctas > INT32_MAX / 2) return DSA_ERR_UNSUPPORTED;
   plan->units_per_cta = (int32_t)upc;
   plan->ctas_per_group = (int32_t)ctas;
-  plan->split_tokens = ctas > 1 ? (int32_t)(ctas - 1) : 0;
   // Balancing the work (live tiles plus a per-token cost) pays off when the
   // tokens have many tiles, so ragged lengths leave many dead ones, and
   // there are enough tokens to spread; elsewhere the length scan at kernel
   // start costs more latency than it saves (measured on the five configs).
   plan->balance_live = (num_tokens >= 16 && plan->tiles_per_token >= 8) ? 1 : 0;
+  // An even split whose CTAs hold whole tokens (units per CTA a multiple of
+  // the tiles per token) splits no token: then there is nothing to combine.
+  const bool whole = !plan->balance_live && upc % plan->tiles_per_token == 0;
+  plan->split_tokens = (ctas > 1 && !whole) ? (int32_t)(ctas - 1) : 0;
   // Workspace: status | sel[T][2] | part_lse[HG][2C][hpg] | part_sel[2C][2] |
   //            part_o[HG][2C][hpg][512] | bounds[C+1]
   //            (| stage[T][H][512] fp32, for MXFP8 output only)
@@ -399,7 +402,7 @@ dsa_status dsa_decode_combine(const dsa_decode_plan_t *plan, void *workspace,
                               float *lse, dsa_stream_t stream) {
   NvtxRange range("dsa_decode_combine");
   if (!plan_ok(plan)) return DSA_ERR_PLAN;
-  if (plan->num_tokens == 0 || plan->ctas_per_group <= 1) return DSA_OK;
+  if (plan->num_tokens == 0 || plan->split_tokens == 0) return DSA_OK;
   if (!out) return DSA_ERR_INVALID_ARG;
   return combine_impl(plan, workspace, workspace_bytes, sink, nullptr, nullptr, 0,
                       DSA_ROPE_NEOX, out, nullptr, lse, stream);

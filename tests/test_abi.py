@@ -217,8 +217,8 @@ def test_rope_needs_both_pointers_and_rows(lib):
 
 
 def test_combine_and_selection_validation(lib):
-    a = Args(T=64, we=512)
-    assert a.plan.ctas_per_group > 1
+    a = Args(T=3, we=512)                      # 15 units over 4 CTAs: tokens are split
+    assert a.plan.ctas_per_group > 1 and a.plan.split_tokens > 0
     assert lib.dsa_decode_combine(ctypes.byref(a.plan), None, 0, None, FAKE, FAKE, None) == -4
     assert lib.dsa_decode_combine(ctypes.byref(a.plan), FAKE, a.nbytes, None, None, FAKE, None) == -1
     assert lib.dsa_decode_combine(ctypes.byref(a.plan), FAKE, a.nbytes, None, FAKE + 2, FAKE,
@@ -240,3 +240,18 @@ def test_plan_live_balancing_flag_and_bounds_slot(lib, T, sms):
     assert plan.ws_bounds_offset % 256 == 0
     assert plan.ws_bounds_offset >= plan.ws_part_o_offset
     assert plan.ws_bounds_offset + 8 * (C + 1) <= nbytes
+
+
+def test_split_tokens_zero_only_when_every_token_is_whole(lib):
+    """An even split whose CTAs hold whole tokens splits nothing, so the plan
+    says split_tokens = 0 and combine launches nothing; otherwise it is the
+    upper bound C - 1."""
+    p, _ = B.dsa_decode_plan(4, 16, 128, 0, num_sms=152)      # 1 tile per token, 4 CTAs
+    assert p.ctas_per_group == 4 and p.units_per_cta % p.tiles_per_token == 0
+    assert p.balance_live == 0 and p.split_tokens == 0
+    p, _ = B.dsa_decode_plan(1, 64, 128, 4096, num_sms=152)   # one token over 33 CTAs
+    assert p.split_tokens == p.ctas_per_group - 1 > 0
+    p, _ = B.dsa_decode_plan(1024, 64, 128, 4096, num_sms=152)   # balanced ranges
+    assert p.balance_live == 1 and p.split_tokens == p.ctas_per_group - 1
+    p, _ = B.dsa_decode_plan(400, 16, 128, 0, num_sms=152)     # 3 whole tokens per CTA
+    assert p.units_per_cta == 3 and p.split_tokens == 0

@@ -101,8 +101,8 @@ def test_model1_record_format_is_accepted(lib):
 
 
 def test_combine_v41_validation(lib):
-    a = Args(T=64, we=512)
-    assert a.plan.ctas_per_group > 1
+    a = Args(T=3, we=512)                      # 15 units over 4 CTAs: tokens are split
+    assert a.plan.ctas_per_group > 1 and a.plan.split_tokens > 0
     p = ctypes.byref(a.plan)
     f = lib.dsa_decode_combine_v41
     nb, nm = a.nbytes, a.plan.workspace_bytes_mx
