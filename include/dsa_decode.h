@@ -52,7 +52,9 @@ typedef enum {
   DSA_ERR_WORKSPACE = -4,   /* workspace NULL, too small or misaligned       */
   DSA_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed          */
   DSA_ERR_TIMEOUT = -6,     /* device status: a bounded wait gave up         */
-  DSA_ERR_PLAN = -7         /* plan not made by dsa_decode_plan / mismatched */
+  DSA_ERR_PLAN = -7,        /* plan not made by dsa_decode_plan / mismatched */
+  DSA_ERR_BOUNDS = -8       /* device status, checking build only: an access
+                               outside its extent was skipped               */
 } dsa_status;
 
 /* KV record formats (one record = one slot = one 512-dim row).

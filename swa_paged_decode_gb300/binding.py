@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libdsa_decode.so")
 DSA_OK = 0
 STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED",
                 -3: "DSA_ERR_ALIGNMENT", -4: "DSA_ERR_WORKSPACE", -5: "DSA_ERR_CUDA",
-                -6: "DSA_ERR_TIMEOUT", -7: "DSA_ERR_PLAN"}
+                -6: "DSA_ERR_TIMEOUT", -7: "DSA_ERR_PLAN", -8: "DSA_ERR_BOUNDS"}
 EXPORTED = ("dsa_decode_plan", "dsa_decode_run", "dsa_decode_combine", "dsa_decode_selection",
             "dsa_decode_read_status", "dsa_decode_status_string", "dsa_decode_abi_version",
             "dsa_decode_run_noalloc", "dsa_decode_run_v41", "dsa_decode_combine_v41")
@@ -85,11 +85,31 @@ class MxOut:
         return self.scale.contiguous().view(torch.uint8)
 
 
+LIB_DEBUG_PATH = os.path.join(_HERE, "lib", "libdsa_decode_debug.so")
+_libs = {}
+
+
+def use_checking_build(on: bool):
+    """Route every call of this module through the checking build
+    (libdsa_decode_debug.so: bounds checks on every global and tile access,
+    reported as DSA_ERR_BOUNDS) or back to the release library."""
+    global _lib
+    _lib = _load_path(LIB_DEBUG_PATH if on else LIB_PATH)
+    return _lib
+
+
 def load(path: str = LIB_PATH):
     """Load libdsa_decode.so (raises if it was not built)."""
     global _lib
     if _lib is not None:
         return _lib
+    _lib = _load_path(path)
+    return _lib
+
+
+def _load_path(path: str):
+    if path in _libs:
+        return _libs[path]
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with `python -m swa_paged_decode_gb300.build`"
                            " (the CUDA library is required; there is no fallback)")
@@ -127,7 +147,7 @@ def load(path: str = LIB_PATH):
     lib.dsa_decode_status_string.argtypes = [ctypes.c_int]
     lib.dsa_decode_abi_version.restype = ctypes.c_int32
     lib.dsa_decode_abi_version.argtypes = []
-    _lib = lib
+    _libs[path] = lib
     return lib
 
 

@@ -19,6 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libdsa_decode.so")
+# The checking build (-DDSA_DEBUG): every global and tile access bounds-checked.
+LIB_DEBUG = os.path.join(LIBDIR, "libdsa_decode_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -40,19 +42,24 @@ def _stale(lib: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Build the release library, or with ``debug`` the checking build."""
     srcs = sources()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(INCLUDE, "dsa_decode.h"))
-    if not force and not extra_flags and not _stale(LIB, srcs + headers + [__file__]):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    lib = LIB_DEBUG if debug else LIB
+    bdir = os.path.join(BUILD, "debug") if debug else BUILD
+    if not force and not extra_flags and not _stale(lib, srcs + headers + [__file__]):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                     "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC, *extra_flags]
+    if debug:
+        flags.append("-DDSA_DEBUG")
     procs = []
     for s in srcs:
-        obj = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(s)[:-3] + ".o")
         log = open(obj + ".log", "w")
         procs.append((s, obj, log, subprocess.Popen([nvcc(), *flags, "-c", s, "-o", obj],
                                                     stdout=log, stderr=subprocess.STDOUT)))
@@ -67,11 +74,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 sys.stderr.write(f.read())
     if failed:
         raise RuntimeError(f"nvcc failed for: {', '.join(os.path.basename(f) for f in failed)}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *[p[1] for p in procs]], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -85,6 +85,15 @@ dsa_status fill_list(const dsa_cache_desc *c, const int32_t *idx, int64_t stride
   L.rec = rb;
   L.width = width;
   L.tiles = (width + dsa::kTile - 1) / dsa::kTile;
+  L.extent = c->num_pages * c->page_stride_bytes;
+#ifdef DSA_DEBUG
+  // Checking build only: a smaller extent for the record checks (a test
+  // knob: records past it are reported and skipped, never read).
+  if (const char *cap = std::getenv("DSA_DEBUG_CHECK_EXTENT")) {
+    const long long v = std::atoll(cap);
+    if (v > 0 && v < L.extent) L.extent = v;
+  }
+#endif
   L.aligned32 = (aligned(c->base, 32) && c->page_stride_bytes % 32 == 0 && rb % 32 == 0) ? 1 : 0;
   L.sectors32 = (aligned(c->base, 32) && c->page_stride_bytes % 32 == 0) ? 1 : 0;
   return DSA_OK;
@@ -256,6 +265,7 @@ const char *dsa_decode_status_string(dsa_status s) {
     case DSA_ERR_CUDA: return "CUDA runtime error";
     case DSA_ERR_TIMEOUT: return "device wait timed out";
     case DSA_ERR_PLAN: return "invalid or mismatched plan";
+    case DSA_ERR_BOUNDS: return "checking build: an out-of-extent access was skipped";
   }
   return "unknown status";
 }

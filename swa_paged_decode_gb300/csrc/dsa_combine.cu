@@ -62,7 +62,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   const int tid = threadIdx.x;
 
   // Row-selection record: sum of the parts (one block per token).
-  if (hg == 0 && blockIdx.y == 0 && tid == 0) {   // one block of the token
+  if (hg == 0 && blockIdx.y == 0 && tid == 0 &&
+      dbg_ok(p.status, t >= 0 && t < p.T && c0 >= 0 && c1 < p.C, kDbgSel)) {   // one block of the token
     uint32_t k = 0, s = 0;
     for (int32_t c = c0; c <= c1; ++c) {
       const int64_t slot = slot_of(c);
@@ -74,9 +75,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   }
 
   // lse of every (part, head) of the chunk
+  const int64_t part_n = (int64_t)p.HG * 2 * p.C * hpg;   // partial (slot, head) records
   for (int i = tid; i < np * kCombineHeads; i += kCombineThreads) {
     const int q = i / kCombineHeads, h = i % kCombineHeads;
-    w_s[i] = p.part_lse[(slot_base + slot_of(c0 + q)) * hpg + hb + h];
+    const int64_t ip = (slot_base + slot_of(c0 + q)) * hpg + hb + h;
+    w_s[i] = dbg_ok(p.status, ip >= 0 && ip < part_n, kDbgPartial) ? p.part_lse[ip] : -INFINITY;
   }
   __syncthreads();
   // per head: M = max_i lse_i, w_i = e^{lse_i - M}, z = sum_i w_i
@@ -102,7 +105,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
       inv = 1.f / den;
     }
     inv_s[tid] = inv;
-    if (dq == 0) p.lse[(int64_t)t * p.H + h0 + hb + tid] = (z > 0.f) ? mx + logf(z) : -INFINITY;
+    const int64_t il = (int64_t)t * p.H + h0 + hb + tid;
+    if (dq == 0 && dbg_ok(p.status, il >= 0 && il < (int64_t)p.T * p.H, kDbgOut))
+      p.lse[il] = (z > 0.f) ? mx + logf(z) : -INFINITY;
   }
   __syncthreads();
 
@@ -124,9 +129,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
       for (int k = 0; k < kItems; ++k) {
         const int e = tid + k * kCombineThreads, h = e / kQ4, d4 = dq + e % kQ4;
         o[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (q < np && w_s[q * kCombineHeads + h] != 0.f)
-          o[u][k] = __ldg(reinterpret_cast<const float4 *>(
-              p.part_o + ((slot_base + slot_of(c0 + q)) * hpg + hb + h) * kD) + d4);
+        const int64_t ip = (slot_base + slot_of(c0 + q)) * hpg + hb + h;
+        if (q < np && w_s[q * kCombineHeads + h] != 0.f &&
+            dbg_ok(p.status, ip >= 0 && ip < part_n, kDbgPartial))
+          o[u][k] = __ldg(reinterpret_cast<const float4 *>(p.part_o + ip * kD) + d4);
       }
     }
 #pragma unroll
@@ -148,6 +154,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   for (int k = 0; k < kItems; ++k) {
     const int e = tid + k * kCombineThreads, h = e / kQ4, d4 = dq + e % kQ4;
     const float inv = inv_s[h];
+    const int64_t io = ((int64_t)t * p.H + h0 + hb + h) * kD + 4 * d4;
+    if (!dbg_ok(p.status, io >= 0 && io + 4 <= (int64_t)p.T * p.H * kD, kDbgOut)) continue;
     if (p.stage) {   // MXFP8 output: fp32 to the staging area, cast later
       *reinterpret_cast<float4 *>(p.stage + ((int64_t)t * p.H + h0 + hb + h) * kD + 4 * d4) =
           make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);

@@ -29,6 +29,7 @@ struct ListArgs {
   const int32_t *ids;    // [T, idx_stride]
   const int32_t *lens;   // [T]
   int64_t idx_stride;
+  int64_t extent;        // bytes of the cache: num_pages * page_stride
   int32_t page_shift;    // log2(page_size)
   int32_t page_mask;     // page_size - 1
   int32_t fmt;           // DSA_REC_*
@@ -346,6 +347,29 @@ __device__ __forceinline__ const float *mx_rope_row(const Params &p, int64_t t) 
 // Status word: first failure wins.
 __device__ inline void report_status(int32_t *status, int32_t code) {
   atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- checking build
+// Built with -DDSA_DEBUG (libdsa_decode_debug.so), the kernels check every
+// record, slot-id, Q and table read, every output store and every store into
+// a shared-memory tile against the extent it must stay in. A failed check
+// skips the access (a record read becomes a row that is not kept) and
+// records DSA_ERR_BOUNDS in the status word and the check's kind in word 1 of
+// the status block (first failure wins). The release build compiles none of
+// it (kDebug is false, every check folds to true).
+enum DebugKind : int32_t {
+  kDbgRecord = 1, kDbgIds = 2, kDbgQ = 3, kDbgTable = 4, kDbgOut = 5, kDbgPartial = 6,
+  kDbgSmemKv = 7, kDbgSmemQ = 8, kDbgSmemP = 9, kDbgSel = 10
+};
+#ifdef DSA_DEBUG
+constexpr bool kDebug = true;
+#else
+constexpr bool kDebug = false;
+#endif
+__device__ __forceinline__ bool dbg_ok(int32_t *status, bool ok, int32_t kind) {
+  if (!kDebug || ok) return true;
+  if (atomicCAS(status, 0, DSA_ERR_BOUNDS) == 0) atomicExch(status + 1, kind);
+  return false;
 }
 
 }  // namespace dsa

@@ -238,6 +238,16 @@ __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, in
   g.r = row0 + row;
   g.sid = sid;
   g.ok = slot_valid(L, g.r, lid == 0 ? c.lim0 : c.lim1, sid);
+  if (kDebug && g.ok) {   // checking build: every byte the loads below touch
+    const uint8_t *rec = record_ptr(L, sid);
+    const uintptr_t ra = reinterpret_cast<uintptr_t>(rec);
+    int back = 0;   // bytes read before the record (realigned layouts)
+    if (kM1 && L.fmt == DSA_REC_MODEL1_584)
+      back = (ra & 15u) ? 8 : 0;
+    else if (L.fmt != DSA_REC_NVFP4_288 && (ra & 31u) != 0 && L.sectors32)
+      back = 16;
+    g.ok = dbg_ok(p.status, rec - back >= L.base && rec + L.rec <= L.base + L.extent, kDbgRecord);
+  }
   const uint4 z = make_uint4(0, 0, 0, 0);
   g.pl = true;
   if (kM1 && L.fmt == DSA_REC_MODEL1_584) {   // 584-byte records, 8-byte aligned
@@ -308,7 +318,15 @@ __device__ __forceinline__ int32_t load_sid(const Params &p, const Cursor &c, in
   cursor_tile(p, c, lid, row0);
   const ListArgs &L = p.list[lid];
   const int32_t r = row0 + row;
+  if (!dbg_ok(p.status, c.t >= 0 && c.t < p.T && r >= 0, kDbgIds)) return -1;
   return r < L.width ? __ldg(L.ids + (int64_t)c.t * L.idx_stride + r) : -1;
+}
+
+// Store of one 16-byte chunk into the 128 KiB KV tile (checked in the
+// checking build).
+__device__ __forceinline__ void st_kv(int32_t *dbg, uint32_t kv_base, uint32_t off, uint32_t a,
+                                      uint32_t b, uint32_t c, uint32_t d) {
+  if (dbg_ok(dbg, off + 16u <= 131072u, kDbgSmemKv)) tc::st_shared_v4(kv_base + off, a, b, c, d);
 }
 
 // Dequantize the two 64-dim k-blocks of M block mb for this thread's row.
@@ -326,7 +344,7 @@ __device__ __forceinline__ uint4 shfl_xor_u4(const uint4 v, int mask) {
 // missing half of each chunk pair from the other lane of their row).
 __device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g,
                                               const uint32_t (&scale2)[4], float rnorm, int mb,
-                                              int row, int j, uint32_t kv_base) {
+                                              int row, int j, uint32_t kv_base, int32_t *dbg) {
   if (fp8) {
     // chunks c = 4m + 2j + e of k-block m; M block mb = k-blocks {2mb, 2mb+1}
 #pragma unroll
@@ -352,8 +370,8 @@ __device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g
           f[2 * i + 1] = tc::hmul2(f[2 * i + 1], sc);
         }
         const int ci = (2 * c) & 7;
-        tc::st_shared_v4(kv_base + sw128_off(row, m, ci, 16384), f[0], f[1], f[2], f[3]);
-        tc::st_shared_v4(kv_base + sw128_off(row, m, ci + 1, 16384), f[4], f[5], f[6], f[7]);
+        st_kv(dbg, kv_base, sw128_off(row, m, ci, 16384), f[0], f[1], f[2], f[3]);
+        st_kv(dbg, kv_base, sw128_off(row, m, ci + 1, 16384), f[4], f[5], f[6], f[7]);
       }
     }
   } else {
@@ -367,7 +385,7 @@ __device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g
     const uint4 sq = mb < 2 ? g.d[8] : g.d[9];
     const uint32_t sw0 = j == 0 ? ((mb & 1) ? sq.z : sq.x) : ((mb & 1) ? sq.w : sq.y);
     const uint32_t sw = j == 0 ? sw0 : __funnelshift_l(sw0, sw0, 16);
-    const uint32_t rb = kv_base + (uint32_t)(2 * mb + j) * 16384u + (uint32_t)(row >> 3) * 1024u +
+    const uint32_t rb = (uint32_t)(2 * mb + j) * 16384u + (uint32_t)(row >> 3) * 1024u +
                         (uint32_t)(row & 7) * 128u;
     const int r7j = (row & 7) ^ (4 * j);
 #pragma unroll
@@ -384,7 +402,7 @@ __device__ __forceinline__ void dequant_block(bool fp8, bool ue, const Gather &g
         const uint32_t sc = i < 2 ? sa : sb;
 #pragma unroll
         for (int q = 0; q < 4; ++q) f[q] = tc::hmul2(f[q], sc);
-        tc::st_shared_v4(rb + ((uint32_t)((4 * ee + i) ^ r7j) << 4), f[0], f[1], f[2], f[3]);
+        st_kv(dbg, kv_base, rb + ((uint32_t)((4 * ee + i) ^ r7j) << 4), f[0], f[1], f[2], f[3]);
       }
     }
   }
@@ -405,7 +423,7 @@ __device__ __forceinline__ uint4 model1_chunk(const Gather &g, int i, int j) {
   return g.pl ? own : make_uint4(own.z, own.w, nx.x, nx.y);
 }
 __device__ __forceinline__ void dequant_block_model1(const Gather &g, float rnorm, int mb, int row,
-                                                     int j, uint32_t kv_base) {
+                                                     int j, uint32_t kv_base, int32_t *dbg) {
 #pragma unroll
   for (int mm = 0; mm < 2; ++mm) {
     const int m = 2 * mb + mm;
@@ -424,8 +442,8 @@ __device__ __forceinline__ void dequant_block_model1(const Gather &g, float rnor
           f[2 * i + 1] = tc::hmul2(f[2 * i + 1], sc);
         }
         const int ci = 2 * (2 * e + j);
-        tc::st_shared_v4(kv_base + sw128_off(row, m, ci, 16384), f[0], f[1], f[2], f[3]);
-        tc::st_shared_v4(kv_base + sw128_off(row, m, ci + 1, 16384), f[4], f[5], f[6], f[7]);
+        st_kv(dbg, kv_base, sw128_off(row, m, ci, 16384), f[0], f[1], f[2], f[3]);
+        st_kv(dbg, kv_base, sw128_off(row, m, ci + 1, 16384), f[4], f[5], f[6], f[7]);
       }
     } else {
 #pragma unroll
@@ -437,7 +455,7 @@ __device__ __forceinline__ void dequant_block_model1(const Gather &g, float rnor
         for (int i = 0; i < 4; ++i)
           f[i] = tc::pack_f16x2(bf16_bits_to_f32(w[i] & 0xFFFFu) * rnorm,
                                 bf16_bits_to_f32(w[i] >> 16) * rnorm);
-        tc::st_shared_v4(kv_base + sw128_off(row, 7, 2 * e + j, 16384), f[0], f[1], f[2], f[3]);
+        st_kv(dbg, kv_base, sw128_off(row, 7, 2 * e + j, 16384), f[0], f[1], f[2], f[3]);
       }
     }
   }
@@ -665,9 +683,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         if (!first) wait(kBarKvFree + mb, ph_free[mb]);
         if (mb == 0 && j == 0) row_e_s[row] = g.ok ? erow : kRowInvalid;
         if (m1)
-          dequant_block_model1(g, rnorm, mb, row, j, kv_base);
+          dequant_block_model1(g, rnorm, mb, row, j, kv_base, p.status);
         else
-          dequant_block(fp8, ue, g, scale2, rnorm, mb, row, j, kv_base);
+          dequant_block(fp8, ue, g, scale2, rnorm, mb, row, j, kv_base, p.status);
       }
       // One hand-off per tile: the QK MMAs are issued once the whole tile is
       // in place, so per-block fences and arrives would only lengthen the
@@ -721,9 +739,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       uint4 qa[kQH], qb[kQH];
 #pragma unroll
       for (int i = 0; i < kQH; ++i) {
-        const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)(h0 + warp + kSmWarps * i) * p.q_sh;
-        qa[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane);
-        qb[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane + 1);
+        const int hq = h0 + warp + kSmWarps * i;
+        const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)hq * p.q_sh;
+        if (dbg_ok(p.status, t >= 0 && t < p.T && hq < p.H, kDbgQ)) {
+          qa[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane);
+          qb[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane + 1);
+        } else {
+          qa[i] = qb[i] = make_uint4(0, 0, 0, 0);
+        }
       }
       // Lanes 28..31 hold dims 448..511. NeoX: dim 448+i pairs with 480+i
       // (two lanes apart); GPT-J: 448+2i with 449+2i (inside a lane, pair
@@ -736,7 +759,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       // completed), read from there for each head.
       float *const csw = reinterpret_cast<float *>(smem + Cfg::kP) + 64 * warp;
       if (rope) {
-        if (lane < 16)
+        if (lane < 16 && dbg_ok(p.status, pos >= 0 && pos < p.cs_rows, kDbgTable))
           reinterpret_cast<float4 *>(csw)[lane] =
               __ldg(reinterpret_cast<const float4 *>(p.cos_sin + pos * 64) + lane);
         __syncwarp();
@@ -793,8 +816,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) f[k] = tc::pack_f16x2(v[2 * k] * down, v[2 * k + 1] * down);
         const int kb = lane >> 2, ci = (lane & 3) * 2;
-        tc::st_shared_v4(q_base + sw128_off(h, kb, ci, HPG * 128), f[0], f[1], f[2], f[3]);
-        tc::st_shared_v4(q_base + sw128_off(h, kb, ci + 1, HPG * 128), f[4], f[5], f[6], f[7]);
+        const uint32_t qo = sw128_off(h, kb, ci, HPG * 128), qo1 = sw128_off(h, kb, ci + 1, HPG * 128);
+        if (dbg_ok(p.status, qo + 16u <= HPG * 1024u && qo1 + 16u <= HPG * 1024u, kDbgSmemQ)) {
+          tc::st_shared_v4(q_base + qo, f[0], f[1], f[2], f[3]);
+          tc::st_shared_v4(q_base + qo1, f[4], f[5], f[6], f[7]);
+        }
       }
       if (tid < HPG) m_s[tid] = kMaxInit;
       tc::fence_async_smem();
@@ -839,10 +865,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           iv = 1.f / den;
         }
         const float lse = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
-        if (seg.whole)
-          p.lse[(int64_t)seg.t * p.H + h0 + h] = lse;
-        else
-          p.part_lse[((int64_t)hg * 2 * p.C + seg.slot) * HPG + h] = lse;
+        if (seg.whole) {
+          const int64_t i = (int64_t)seg.t * p.H + h0 + h;
+          if (dbg_ok(p.status, i >= 0 && i < (int64_t)p.T * p.H, kDbgOut)) p.lse[i] = lse;
+        } else {
+          const int64_t i = ((int64_t)hg * 2 * p.C + seg.slot) * HPG + h;
+          if (dbg_ok(p.status, i >= 0 && i < (int64_t)p.HG * 2 * p.C * HPG, kDbgPartial))
+            p.part_lse[i] = lse;
+        }
         red_s[256 - 64 + h] = iv;   // read below; sums of row 3 were consumed above
       }
       if (tid == 0) {   // kept rows / checksum of the token, then clear the slot
@@ -856,8 +886,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         if (hg == 0) {
           int32_t *dst =
               seg.whole ? (p.sel + 2 * (int64_t)seg.t) : (p.part_sel + 2 * (int64_t)seg.slot);
-          dst[0] = (int32_t)k2;
-          dst[1] = (int32_t)c2;
+          if (dbg_ok(p.status, seg.whole ? (seg.t >= 0 && seg.t < p.T)
+                                         : (seg.slot >= 0 && seg.slot < 2 * p.C), kDbgSel)) {
+            dst[0] = (int32_t)k2;
+            dst[1] = (int32_t)c2;
+          }
         }
       }
       if (seg_worked) ++sord;
@@ -876,12 +909,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
             const int h = half * NH + 8 * g8 + i;
             const float iv = red_s[256 - 64 + h];
             const float v = (!seg_worked || iv == 0.f) ? 0.f : o[i] * iv;
+            const int64_t io = ((int64_t)seg.t * p.H + h0 + h) * kD + d;
+            const int64_t ip = (((int64_t)hg * 2 * p.C + seg.slot) * HPG + h) * kD + d;
+            if (seg.whole && !dbg_ok(p.status, io >= 0 && io < (int64_t)p.T * p.H * kD, kDbgOut))
+              continue;
+            if (!seg.whole &&
+                !dbg_ok(p.status, ip >= 0 && ip < (int64_t)p.HG * 2 * p.C * HPG * kD, kDbgPartial))
+              continue;
             if (seg.whole && stage != nullptr)
-              stage[((int64_t)seg.t * p.H + h0 + h) * kD + d] = v;
+              stage[io] = v;
             else if (seg.whole)
-              p.out[((int64_t)seg.t * p.H + h0 + h) * kD + d] = __float2bfloat16_rn(v);
+              p.out[io] = __float2bfloat16_rn(v);
             else
-              p.part_o[(((int64_t)hg * 2 * p.C + seg.slot) * HPG + h) * kD + d] = v;
+              p.part_o[ip] = v;
           }
         }
       }
@@ -974,7 +1014,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) pw[e] = tc::pack_f16x2(v[8 * k + 2 * e], v[8 * k + 2 * e + 1]);
           const int ci = half * (NH / 8) + k;
-          tc::st_shared_v4(p_base + p_off<HPG>(prow, ci), pw[0], pw[1], pw[2], pw[3]);
+          const uint32_t po = p_off<HPG>(prow, ci);
+          if (dbg_ok(p.status, po + 16u <= Cfg::kPBytes, kDbgSmemP))
+            tc::st_shared_v4(p_base + po, pw[0], pw[1], pw[2], pw[3]);
         }
       };
       float x[NH];
