@@ -567,10 +567,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     bool first = true;
     int warm = 0;
     uint32_t kept = 0, chk = 0, pord = 0;
-    // Tile records are loaded into registers one tile ahead; while the CTA
-    // warms up (its first tiles) they are also prefetched into L2 (bulk, one
-    // thread per row) two tiles ahead. In steady state the register loads
-    // cover the latency and the extra prefetch traffic measured slower.
+    // Tile records are loaded into registers one tile ahead, and prefetched
+    // into L2 (bulk, one thread per row) two tiles ahead while the CTA warms
+    // up and for fp8 tiles (see below).
     auto prefetch = [&](const Cursor &c, int32_t sid) {
       if (j != 0 || c.u >= u1) return;
       int32_t lid2, row02;
@@ -694,7 +693,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarKvFull]);
       first = false;
-      if (warm < 2) prefetch(cn2, sid_n2);   // L2 prefetch only while the CTA warms up
+      // L2 prefetch two tiles ahead: while the CTA warms up, and always for
+      // fp8 tiles, whose 17 sector loads per row otherwise keep the load
+      // queue full into the softmax (config 4: +7 %); for NVFP4 tiles the
+      // register loads alone cover the latency (prefetching them cost 1.5 %).
+      if (warm < 2 || p.list[cn2.k < p.list[0].tiles ? 0 : 1].fmt != DSA_REC_NVFP4_288)
+        prefetch(cn2, sid_n2);
       ++warm;
       cu = cn;
       cn = cn2;
