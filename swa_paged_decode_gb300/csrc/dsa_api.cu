@@ -303,18 +303,20 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   plan->kernel = dsa_tc_supports(plan->heads_per_group) ? dsa::kKernelTc : dsa::kKernelSimt;
   if (const char *k = std::getenv("DSA_DECODE_KERNEL"))
     if (std::strcmp(k, "simt") == 0) plan->kernel = dsa::kKernelSimt;
-  // Small batches: while the units of all head groups would give each SM
-  // at most 4, halve the heads per group (down to 16). Each CTA then stages
-  // Q for and finalizes fewer heads -- the per-token steps that bound a CTA
-  // with a few tiles -- and more CTAs share them; the groups read the same
-  // records (the repeats mostly hit L2). Measured per step: config 5 T=1
-  // 53 -> 29 us, T=8 60 -> 47 us, config 2 39 -> 31 us, larger batches
-  // unchanged. FlashMLA spreads a small batch the same way over
-  // num_sm_parts = num_sms / s_q parts (sparse_decode.h, get_meta); here the
-  // extra parts split the heads.
+  // Small batches: halve the heads per group (down to 16) while the units of
+  // all head groups would give each SM at most 4 (the first halving) or 2
+  // (further ones). Each CTA then stages Q for and finalizes fewer heads --
+  // the per-token steps that bound a CTA with a few tiles -- and more CTAs
+  // share them; the groups read the same records (the repeats mostly hit
+  // L2). Measured per step: config 5 T=1 53 -> 29 us, T=8 60 -> 45 us,
+  // config 2 39 -> 31 us, larger batches unchanged. FlashMLA spreads a small
+  // batch the same way over num_sm_parts = num_sms / s_q parts
+  // (sparse_decode.h, get_meta); here the extra parts split the heads.
   if (plan->kernel == dsa::kKernelTc) {
+    const int32_t hpg0 = plan->heads_per_group;
     while (plan->heads_per_group > 16 &&
-           plan->total_units * plan->head_groups <= 4 * (int64_t)num_sms) {
+           plan->total_units * plan->head_groups <=
+               (plan->heads_per_group == hpg0 ? 4 : 2) * (int64_t)num_sms) {
       plan->head_groups *= 2;
       plan->heads_per_group /= 2;
     }
