@@ -43,9 +43,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # while the kernel sources hash to `sources`. The capture is summarised under
 # profiles/ with the command that made it.
 NCU_TRAFFIC = {
-    "sources": "785b2e910b26d3bf",
+    "sources": "8b10738ad1e8d06a",
     "workload": "config5_T256_H64",
-    "bytes_per_launch": 426228736 + 25545984,
+    "bytes_per_launch": 426197248 + 25872384,
     "rows_per_launch": 256 * (128 + 4096),
 }
 KERNEL_SOURCES = ("swa_paged_decode_gb300/csrc/dsa_tc.cu", "swa_paged_decode_gb300/csrc/tc_ptx.cuh",
@@ -227,6 +227,12 @@ def max_over_ranks(x: float, world: int, device) -> float:
 
 def time_steps(step: Step, steps: int, warmup: int, flush: torch.Tensor, clocks=None,
                world: int = 1):
+    """Timed region: `steps` whole steps (run then combine issued back to
+    back, as a caller issues them; L2 flushed before each), events only
+    around each step. Then, outside it, a second pass with events around
+    the decode kernel alone (an event between run and combine would hold
+    back the combine's programmatic early launch, so it is not in the timed
+    steps)."""
     for _ in range(warmup):
         flush.zero_()
         step()
@@ -234,18 +240,23 @@ def time_steps(step: Step, steps: int, warmup: int, flush: torch.Tensor, clocks=
     rank_barrier(world)            # all replicas start the timed region together
     torch.cuda.synchronize()
     E = lambda: torch.cuda.Event(enable_timing=True)
-    evs = [(E(), E(), E(), E()) for _ in range(steps)]
+    evs = [(E(), E()) for _ in range(steps)]
     ctx = clocks if clocks is not None else _Null()
     with ctx:
-        for s0, k0, k1, s1 in evs:
+        for s0, s1 in evs:
             flush.zero_()
             s0.record()
-            step(k0, k1)
+            step()
             s1.record()
         torch.cuda.synchronize()
     rank_barrier(world)
-    step_ms = [a.elapsed_time(b) for a, _, _, b in evs]
-    kern_ms = [a.elapsed_time(b) for _, a, b, _ in evs]
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    kev = [(E(), E()) for _ in range(steps)]
+    for k0, k1 in kev:
+        flush.zero_()
+        step(k0, k1)
+    torch.cuda.synchronize()
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
     return sum(step_ms), step_ms, kern_ms
 
 
