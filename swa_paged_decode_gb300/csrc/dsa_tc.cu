@@ -725,6 +725,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     const float4 *hf_s4 = reinterpret_cast<const float4 *>(headf_s) + half * (NH / 4);
     int32_t cur_t = -1;
     bool seg_worked = false, first_pv = true;
+    // the sink logit of head tid, read once (finalize needs it per token)
+    const float sink_h = (tid < HPG && p.sink) ? __ldg(p.sink + h0 + tid) : 0.f;
 
     // Q of token t -> f16 K-major SW128 tile. RoPE (NeoX) in fp32, then a
     // power-of-two prescale per head so its max |q| lies in [1, 2): exact
@@ -740,35 +742,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         if (tid == 0) report_status(p.status, DSA_ERR_INVALID_ARG);
         pos = 0;
       }
+      // Lane -> dims: lanes 0..27 hold 8-dim chunks 2 lane and 2 lane + 1
+      // (dims 16 lane .. 16 lane + 15); lanes 28..31 (the RoPE dims
+      // 448..511) hold chunks 56 + r and 60 + r, r = lane - 28 (dims
+      // 448 + 8r .. +7 and 480 + 8r .. +7), so that both NeoX pairs
+      // (448 + i, 480 + i) and GPT-J pairs (448 + 2i, 449 + 2i) lie inside
+      // one lane and the rotation needs no shuffles.
+      const bool rl = lane >= 28;
+      const int ca = rl ? 56 + (lane - 28) : 2 * lane, cb = rl ? 60 + (lane - 28) : 2 * lane + 1;
       uint4 qa[kQH], qb[kQH];
 #pragma unroll
       for (int i = 0; i < kQH; ++i) {
         const int hq = h0 + warp + kSmWarps * i;
         const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)hq * p.q_sh;
         if (dbg_ok(p.status, t >= 0 && t < p.T && hq < p.H, kDbgQ)) {
-          qa[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane);
-          qb[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + 2 * lane + 1);
+          qa[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + ca);
+          qb[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + cb);
         } else {
           qa[i] = qb[i] = make_uint4(0, 0, 0, 0);
         }
       }
-      // Lanes 28..31 hold dims 448..511. NeoX: dim 448+i pairs with 480+i
-      // (two lanes apart); GPT-J: 448+2i with 449+2i (inside a lane, pair
-      // index 8 (lane - 28) + k for its values 2k, 2k+1).
+      // This lane's cos / sin from the token's table row: NeoX pairs
+      // 8r .. 8r + 7; GPT-J pairs 4r .. 4r + 3 (chunk 56 + r) and
+      // 16 + 4r .. 16 + 4r + 3 (chunk 60 + r). Entry i is cos, i + 32 sin.
       const bool rope = p.cos_sin != nullptr;
       const bool gptj = kExt && p.rope_gptj != 0;
-      const bool rlane = rope && lane >= 28, firsth = lane < 30;
-      // The token's table row, copied once into this warp's slice of the P
-      // buffer (free while Q is staged: the previous token's last PV has
-      // completed), read from there for each head.
-      float *const csw = reinterpret_cast<float *>(smem + Cfg::kP) + 64 * warp;
-      if (rope) {
-        if (lane < 16 && dbg_ok(p.status, pos >= 0 && pos < p.cs_rows, kDbgTable))
-          reinterpret_cast<float4 *>(csw)[lane] =
-              __ldg(reinterpret_cast<const float4 *>(p.cos_sin + pos * 64) + lane);
-        __syncwarp();
+      float c8[8], s8[8];
+      if (rope && rl && dbg_ok(p.status, pos >= 0 && pos < p.cs_rows, kDbgTable)) {
+        const float4 *row = reinterpret_cast<const float4 *>(p.cos_sin + pos * 64);
+        const int r = lane - 28;
+        const int f0 = gptj ? r : 2 * r, f1 = gptj ? 4 + r : 2 * r + 1;   // float4 index of cos
+        const float4 ca0 = __ldg(row + f0), ca1 = __ldg(row + f1);
+        const float4 sa0 = __ldg(row + 8 + f0), sa1 = __ldg(row + 8 + f1);
+        c8[0] = ca0.x; c8[1] = ca0.y; c8[2] = ca0.z; c8[3] = ca0.w;
+        c8[4] = ca1.x; c8[5] = ca1.y; c8[6] = ca1.z; c8[7] = ca1.w;
+        s8[0] = sa0.x; s8[1] = sa0.y; s8[2] = sa0.z; s8[3] = sa0.w;
+        s8[4] = sa1.x; s8[5] = sa1.y; s8[6] = sa1.z; s8[7] = sa1.w;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          c8[k] = 1.f;
+          s8[k] = 0.f;
+        }
       }
-      const float *cs = csw + (gptj ? 8 * (lane & 3) : (lane & 1) * 16);
+      const bool rot = rope && rl;
 #pragma unroll
       for (int i = 0; i < kQH; ++i) {
         const int h = warp + kSmWarps * i;
@@ -779,48 +796,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           v[2 * k] = bf16_bits_to_f32(w[k] & 0xFFFFu);
           v[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
         }
-        if (rope && gptj) {   // every lane reads a valid row entry, lanes 28..31 use it
-          float c[8], sn[8];
+        if (rot) {
+          if (gptj) {   // (v[2m], v[2m+1]) pair 4r + m; (v[8+2m], v[9+2m]) pair 16 + 4r + m
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            c[k] = cs[k];
-            sn[k] = cs[kRopeHalf + k];
-          }
+            for (int m = 0; m < 8; ++m) {
+              const int a = 2 * m;   // m < 4: chunk A, else chunk B (c8/s8 index m)
+              const float x1 = v[a], x2 = v[a + 1];
+              v[a] = fmaf(x1, c8[m], -(x2 * s8[m]));
+              v[a + 1] = fmaf(x2, c8[m], x1 * s8[m]);
+            }
+          } else {      // (v[k], v[8+k]) pair 8r + k
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float x1 = v[2 * k], x2 = v[2 * k + 1];
-            const float r1 = fmaf(x1, c[k], -(x2 * sn[k])), r2 = fmaf(x2, c[k], x1 * sn[k]);
-            v[2 * k] = rlane ? r1 : x1;
-            v[2 * k + 1] = rlane ? r2 : x2;
-          }
-        } else if (rope) {   // branch-free: every lane reads a valid row entry, lanes 28..31 use it
-          float c[16], sn[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            c[k] = cs[k];
-            sn[k] = cs[kRopeHalf + k];
-          }
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[k], 2);
-            const float r = firsth ? fmaf(v[k], c[k], -other * sn[k]) : fmaf(v[k], c[k], other * sn[k]);
-            v[k] = rlane ? r : v[k];
+            for (int k = 0; k < 8; ++k) {
+              const float x1 = v[k], x2 = v[8 + k];
+              v[k] = fmaf(x1, c8[k], -(x2 * s8[k]));
+              v[8 + k] = fmaf(x2, c8[k], x1 * s8[k]);
+            }
           }
         }
         float mx = 0.f;
 #pragma unroll
         for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(v[k]));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        int e = (mx > 0.f) ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+        // max |q| of the head: non-negative floats order as their bits
+        const uint32_t mbits = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+        int e = mbits ? (int)((mbits >> 23) & 0xFF) - 127 : 0;
         e = e < -126 ? -126 : (e > 126 ? 126 : e);
         const float down = __uint_as_float((uint32_t)(127 - e) << 23);
         if (lane == 0) headf_s[h] = p.scale_log2 * __uint_as_float((uint32_t)(127 + e) << 23);
         uint32_t f[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) f[k] = tc::pack_f16x2(v[2 * k] * down, v[2 * k + 1] * down);
-        const int kb = lane >> 2, ci = (lane & 3) * 2;
-        const uint32_t qo = sw128_off(h, kb, ci, HPG * 128), qo1 = sw128_off(h, kb, ci + 1, HPG * 128);
+        const uint32_t qo = sw128_off(h, ca >> 3, ca & 7, HPG * 128);
+        const uint32_t qo1 = sw128_off(h, cb >> 3, cb & 7, HPG * 128);
         if (dbg_ok(p.status, qo + 16u <= HPG * 1024u && qo1 + 16u <= HPG * 1024u, kDbgSmemQ)) {
           tc::st_shared_v4(q_base + qo, f[0], f[1], f[2], f[3]);
           tc::st_shared_v4(q_base + qo1, f[4], f[5], f[6], f[7]);
@@ -863,7 +870,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         if (l > 0.f) {
           float den = l;
           if (seg.whole && p.sink) {
-            const float sk = __ldg(p.sink + h0 + h);
+            const float sk = sink_h;
             den = (sk == INFINITY) ? INFINITY : l + tc::ex2(sk * kLog2e - m);
           }
           iv = 1.f / den;
