@@ -281,7 +281,7 @@ __device__ inline float e2m1_to_f32(uint32_t nib) {
 // skip it (they may be captured into a CUDA graph, where no set-up call is
 // wanted). Thread-safe. Bits in use: tensor-core kernels 0-2 (plain), 20-22
 // (V4.1 options), 24-26 (exact-budget waits), 28-30 and 32-34 (MODEL1 records),
-// SIMT kernels 8-11, combine 16.
+// SIMT kernels 8-11, combine 16-18.
 cudaError_t dsa_configure_once(int bit, cudaError_t (*f)(void *), void *arg);
 
 // Programmatic dependent launch: the decode kernels let the combine grid be
