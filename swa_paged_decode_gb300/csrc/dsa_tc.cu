@@ -1057,13 +1057,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         load_s(x);
 #pragma unroll
         for (int j = 0; j < NH; ++j) x[j] = fmaf(x[j], headf_s[half * NH + j] * rs, er);   // y
+        // Per-head max over the warp's 32 rows by recursive halving, in
+        // place (x is reloaded below): at step st a lane keeps the upper
+        // half of its 2 st values when lane bit st is set, else the lower,
+        // and takes the max with the partner's copy of that half; head j
+        // ends in lane j (NH < 32: lanes j, j + NH, ... are folded last).
 #pragma unroll
-        for (int j = 0; j < NH; ++j) {
-          float v = x[j];
+        for (int st = NH / 2; st >= 1; st >>= 1) {
+          const bool up = (lane & st) != 0;
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-          if (lane == 0) red_s[q4 * 64 + half * NH + j] = v;
+          for (int i = 0; i < st; ++i) {
+            const float send = up ? x[i] : x[i + st];
+            const float keep = up ? x[i + st] : x[i];
+            x[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, st));
+          }
         }
+#pragma unroll
+        for (int off = NH; off < 32; off <<= 1) x[0] = fmaxf(x[0], __shfl_xor_sync(0xffffffffu, x[0], off));
+        if (lane < NH) red_s[q4 * 64 + half * NH + lane] = x[0];
         sm_bar();
         if (tid < HPG) {   // new max and rescale factor of head tid (factor -> red_s[tid])
           const float tm = fmaxf(fmaxf(red_s[tid], red_s[64 + tid]), fmaxf(red_s[128 + tid], red_s[192 + tid]));
@@ -1089,6 +1100,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
             }
           }
         }
+        load_s(x);
+#pragma unroll
+        for (int j = 0; j < NH; ++j) x[j] = fmaf(x[j], headf_s[half * NH + j] * rs, er);   // y
 #pragma unroll
         for (int g4 = 0; g4 < NH / 4; ++g4) {
           const float4 m4 = m_s4[g4];
