@@ -116,8 +116,9 @@ __device__ inline int64_t token_cost(int64_t live) {
 }
 
 // Unit range [u0, u1) of CTA c. Called by every thread of the block (it
-// synchronizes the block); scr: shared scratch of blockDim.x + 2 int64. Also
-// publishes the range to p.bounds for the combine kernel.
+// synchronizes the block; blockDim.x a multiple of 32, at most 1024); scr:
+// shared scratch of blockDim.x + 2 + blockDim.x / 32 int64. Also publishes
+// the range to p.bounds for the combine kernel.
 __device__ inline void cta_range(const Params &p, int32_t c, int64_t *scr, int64_t &u0,
                                  int64_t &u1) {
   const int n = blockDim.x, tid = threadIdx.x;
@@ -135,14 +136,30 @@ __device__ inline void cta_range(const Params &p, int32_t c, int64_t *scr, int64
   const int64_t t0 = T * tid / n, t1 = T * (tid + 1) / n;
   int64_t sum = 0;
   for (int64_t t = t0; t < t1; ++t) sum += token_cost(live_tiles_token(p, t));
-  scr[tid] = sum;
-  __syncthreads();
-  for (int off = 1; off < n; off <<= 1) {   // inclusive scan over the threads' token chunks
-    const int64_t v = tid >= off ? scr[tid - off] : 0;
-    __syncthreads();
-    scr[tid] += v;
-    __syncthreads();
+  // inclusive scan over the threads' token chunks: within each warp by
+  // shuffles, then over the warp totals (one warp), then their offsets
+  const int lane = tid & 31, wid = tid >> 5, nw = n >> 5;
+  int64_t v = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += y;
   }
+  int64_t *wsum = scr + n + 2;   // [nw] warp totals, then their inclusive prefixes
+  if (lane == 31) wsum[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int64_t w = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    if (lane < nw) wsum[lane] = w;
+  }
+  __syncthreads();
+  scr[tid] = v + (wid > 0 ? wsum[wid - 1] : 0);
+  __syncthreads();
   const int64_t L = scr[n - 1];   // total cost
   if (tid < 2) {
     const int64_t cc = (int64_t)c + tid;
