@@ -1035,21 +1035,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       // Scores and, against the current running max, P -- optimistically:
       // the max moves on only when a score passes it by kRescaleSlack (a few
       // tiles per token), and then the whole group redoes P below.
-      bool need = false;
+      // (The token's first tile always raises the max from its initial
+      // value: it goes straight to the exact pass.)
+      bool need = first_pv;
+      if (!first_pv) {
 #pragma unroll
-      for (int g4 = 0; g4 < NH / 4; ++g4) {
-        const float4 m4 = m_s4[g4], f4 = hf_s4[g4];
-        const float mm[4] = {m4.x, m4.y, m4.z, m4.w}, hf[4] = {f4.x, f4.y, f4.z, f4.w};
+        for (int g4 = 0; g4 < NH / 4; ++g4) {
+          const float4 m4 = m_s4[g4], f4 = hf_s4[g4];
+          const float mm[4] = {m4.x, m4.y, m4.z, m4.w}, hf[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float &xv = x[4 * g4 + i];
-          const float t = fmaf(xv, hf[i] * rs, er - mm[i]);   // y - m (-inf if not kept)
-          need |= t > kRescaleSlack;
-          xv = tc::ex2(t);
+          for (int i = 0; i < 4; ++i) {
+            float &xv = x[4 * g4 + i];
+            const float t = fmaf(xv, hf[i] * rs, er - mm[i]);   // y - m (-inf if not kept)
+            need |= t > kRescaleSlack;
+            xv = tc::ex2(t);
+          }
         }
+        store_p(x);
+        tc::fence_async_smem();
       }
-      store_p(x);
-      tc::fence_async_smem();
       tc::tc_fence_before();
       if (sm_bar_or(need ? 1 : 0)) {
         // Raise the running max to the tile max; rescale sums and O; redo P.
