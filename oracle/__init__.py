@@ -32,7 +32,10 @@ FMT_FP8_528 = 0
 FMT_NVFP4_288 = 1
 FMT_FP8_528_UE8M0 = 2
 FMT_MODEL1_584 = 3
-RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288, FMT_FP8_528_UE8M0: 528, FMT_MODEL1_584: 584}
+FMT_V32_656 = 4
+RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288, FMT_FP8_528_UE8M0: 528, FMT_MODEL1_584: 584,
+                FMT_V32_656: 656}
+KEY_DIMS = {FMT_V32_656: 576}   # formats whose keys have more than 512 dims
 ROPE_NEOX = 0
 ROPE_GPTJ = 1
 
@@ -124,7 +127,7 @@ def ue8m0_ceil(v: float) -> int:
 def dequant_record(record: np.ndarray, fmt: int) -> np.ndarray:
     rec = np.ascontiguousarray(record, dtype=np.uint8)
     assert rec.size == RECORD_BYTES[fmt]
-    out = np.zeros(512, dtype=np.float64)
+    out = np.zeros(KEY_DIMS.get(fmt, 512), dtype=np.float64)
     _load().oracle_dequant_record(rec.ctypes.data, fmt, out.ctypes.data)
     return out
 
@@ -153,7 +156,8 @@ def decode(q, caches, lists, *, scale: float, sink=None, positions=None, cos_sin
            tokens=None, nthreads: int | None = None, rope_style: int = ROPE_NEOX):
     """Run the oracle.
 
-    q        : bf16 [T, H, 512] (torch CPU tensor) or uint16 numpy bit patterns.
+    q        : bf16 [T, H, 512] (torch CPU tensor) or uint16 numpy bit patterns;
+               [T, H, 576] when the lists hold V3.2 records (no RoPE then).
     caches   : sequence of dicts {bytes: uint8 array (whole cache), num_pages,
                page_size, page_stride, format} -- one per list.
     lists    : sequence of dicts {ids: int32 [T, >=width], lens: int32 [T], width}.
@@ -166,7 +170,7 @@ def decode(q, caches, lists, *, scale: float, sink=None, positions=None, cos_sin
     lib = _load()
     qn = _np(q, np.uint16)
     T, H, D = qn.shape
-    assert D == 512
+    assert D == (576 if any(int(c["format"]) == FMT_V32_656 for c in caches) else 512)
     if tokens is None:
         tokens = np.arange(T, dtype=np.int32)
     tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))

@@ -40,6 +40,15 @@
  *      meaning 2^(b-127)), byte 583 unused: k[d] = e4m3(byte d) *
  *      2^(byte[576 + d/64] - 127) for d < 448, k[d] = bf16 value for
  *      d >= 448.
+ *      The V3.2 record of the same page (bytes_per_token = 512 + 64*2 +
+ *      (512/128)*4 for d_qk = 576, d_v = 512; again only byte counts):
+ *      read as the fp8 record above (512 e4m3 codes, then 4 little-endian
+ *      fp32 scales, one per 128 dims) followed by the 64 extra key dims as
+ *      little-endian bf16 values (bytes 528..655). The key has 576 dims,
+ *      k[d] = e4m3(byte d) * scale(d / 128) for d < 512 and k[512 + i] =
+ *      bf16 value i; the value row is k[0..511]. Q then has 576 dims, taken
+ *      as given (the page's kernel applies no rotation; a RoPE table is
+ *      rejected with this record), and out has 512.
  *   4. Q.  q = bf16 value of q[t, h, :] in fp64. With RoPE on, the last 64
  *      dims are rotated by the fp32 table row cos_sin[positions[t]] =
  *      [cos(32) | sin(32)], pair i taking c = cos[i], s = sin[i]:
@@ -71,7 +80,8 @@
 #include <stdlib.h>
 #include <string.h>
 
-#define ORACLE_D 512
+#define ORACLE_D 512      /* value dims (and key dims, but for the V3.2 record) */
+#define ORACLE_DQK_V32 576
 #define ORACLE_ROPE_START 448
 #define ORACLE_ROPE_HALF 32
 
@@ -79,7 +89,8 @@ enum {
   ORACLE_FMT_FP8_528 = 0,
   ORACLE_FMT_NVFP4_288 = 1,
   ORACLE_FMT_FP8_528_UE8M0 = 2,
-  ORACLE_FMT_MODEL1_584 = 3
+  ORACLE_FMT_MODEL1_584 = 3,
+  ORACLE_FMT_V32_656 = 4
 };
 enum { ORACLE_ROPE_NEOX = 0, ORACLE_ROPE_GPTJ = 1 };
 
@@ -148,14 +159,21 @@ static double bf16_value(uint16_t u) {
 
 static int record_bytes(int32_t format) {
   if (format == ORACLE_FMT_NVFP4_288) return 288;
+  if (format == ORACLE_FMT_V32_656) return 656;
   return format == ORACLE_FMT_MODEL1_584 ? 584 : 528;
 }
 
-/* Step 3: one record -> 512 fp64 values. */
+/* Step 3: one record -> its key dims in fp64 (512 values; 576 for the V3.2
+ * record). */
 void oracle_dequant_record(const uint8_t *rec, int32_t format, double *k) {
-  if (format == ORACLE_FMT_FP8_528) {
+  if (format == ORACLE_FMT_FP8_528 || format == ORACLE_FMT_V32_656) {
     for (int d = 0; d < ORACLE_D; ++d)
       k[d] = oracle_e4m3_value(rec[d]) * le_f32(rec + 512 + 4 * (d / 128));
+    if (format == ORACLE_FMT_V32_656)
+      for (int i = 0; i < ORACLE_DQK_V32 - ORACLE_D; ++i) {
+        const uint8_t *b = rec + 528 + 2 * i;
+        k[ORACLE_D + i] = bf16_value((uint16_t)(b[0] | (b[1] << 8)));
+      }
   } else if (format == ORACLE_FMT_FP8_528_UE8M0) {
     for (int d = 0; d < ORACLE_D; ++d)
       k[d] = oracle_e4m3_value(rec[d]) * oracle_ue8m0_value(rec[512 + d / 32]);
@@ -186,7 +204,7 @@ static uint32_t fmix32(uint32_t h) {
 
 /* Step 1 for one token: kept rows of one list -> appended to K. */
 static int64_t gather_list(const oracle_cache *c, const oracle_list *l, int32_t lid,
-                           int32_t t, double *K, int64_t n, uint32_t *sum) {
+                           int32_t t, int dk, double *K, int64_t n, uint32_t *sum) {
   int32_t len = l->lens[t];
   int32_t limit = len < 0 ? 0 : (len > l->width ? l->width : len);
   int64_t slots = c->num_pages * (int64_t)c->page_size;
@@ -197,7 +215,7 @@ static int64_t gather_list(const oracle_cache *c, const oracle_list *l, int32_t 
     int64_t blk = (int64_t)id / c->page_size;
     int64_t off = (int64_t)id % c->page_size;
     const uint8_t *rec = c->base + blk * c->page_stride + off * rb;
-    oracle_dequant_record(rec, c->format, K + n * ORACLE_D);
+    oracle_dequant_record(rec, c->format, K + n * dk);
     *sum += fmix32((uint32_t)id * 0x9E3779B1u + 2u * (uint32_t)r + (uint32_t)lid);
     ++n;
   }
@@ -216,6 +234,7 @@ typedef struct {
   const float *cos_sin;
   int64_t cs_rows;
   int32_t rope_style;   /* ORACLE_ROPE_* */
+  int32_t dk;           /* key / query dims: 512, or 576 with V3.2 records */
   double scale;
   const int32_t *tokens;
   int32_t n_tokens;
@@ -233,14 +252,15 @@ static void one_token(oracle_job *J, int32_t i, double *K, double *s) {
   int64_t n = 0;
   uint32_t sum = 0;
   for (int32_t L = 0; L < J->nlists; ++L)
-    n = gather_list(&J->caches[L], &J->lists[L], L, t, K, n, &sum);
+    n = gather_list(&J->caches[L], &J->lists[L], L, t, J->dk, K, n, &sum);
   J->kept[i] = (int32_t)n;
   J->checksum[i] = sum;
 
-  double q[ORACLE_D];
+  double q[ORACLE_DQK_V32];
+  const int dk = J->dk;
   for (int32_t h = 0; h < J->H; ++h) {
     const uint16_t *qh = J->q + (int64_t)t * J->q_st + (int64_t)h * J->q_sh;
-    for (int d = 0; d < ORACLE_D; ++d) q[d] = bf16_value(qh[d]);
+    for (int d = 0; d < dk; ++d) q[d] = bf16_value(qh[d]);
     if (J->cos_sin) {
       int64_t pos = J->positions[t];
       const float *row = J->cos_sin + pos * 64;
@@ -262,9 +282,9 @@ static void one_token(oracle_job *J, int32_t i, double *K, double *s) {
     /* Step 5: scores. */
     double mx = -INFINITY;
     for (int64_t j = 0; j < n; ++j) {
-      const double *k = K + j * ORACLE_D;
+      const double *k = K + j * dk;
       double dot = 0.0;
-      for (int d = 0; d < ORACLE_D; ++d) dot += q[d] * k[d];
+      for (int d = 0; d < dk; ++d) dot += q[d] * k[d];
       s[j] = J->scale * dot;
       if (s[j] > mx) mx = s[j];
     }
@@ -285,7 +305,7 @@ static void one_token(oracle_job *J, int32_t i, double *K, double *s) {
     double den = z + exp(sk - mx);
     for (int64_t j = 0; j < n; ++j) {
       double w = exp(s[j] - mx) / den;
-      const double *k = K + j * ORACLE_D;
+      const double *k = K + j * dk;   /* the value: the key's first 512 dims */
       for (int d = 0; d < ORACLE_D; ++d) o[d] += w * k[d];
     }
   }
@@ -295,7 +315,7 @@ static void *worker(void *arg) {
   oracle_job *J = (oracle_job *)arg;
   int64_t maxrows = 0;
   for (int32_t L = 0; L < J->nlists; ++L) maxrows += J->lists[L].width;
-  double *K = (double *)malloc((size_t)(maxrows > 0 ? maxrows : 1) * ORACLE_D * sizeof(double));
+  double *K = (double *)malloc((size_t)(maxrows > 0 ? maxrows : 1) * J->dk * sizeof(double));
   double *s = (double *)malloc((size_t)(maxrows > 0 ? maxrows : 1) * sizeof(double));
   if (!K || !s) {
     J->status = -1;
@@ -310,6 +330,8 @@ static void *worker(void *arg) {
 /* Runs steps 1-6 for the listed tokens. Outputs are indexed by position in
  * `tokens`: out[n_tokens][H][512], lse[n_tokens][H], kept[n_tokens],
  * checksum[n_tokens]. rope_style: ORACLE_ROPE_NEOX or ORACLE_ROPE_GPTJ.
+ * q rows have 576 dims when the lists hold V3.2 records (all of them, and
+ * no RoPE table), else 512.
  * Returns 0, or -1 on bad arguments / out of memory. */
 int oracle_decode(int32_t H, const uint16_t *q, int64_t q_st, int64_t q_sh,
                   const oracle_cache *caches, const oracle_list *lists, int32_t nlists,
@@ -320,6 +342,10 @@ int oracle_decode(int32_t H, const uint16_t *q, int64_t q_st, int64_t q_sh,
   if (H <= 0 || !q || !caches || !lists || nlists < 1 || nlists > 2 || n_tokens < 0) return -1;
   if (rope_style != ORACLE_ROPE_NEOX && rope_style != ORACLE_ROPE_GPTJ) return -1;
   if (cos_sin && !positions) return -1;
+  int v32 = 0;
+  for (int32_t L = 0; L < nlists; ++L) v32 += caches[L].format == ORACLE_FMT_V32_656;
+  if (v32 != 0 && (v32 != nlists || cos_sin)) return -1;
+  const int dk = v32 ? ORACLE_DQK_V32 : ORACLE_D;
   if (nthreads < 1) nthreads = 1;
   if (nthreads > n_tokens && n_tokens > 0) nthreads = n_tokens;
   oracle_job *jobs = (oracle_job *)calloc((size_t)nthreads, sizeof(oracle_job));
@@ -335,6 +361,7 @@ int oracle_decode(int32_t H, const uint16_t *q, int64_t q_st, int64_t q_sh,
     J->caches = caches; J->lists = lists; J->nlists = nlists;
     J->sink = sink; J->positions = positions; J->cos_sin = cos_sin; J->cs_rows = cs_rows;
     J->rope_style = rope_style;
+    J->dk = dk;
     J->scale = scale; J->tokens = tokens; J->n_tokens = n_tokens;
     J->out = out; J->lse = lse; J->kept = kept; J->checksum = checksum;
     J->nthreads = nthreads; J->tid = w; J->status = 0;

@@ -25,6 +25,10 @@ workloads of this method):
     e4m3 codes of dims 0..447 with one ue8m0 scale per 64 dims (same rule as
     above, per 64 dims), dims 448..511 (the RoPE part) as little-endian bf16
     (round to nearest even), the 7 scale bytes, one zero pad byte.
+  * V3.2-656 (same page: 512 + 64*2 + (512/128)*4 bytes for d_qk = 576,
+    d_v = 512): the fp8-528 record of the first 512 source dims, then the
+    64 further key dims as little-endian bf16 (round to nearest even); the
+    source rows have 576 dims, Q too, and no RoPE is applied to Q.
 
 The five named workloads follow the configurations the method is measured on
 (T tokens, H query heads, one shared 512-dim KV row per slot). Seeds: workload
@@ -44,10 +48,13 @@ FMT_FP8_528 = 0
 FMT_NVFP4_288 = 1
 FMT_FP8_528_UE8M0 = 2
 FMT_MODEL1_584 = 3
+FMT_V32_656 = 4
 RECORD_BYTES = {FMT_FP8_528: 528, FMT_NVFP4_288: 288, FMT_FP8_528_UE8M0: 528,
-                FMT_MODEL1_584: 584}
+                FMT_MODEL1_584: 584, FMT_V32_656: 656}
 FMT_NAMES = {FMT_FP8_528: "fp8_528", FMT_NVFP4_288: "nvfp4_288",
-             FMT_FP8_528_UE8M0: "fp8_528_ue8m0", FMT_MODEL1_584: "model1_584"}
+             FMT_FP8_528_UE8M0: "fp8_528_ue8m0", FMT_MODEL1_584: "model1_584",
+             FMT_V32_656: "v32_656"}
+KEY_DIMS_V32 = 576   # key / query dims with V3.2 records (values keep 512)
 ROPE_NEOX = 0   # dim 448+i pairs with 480+i
 ROPE_GPTJ = 1   # dim 448+2i pairs with 449+2i
 ROPE_TABLE_ROWS = 131072
@@ -162,6 +169,13 @@ def encode_model1_records(x: torch.Tensor) -> torch.Tensor:
     return torch.cat([codes, rope, sbytes, pad], dim=1)
 
 
+def encode_v32_records(x: torch.Tensor) -> torch.Tensor:
+    """[n, 576] float -> [n, 656] uint8 V3.2 records."""
+    n = x.shape[0]
+    tail = x[:, HEAD_DIM:].float().to(torch.bfloat16).contiguous().view(torch.uint8).reshape(n, 128)
+    return torch.cat([encode_fp8_records(x[:, :HEAD_DIM]), tail], dim=1)
+
+
 def _e2m1_codes(y: torch.Tensor) -> torch.Tensor:
     """Round-to-nearest-even onto e2m1 magnitudes {0,.5,1,1.5,2,3,4,6}, saturating
     at 6; returns 4-bit codes (sign in bit 3) as uint8."""
@@ -202,11 +216,12 @@ def make_cache(num_slots: int, page_size: int, fmt: int, gen: torch.Generator,
     recs = data[:, :page_size * rb].view(num_pages, page_size, rb)
     enc = {FMT_FP8_528: encode_fp8_records, FMT_NVFP4_288: encode_nvfp4_records,
            FMT_FP8_528_UE8M0: encode_fp8_ue8m0_records,
-           FMT_MODEL1_584: encode_model1_records}[fmt]
+           FMT_MODEL1_584: encode_model1_records, FMT_V32_656: encode_v32_records}[fmt]
+    dk = KEY_DIMS_V32 if fmt == FMT_V32_656 else HEAD_DIM
     chunk = max(page_size, chunk - chunk % page_size)
     for s0 in range(0, num_slots, chunk):
         s1 = min(num_slots, s0 + chunk)          # both multiples of page_size
-        x = torch.randn((s1 - s0, HEAD_DIM), generator=gen, device=device)
+        x = torch.randn((s1 - s0, dk), generator=gen, device=device)
         if tuple(mag) != (0,):
             m = torch.tensor([float(k) for k in mag], dtype=torch.float32, device=device)
             sl = torch.arange(s0, s1, device=device) % len(mag)
@@ -273,7 +288,10 @@ def make_workload(*, T: int, H: int, swa: dict, extra: Optional[dict] = None,
     specs = [swa] + ([extra] if extra is not None else [])
     caches = [make_cache(s["slots"], s["page"], s["fmt"], gen, device, page_pad,
                          mag=s.get("mag", (0,))) for s in specs]
-    q = torch.randn((T, H, HEAD_DIM), generator=gen, device=device)
+    v32 = [s["fmt"] == FMT_V32_656 for s in specs]
+    assert not any(v32) or (all(v32) and not rope), "V3.2 records: every list, no RoPE"
+    dk = KEY_DIMS_V32 if any(v32) else HEAD_DIM
+    q = torch.randn((T, H, dk), generator=gen, device=device)
     if q_log2:
         q = q * 2.0 ** q_log2
     q = q.to(torch.bfloat16)
@@ -295,7 +313,7 @@ def make_workload(*, T: int, H: int, swa: dict, extra: Optional[dict] = None,
         pos = torch.randint(0, ROPE_TABLE_ROWS, (T,), generator=gen, device=device,
                             dtype=torch.int64)
         cs = rope_table(ROPE_TABLE_ROWS, device)
-    return Workload(name, T, H, scale if scale is not None else HEAD_DIM ** -0.5, q,
+    return Workload(name, T, H, scale if scale is not None else dk ** -0.5, q,
                     caches[0], lists[0],
                     caches[1] if extra is not None else None,
                     lists[1] if extra is not None else None, sk, pos, cs, rope_style)
@@ -329,15 +347,23 @@ CONFIG5_BATCHES = (1, 8, 64, 256, 1024)
 
 def make_config(k: int, *, T: Optional[int] = None, device="cpu",
                 seed: Optional[int] = None, page_pad: int = 0, v41: bool = False,
-                model1: bool = False) -> Workload:
+                model1: bool = False, v32: bool = False) -> Workload:
     """Measured configuration k. ``v41``: the same shapes and draws in the
     V4.1 form -- every fp8-528 list holds ue8m0-scaled records, RoPE pairs
     dims GPT-J style. ``model1``: every fp8-528 list holds MODEL1 records
-    instead (same draws, same RoPE)."""
+    instead (same draws, same RoPE). ``v32``: every list holds V3.2 records
+    (576-dim keys and Q, no RoPE; same widths, lengths and caches' slot
+    counts and pages)."""
     c = dict(CONFIGS[k])
     if T is not None:
         c["T"] = T
     name = f"config{k}_T{c['T']}_H{c['H']}"
+    if v32:
+        for key in ("swa", "extra"):
+            if c[key] is not None:
+                c[key] = dict(c[key], fmt=FMT_V32_656)
+        c["rope"] = False
+        name += "_v32"
     if model1:
         for key in ("swa", "extra"):
             if c[key] is not None and c[key]["fmt"] == FMT_FP8_528:
