@@ -59,10 +59,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, help="workload 1..5")
-    ap.add_argument("--variant", choices=["base", "v41", "model1"], default="base",
+    ap.add_argument("--variant", choices=["base", "v41", "model1", "v32"], default="base",
                     help="v41: ue8m0 fp8 records, GPT-J RoPE, MXFP8 o-fused output "
                          f"({MX_GROUP} heads per group); model1: MODEL1 (584 B) records "
-                         "in place of the fp8-528 lists")
+                         "in place of the fp8-528 lists; v32: V3.2 (656 B, 576-dim keys) "
+                         "records in every list, no RoPE")
     ap.add_argument("--tokens", type=int, default=None, help="batch size (default: config's)")
     ap.add_argument("--per-config", dest="per_config", action="store_true", default=True)
     ap.add_argument("--quick", dest="per_config", action="store_false",
@@ -102,10 +103,11 @@ def algorithmic(w: W.Workload, mx: bool = False):
     cnt = kept_rows(w)
     rows = sum(int(k.sum()) for k, _ in cnt)
     gathered = sum(int(k.sum()) * rb for k, rb in cnt)
-    flops = 2 * 2 * W.HEAD_DIM * w.H * rows      # QK^T and PV, 2 flops per MAC
+    dqk = int(w.q.shape[-1])                     # 512, or 576 with V3.2 records
+    flops = 2 * (dqk + W.HEAD_DIM) * w.H * rows  # QK^T (dqk) and PV (512), 2 flops per MAC
     ids_bytes = 4 * (w.swa.width + (0 if w.extra is None else w.extra.width)) * w.T
     out_bytes = w.T * w.H * (W.HEAD_DIM + W.HEAD_DIM // 32) if mx else w.T * w.H * W.HEAD_DIM * 2
-    io_bytes = w.T * w.H * W.HEAD_DIM * 2 + out_bytes + w.T * w.H * 4   # q in, out, lse
+    io_bytes = w.T * w.H * dqk * 2 + out_bytes + w.T * w.H * 4   # q in, out, lse
     return dict(rows=rows, gathered_bytes=gathered, flops=flops,
                 total_bytes=gathered + ids_bytes + io_bytes)
 
@@ -411,7 +413,7 @@ def gpu_arm(args, rank, world, B, peaks, peak_kind):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     mx = args.variant == "v41"
     w = W.make_config(args.config, T=args.tokens, device=dev, v41=mx,
-                      model1=args.variant == "model1")
+                      model1=args.variant == "model1", v32=args.variant == "v32")
     alg = algorithmic(w, mx)
     step = Step(w, B, mx)
     clocks = ClockSampler(dev.index)
@@ -604,7 +606,7 @@ def reference_arm(args):
 
     mx = args.variant == "v41"
     w = W.make_config(args.config, T=args.tokens, device="cpu", v41=mx,
-                      model1=args.variant == "model1")
+                      model1=args.variant == "model1", v32=args.variant == "v32")
     a = W.oracle_args(w)
     cores = os.cpu_count() or 1
     rng = np.random.default_rng(0)

@@ -84,10 +84,26 @@ typedef enum {
  * account); FP8_528 values are code * (scale * 2^-e rounded to f16),
  * rounded to f16 (relative error <= 2^-11 for blocks within 2^14 of the
  * row's largest scale; scales up to 2^55).
+ * V32_656  : FlashMLA's V3.2 record (sparse_decode.h page: bytes_per_token =
+ *            512 + 64*2 + (512/128)*4 for d_qk = 576, d_v = 512; only the
+ *            byte counts are given): read as the FP8_528 record followed by
+ *            the key's 64 further dims as little-endian bf16 (bytes
+ *            528..655). Keys have 576 dims and values are their first 512;
+ *            q then has 576 dims per head. Needs a plan made with d_qk = 576
+ *            (dsa_decode_plan_qk), every list in this format, and no RoPE
+ *            table (q arrives as the model rotated it). Precision as FP8_528
+ *            for dims 0..511; the bf16 dims are exact down to 2^-26 of the
+ *            row's largest value (e takes them into account).
  * Source: the swapab page (record sizes 528 and 288, NVFP4 block of 16 with
  * e4m3 scales) with the fp32-per-128 scale layout of FlashMLA's V3.2 record
  * (sparse_decode.h, bytes_per_token = 512 + ... + (512/128)*4).            */
-enum { DSA_REC_FP8_528 = 0, DSA_REC_NVFP4_288 = 1, DSA_REC_FP8_528_UE8M0 = 2, DSA_REC_MODEL1_584 = 3 };
+enum {
+  DSA_REC_FP8_528 = 0,
+  DSA_REC_NVFP4_288 = 1,
+  DSA_REC_FP8_528_UE8M0 = 2,
+  DSA_REC_MODEL1_584 = 3,
+  DSA_REC_V32_656 = 4
+};
 
 /* RoPE pairings of q dims 448..511 with a table row [cos(32) | sin(32)]:
  * NEOX pairs dim 448+i with 480+i, GPTJ pairs 448+2i with 449+2i (the swapab
@@ -154,7 +170,10 @@ typedef struct {
                               DSA_DECODE_WAIT_BUDGET environment variable at
                               planning time, so tests can make a wait run
                               out on purpose                                 */
-  int64_t reserved[11];
+  int64_t d_qk;             /* key / query dims the plan was made for: 512, or
+                              576 (V3.2 records); 0 in a zeroed plan reads
+                              as 512                                        */
+  int64_t reserved[10];
 } dsa_decode_plan_t;
 
 /* Plan one decode call.
@@ -173,6 +192,18 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
                            int32_t extra_width, int32_t num_sms,
                            dsa_decode_plan_t *plan, size_t *workspace_bytes);
 
+/* Defined by: FlashMLA's sparse_decode.h page, sparse_attn_decode_interface
+ * (d_qk == 576 || d_qk == 512; d_qk = 576 with d_v = 512 is its V3.2 model
+ * type), with the scheduling of dsa_decode_plan.
+ * As dsa_decode_plan, for key / query dims d_qk: 512 (the same plan), or
+ * 576 for V3.2 records. With 576 the heads are split into
+ * groups of at most 32 (a 576-dim Q tile of 64 heads and the key tile do not
+ * fit in shared memory together), so num_heads must be 16, 32, 64 or 128
+ * (48 and 96 give DSA_ERR_UNSUPPORTED). Other d_qk: DSA_ERR_INVALID_ARG. */
+dsa_status dsa_decode_plan_qk(int32_t num_tokens, int32_t num_heads, int32_t swa_width,
+                              int32_t extra_width, int32_t num_sms, int32_t d_qk,
+                              dsa_decode_plan_t *plan, size_t *workspace_bytes);
+
 /* Run the fused gather + dequant + attention kernel (argument order after the
  * plan and workspace follows the problem statement: q, sliding-window cache
  * and list, extra cache and list, sink, positions, cos_sin, scale, out, lse).
@@ -184,8 +215,10 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
  * one KV head, d_v = 512, an optional extra cache with its own indices and
  * lengths, an optional attention sink, out and lse returned).
  *
- * q          : bf16 [T, H, 512], element (t, h, d) at q + t*q_stride_t +
- *              h*q_stride_h + d (strides in elements); 16-byte aligned rows.
+ * q          : bf16 [T, H, d_qk] (d_qk = 512, or 576 with V3.2 records),
+ *              element (t, h, d) at q + t*q_stride_t + h*q_stride_h + d
+ *              (strides in elements, q_stride_h >= d_qk); 16-byte aligned
+ *              rows.
  * swa_cache  : required. swa_idx: int32 [T, swa_idx_stride >= swa_width]
  *              slot ids (-1 = unused). swa_lens: int32 [T]; entries at
  *              positions >= clamp(len, 0, width) are ignored.

@@ -22,7 +22,7 @@ DSA_OK = 0
 STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED",
                 -3: "DSA_ERR_ALIGNMENT", -4: "DSA_ERR_WORKSPACE", -5: "DSA_ERR_CUDA",
                 -6: "DSA_ERR_TIMEOUT", -7: "DSA_ERR_PLAN", -8: "DSA_ERR_BOUNDS"}
-EXPORTED = ("dsa_decode_plan", "dsa_decode_run", "dsa_decode_combine", "dsa_decode_selection",
+EXPORTED = ("dsa_decode_plan", "dsa_decode_plan_qk", "dsa_decode_run", "dsa_decode_combine", "dsa_decode_selection",
             "dsa_decode_read_status", "dsa_decode_status_string", "dsa_decode_abi_version",
             "dsa_decode_run_noalloc", "dsa_decode_run_v41", "dsa_decode_combine_v41")
 DSA_ROPE_NEOX = 0
@@ -49,8 +49,8 @@ class Plan(ctypes.Structure):
         [(n, ctypes.c_int64) for n in (
             "total_units", "ws_sel_offset", "ws_part_lse_offset", "ws_part_sel_offset",
             "ws_part_o_offset", "workspace_bytes", "ws_bounds_offset", "balance_live",
-            "ws_stage_offset", "workspace_bytes_mx", "wait_budget_cycles")] + \
-        [("reserved", ctypes.c_int64 * 11)]
+            "ws_stage_offset", "workspace_bytes_mx", "wait_budget_cycles", "d_qk")] + \
+        [("reserved", ctypes.c_int64 * 10)]
 
 
 _lib = None
@@ -118,6 +118,9 @@ def _load_path(path: str):
     lib.dsa_decode_plan.restype = ctypes.c_int
     lib.dsa_decode_plan.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(Plan),
                                     ctypes.POINTER(ctypes.c_size_t)]
+    lib.dsa_decode_plan_qk.restype = ctypes.c_int
+    lib.dsa_decode_plan_qk.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(Plan),
+                                       ctypes.POINTER(ctypes.c_size_t)]
     lib.dsa_decode_run.restype = ctypes.c_int
     lib.dsa_decode_run.argtypes = [ctypes.POINTER(Plan), vp, ctypes.c_size_t, vp, i64, i64,
                                    ctypes.POINTER(CacheDesc), vp, i64, vp,
@@ -180,6 +183,18 @@ def dsa_decode_plan(num_tokens: int, num_heads: int, swa_width: int, extra_width
     _check("dsa_decode_plan", load().dsa_decode_plan(num_tokens, num_heads, swa_width,
                                                      extra_width, num_sms, ctypes.byref(plan),
                                                      ctypes.byref(ws)))
+    return plan, int(ws.value)
+
+
+def dsa_decode_plan_qk(num_tokens: int, num_heads: int, swa_width: int, extra_width: int = 0,
+                       num_sms: int = 0, d_qk: int = 512):
+    """-> (Plan, workspace_bytes) for key / query dims d_qk (512, or 576 for
+    V3.2 records)."""
+    plan = Plan()
+    ws = ctypes.c_size_t(0)
+    _check("dsa_decode_plan_qk", load().dsa_decode_plan_qk(num_tokens, num_heads, swa_width,
+                                                           extra_width, num_sms, d_qk,
+                                                           ctypes.byref(plan), ctypes.byref(ws)))
     return plan, int(ws.value)
 
 
@@ -300,8 +315,9 @@ class Decoder:
     MXFP8 output goes through the V4.1 entry points."""
 
     def __init__(self, w: W.Workload, num_sms: int = 0, mx_group: Optional[int] = None):
-        self.plan, nbytes = dsa_decode_plan(w.T, w.H, w.swa.width,
-                                            0 if w.extra is None else w.extra.width, num_sms)
+        self.plan, nbytes = dsa_decode_plan_qk(w.T, w.H, w.swa.width,
+                                               0 if w.extra is None else w.extra.width, num_sms,
+                                               int(w.q.shape[-1]))
         dev = w.q.device
         if mx_group is not None:
             nbytes = self.plan.workspace_bytes_mx

@@ -53,6 +53,7 @@ bool pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 int record_bytes(int32_t fmt) {
   if (fmt == DSA_REC_FP8_528 || fmt == DSA_REC_FP8_528_UE8M0) return 528;
   if (fmt == DSA_REC_MODEL1_584) return 584;
+  if (fmt == DSA_REC_V32_656) return 656;
   return fmt == DSA_REC_NVFP4_288 ? 288 : -1;
 }
 
@@ -172,7 +173,8 @@ dsa_status run_impl(const dsa_decode_plan_t *plan, void *workspace, size_t works
   if (plan->num_tokens == 0) return DSA_OK;
   if (!q || !lse) return DSA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return DSA_ERR_INVALID_ARG;
-  if (q_stride_h < dsa::kD || q_stride_t < (int64_t)plan->num_heads * q_stride_h)
+  const int64_t dqk = plan->d_qk == 576 ? 576 : dsa::kD;
+  if (q_stride_h < dqk || q_stride_t < (int64_t)plan->num_heads * q_stride_h)
     return DSA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || q_stride_t % 8 != 0 || q_stride_h % 8 != 0) return DSA_ERR_ALIGNMENT;
   if (!aligned(lse, 4)) return DSA_ERR_ALIGNMENT;
@@ -202,6 +204,12 @@ dsa_status run_impl(const dsa_decode_plan_t *plan, void *workspace, size_t works
     if (s != DSA_OK) return s;
     p.nlists = 2;
   }
+  // V3.2 records: in every list, with a plan for 576-dim keys, no RoPE
+  // table and no V4.1 output options; other records with 512-dim keys
+  for (int i = 0; i < p.nlists; ++i)
+    if ((p.list[i].fmt == DSA_REC_V32_656) != (dqk == 576)) return DSA_ERR_UNSUPPORTED;
+  if (dqk == 576 && (cos_sin || mx || rope_style != DSA_ROPE_NEOX)) return DSA_ERR_UNSUPPORTED;
+  p.dqk = (int32_t)dqk;
   p.q = static_cast<const __nv_bfloat16 *>(q);
   p.q_st = q_stride_t;
   p.q_sh = q_stride_h;
@@ -273,10 +281,20 @@ const char *dsa_decode_status_string(dsa_status s) {
 dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_width,
                            int32_t extra_width, int32_t num_sms, dsa_decode_plan_t *plan,
                            size_t *workspace_bytes) {
+  return dsa_decode_plan_qk(num_tokens, num_heads, swa_width, extra_width, num_sms, 512, plan,
+                            workspace_bytes);
+}
+
+dsa_status dsa_decode_plan_qk(int32_t num_tokens, int32_t num_heads, int32_t swa_width,
+                              int32_t extra_width, int32_t num_sms, int32_t d_qk,
+                              dsa_decode_plan_t *plan, size_t *workspace_bytes) {
   if (!plan || !workspace_bytes) return DSA_ERR_INVALID_ARG;
   if (num_tokens < 0 || swa_width < 1 || extra_width < 0 || num_sms < 0)
     return DSA_ERR_INVALID_ARG;
+  if (d_qk != 512 && d_qk != 576) return DSA_ERR_INVALID_ARG;
   if (!heads_supported(num_heads)) return DSA_ERR_UNSUPPORTED;
+  // 576-dim keys: groups of at most 32 heads on the tensor-core kernel
+  if (d_qk == 576 && (num_heads == 48 || num_heads == 96)) return DSA_ERR_UNSUPPORTED;
   if (num_sms == 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
@@ -291,8 +309,13 @@ dsa_status dsa_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t swa_wi
   plan->swa_width = swa_width;
   plan->extra_width = extra_width;
   plan->num_sms = num_sms;
+  plan->d_qk = d_qk;
   plan->head_groups = num_heads <= 64 ? 1 : 2;
   plan->heads_per_group = num_heads / plan->head_groups;
+  while (d_qk == 576 && plan->heads_per_group > 32) {
+    plan->head_groups *= 2;
+    plan->heads_per_group /= 2;
+  }
   plan->tiles_swa = (swa_width + dsa::kTile - 1) / dsa::kTile;
   plan->tiles_extra = (extra_width + dsa::kTile - 1) / dsa::kTile;
   plan->tiles_per_token = plan->tiles_swa + plan->tiles_extra;

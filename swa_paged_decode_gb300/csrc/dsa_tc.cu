@@ -71,16 +71,18 @@ constexpr int kRowExpMax = 48;
 constexpr int32_t kRowInvalid = INT32_MIN;       // row record of a row that is not kept
 constexpr float kMaxInit = -1e30f;               // running max before any kept row
 
-template <int HPG>
+template <int HPG, bool V32 = false>
 struct TcCfg {
   static constexpr int kSmRegs = HPG == 64 ? 152 : 144;
   static constexpr int kPrRegs = 2 * kLaunchRegs - kSmRegs;
   static constexpr int kHalf = HPG / 2;                  // heads per softmax thread
   static constexpr int kPRow = HPG * 2;                  // bytes per P row
   static constexpr uint32_t kPBytes = 128 * kPRow;
+  static constexpr int kQD = V32 ? 576 : 512;            // Q (and key) dims
   static constexpr uint32_t kKV = 0;                     // 128 x 512 f16 = 128 KiB
-  static constexpr uint32_t kQ = 131072;                 // HPG x 512 f16
-  static constexpr uint32_t kP = kQ + HPG * 1024;        // [128 x HPG] f16
+  static constexpr uint32_t kKR = 131072;                // V32: [128 x 64] f16, key dims 512..575
+  static constexpr uint32_t kQ = kKR + (V32 ? 16384 : 0);   // HPG x kQD f16 (k-blocks of 64 dims)
+  static constexpr uint32_t kP = kQ + HPG * kQD * 2;     // [128 x HPG] f16
   static constexpr uint32_t kRho = kP + kPBytes;         // [128] int32 row exponent, kRowInvalid: not kept
   static constexpr uint32_t kHeadF = kRho + 1024;        // [64] f32 per-head score factor
   static constexpr uint32_t kM = kHeadF + 256;           // [64] running max (log2)
@@ -223,13 +225,14 @@ __device__ __forceinline__ int row_exp(uint32_t field) {
 struct Gather {
   uint4 d[18];
   uint4 tail;
+  uint4 rp[4];   // V3.2 records: this lane's 32 bf16 key dims 512 + 32j ..
   int32_t sid;
   int32_t r;
   bool ok;
   bool pl;
 };
 
-template <bool kM1>
+template <bool kM1, bool kV32>
 __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, int32_t sid, int row,
                                             int j, Gather &g) {
   int32_t lid, row0;
@@ -268,7 +271,13 @@ __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, in
     }
     return;
   }
-  if (L.fmt != DSA_REC_NVFP4_288) {   // both 528-byte fp8 records
+  if (L.fmt != DSA_REC_NVFP4_288) {   // both 528-byte fp8 records (and V3.2's first 528 bytes)
+    if constexpr (kV32) {   // bytes 528..655: lane j takes 64 of them (16-byte aligned)
+      const uint8_t *rec = record_ptr(L, sid);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        g.rp[i] = g.ok ? tc::ldg_nc_v4(rec + 528 + 64 * j + 16 * i) : make_uint4(0, 0, 0, 0);
+    }
     if (g.ok) {
       const uint8_t *rec = record_ptr(L, sid);
       if ((reinterpret_cast<uintptr_t>(rec) & 31u) == 0) {   // chunk pairs are whole 32-byte sectors
@@ -310,6 +319,25 @@ __device__ __forceinline__ void issue_loads(const Params &p, const Cursor &c, in
 #pragma unroll
       for (int k = 0; k < 10; ++k) g.d[k] = z;
     }
+  }
+}
+
+// V3.2 records: this lane's 32 bf16 key dims 512 + 32j .. (g.rp) times the
+// row's 2^-e into the [128 x 64] f16 tile of dims 512..575 (K-major, one
+// SW128 k-block; chunks 4j .. 4j + 3 of the row).
+__device__ __forceinline__ void dequant_tail_v32(const Gather &g, float rnorm, int row, int j,
+                                                 uint32_t kr_base, int32_t *dbg) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {g.rp[i].x, g.rp[i].y, g.rp[i].z, g.rp[i].w};
+    uint32_t f[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      f[k] = tc::pack_f16x2(__uint_as_float(w[k] << 16) * rnorm,
+                            __uint_as_float(w[k] & 0xFFFF0000u) * rnorm);
+    const uint32_t off = sw128_off(row, 0, 4 * j + i, 0);
+    if (dbg_ok(dbg, off + 16u <= 16384u, kDbgSmemKv))
+      tc::st_shared_v4(kr_base + off, f[0], f[1], f[2], f[3]);
   }
 }
 
@@ -485,10 +513,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // output); the plain instantiation compiles none of their code. kM1: MODEL1
 // records as well, in instantiations of their own (with or without kExt).
 // kStrict: the plan carries a wait budget (a test knob); only that
-// instantiation compiles the exact-budget waits.
-template <int HPG, bool kExt, bool kStrict, bool kM1>
+// instantiation compiles the exact-budget waits. kV32: V3.2 records (576-dim
+// keys and Q: a 16 KB tile of the key dims 512..575 and a 9-block Q tile;
+// at most 32 heads per group, no RoPE).
+template <int HPG, bool kExt, bool kStrict, bool kM1, bool kV32>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
-  using Cfg = TcCfg<HPG>;
+  using Cfg = TcCfg<HPG, kV32>;
   constexpr int NH = Cfg::kHalf;
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -502,6 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   const uint32_t sbase = raw_base + pad;
   const uint32_t kv_base = sbase + Cfg::kKV;
   const uint32_t q_base = sbase + Cfg::kQ;
+  const uint32_t kr_base = sbase + Cfg::kKR;   // V3.2 records only
   const uint32_t p_base = sbase + Cfg::kP;
   int32_t *row_e_s = reinterpret_cast<int32_t *>(smem + Cfg::kRho);
   float *m_s = reinterpret_cast<float *>(smem + Cfg::kM);
@@ -596,7 +627,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const int32_t sid0 = load_sid(p, cu, row);
       prefetch(cu, sid0);
       prefetch(cn, sid_n1);
-      issue_loads<kM1>(p, cu, sid0, row, j, g);
+      issue_loads<kM1, kV32>(p, cu, sid0, row, j, g);
     }
     while (cu.u < u1) {
       const int32_t t = cu.t;
@@ -630,7 +661,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         } else {    // e from the largest exponent field of the 4 fp32 scales
           const uint32_t f = max(max((sv.x >> 23) & 0xFFu, (sv.y >> 23) & 0xFFu),
                                  max((sv.z >> 23) & 0xFFu, (sv.w >> 23) & 0xFFu));
-          erow = row_exp(f);
+          int fe = (int)f;
+          if constexpr (kV32) {
+            // and from the bf16 key dims' largest magnitude (exponent field
+            // minus 8, as for MODEL1), over both halves of the row
+            uint32_t bm = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              bm = __vmaxu2(bm, __vmaxu2(__vmaxu2(g.rp[i].x & 0x7FFF7FFFu, g.rp[i].y & 0x7FFF7FFFu),
+                                         __vmaxu2(g.rp[i].z & 0x7FFF7FFFu, g.rp[i].w & 0x7FFF7FFFu)));
+            bm = max(bm & 0xFFFFu, bm >> 16);
+            bm = max(bm, (uint32_t)__shfl_xor_sync(0xffffffffu, bm, 1));
+            fe = max(fe, (int)(bm >> 7) - 8);
+          }
+          erow = row_exp((uint32_t)max(fe, 0));
           const float rn = pow2i(-erow);
 #pragma unroll
           for (int b = 0; b < 4; ++b) scale2[b] = scale_f16x2(__uint_as_float(scale2[b]) * rn);
@@ -685,6 +729,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           dequant_block_model1(g, rnorm, mb, row, j, kv_base, p.status);
         else
           dequant_block(fp8, ue, g, scale2, rnorm, mb, row, j, kv_base, p.status);
+        if constexpr (kV32) {   // key dims 512..575 once the previous QK has read them
+          if (mb == 0) dequant_tail_v32(g, rnorm, row, j, kr_base, p.status);
+        }
       }
       // One hand-off per tile: the QK MMAs are issued once the whole tile is
       // in place, so per-block fences and arrives would only lengthen the
@@ -703,7 +750,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       cu = cn;
       cn = cn2;
       sid_n1 = sid_n2;
-      if (cu.u < u1) issue_loads<kM1>(p, cu, sid_next, row, j, g);
+      if (cu.u < u1) issue_loads<kM1, kV32>(p, cu, sid_next, row, j, g);
     }
   } else {
     // ======================================================== softmax / epilogue / MMA
@@ -751,6 +798,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const bool rl = lane >= 28;
       const int ca = rl ? 56 + (lane - 28) : 2 * lane, cb = rl ? 60 + (lane - 28) : 2 * lane + 1;
       uint4 qa[kQH], qb[kQH];
+      uint4 qc[kV32 ? kQH : 1];   // V3.2: lanes 0..7 also hold chunk 64 + lane (dims 512..575)
 #pragma unroll
       for (int i = 0; i < kQH; ++i) {
         const int hq = h0 + warp + kSmWarps * i;
@@ -758,8 +806,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         if (dbg_ok(p.status, t >= 0 && t < p.T && hq < p.H, kDbgQ)) {
           qa[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + ca);
           qb[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + cb);
+          if constexpr (kV32)
+            qc[i] = lane < 8 ? __ldg(reinterpret_cast<const uint4 *>(qh) + 64 + lane)
+                             : make_uint4(0, 0, 0, 0);
         } else {
           qa[i] = qb[i] = make_uint4(0, 0, 0, 0);
+          if constexpr (kV32) qc[i] = make_uint4(0, 0, 0, 0);
         }
       }
       // This lane's cos / sin from the token's table row: NeoX pairs
@@ -817,6 +869,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         float mx = 0.f;
 #pragma unroll
         for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(v[k]));
+        float vc[8];   // V3.2: the lane's dims of chunk 64 + lane (zeros past lane 7)
+        if constexpr (kV32) {
+          const uint32_t wc[4] = {qc[i].x, qc[i].y, qc[i].z, qc[i].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            vc[2 * k] = bf16_bits_to_f32(wc[k] & 0xFFFFu);
+            vc[2 * k + 1] = bf16_bits_to_f32(wc[k] >> 16);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx = fmaxf(mx, fabsf(vc[k]));
+        }
         // max |q| of the head: non-negative floats order as their bits
         const uint32_t mbits = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
         int e = mbits ? (int)((mbits >> 23) & 0xFF) - 127 : 0;
@@ -831,6 +894,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         if (dbg_ok(p.status, qo + 16u <= HPG * 1024u && qo1 + 16u <= HPG * 1024u, kDbgSmemQ)) {
           tc::st_shared_v4(q_base + qo, f[0], f[1], f[2], f[3]);
           tc::st_shared_v4(q_base + qo1, f[4], f[5], f[6], f[7]);
+        }
+        if constexpr (kV32) {   // chunk 64 + lane into k-block 8
+          if (lane < 8) {
+            uint32_t fc[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) fc[k] = tc::pack_f16x2(vc[2 * k] * down, vc[2 * k + 1] * down);
+            const uint32_t qo2 = sw128_off(h, 8, lane, HPG * 128);
+            if (dbg_ok(p.status, qo2 + 16u <= HPG * 1152u, kDbgSmemQ))
+              tc::st_shared_v4(q_base + qo2, fc[0], fc[1], fc[2], fc[3]);
+          }
         }
       }
       if (tid < HPG) m_s[tid] = kMaxInit;
@@ -978,6 +1051,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
               const uint64_t bd = dB_qk + (uint64_t)((kb * HPG * 128 + ks * 32) >> 4);
               tc::mma_f16(d_tmem, ad, bd, Cfg::kIdQK, (kb | ks) ? 1u : 0u);
             }
+          }
+          if constexpr (kV32) {   // key dims 512..575: the tail tile against Q's k-block 8
+            const uint64_t dA_kr = tc::sdesc(kr_base, 16, 1024, tc::kSwz128);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_f16(tmem + Cfg::kColS, dA_kr + (uint64_t)((ks * 32) >> 4),
+                          dB_qk + (uint64_t)((8 * HPG * 128 + ks * 32) >> 4), Cfg::kIdQK, 1u);
           }
           tc::mma_commit(&bars[kBarSFull]);
         }
@@ -1173,15 +1253,31 @@ bool dsa_tc_supports(int hpg) { return hpg == 16 || hpg == 32 || hpg == 64; }
 namespace {
 // Checks that the kernel kept exactly kLaunchRegs registers per thread (the
 // warpgroup register split assumes it) and raises its shared-memory limit.
-template <int N, bool E, bool S, bool M>
+template <int N, bool E, bool S, bool M, bool V = false>
 cudaError_t tc_setup(void *) {
   using namespace dsa;
   cudaFuncAttributes fa;
-  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E, S, M>);
+  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E, S, M, V>);
   if (err != cudaSuccess) return err;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(tc_decode_kernel<N, E, S, M>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<N>::kSmem);
+  return cudaFuncSetAttribute(tc_decode_kernel<N, E, S, M, V>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)TcCfg<N, V>::kSmem);
+}
+
+// V3.2 records (576-dim keys): groups of 16 or 32 heads only.
+template <int N>
+cudaError_t launch_v32(const dsa::Params &p, dim3 grid, dim3 block, cudaStream_t stream, int bit) {
+  using namespace dsa;
+  if constexpr (N > 32) {
+    return cudaErrorInvalidValue;
+  } else {
+    const cudaError_t err = dsa_configure_once(bit, &tc_setup<N, false, false, false, true>, nullptr);
+    if (err != cudaSuccess) return err;
+    tc_decode_kernel<N, false, false, false, true>
+        <<<grid, block, (int)TcCfg<N, true>::kSmem, stream>>>(p);
+    return cudaSuccess;
+  }
 }
 }  // namespace
 
@@ -1192,36 +1288,40 @@ cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
     return p.list[0].fmt == f || (p.nlists > 1 && p.list[1].fmt == f);
   };
   const bool m1 = has_fmt(DSA_REC_MODEL1_584);
+  const bool v32 = p.dqk == 576;
   const bool ext = p.rope_gptj || p.mx_on || has_fmt(DSA_REC_FP8_528_UE8M0);
   // exact-budget waits (a plan with a wait budget) exist for the plain form
   const bool strict = !ext && p.wait_budget > 0;
   cudaError_t err = cudaSuccess;
   switch (p.hpg) {
-#define DSA_TC_CASE(N, BIT)                                                              \
-  case N: {                                                                              \
-    const int smem = (int)TcCfg<N>::kSmem;                                               \
-    if (m1 && ext) {                                                                     \
-      err = dsa_configure_once(BIT + 28, &tc_setup<N, true, false, true>, nullptr);      \
-      if (err != cudaSuccess) return err;                                                \
-      tc_decode_kernel<N, true, false, true><<<grid, block, smem, stream>>>(p);          \
-    } else if (m1) {                                                                     \
-      err = dsa_configure_once(BIT + 32, &tc_setup<N, false, false, true>, nullptr);     \
-      if (err != cudaSuccess) return err;                                                \
-      tc_decode_kernel<N, false, false, true><<<grid, block, smem, stream>>>(p);         \
-    } else if (ext) {                                                                    \
-      err = dsa_configure_once(BIT + 20, &tc_setup<N, true, false, false>, nullptr);     \
-      if (err != cudaSuccess) return err;                                                \
-      tc_decode_kernel<N, true, false, false><<<grid, block, smem, stream>>>(p);         \
-    } else if (strict) {                                                                 \
-      err = dsa_configure_once(BIT + 24, &tc_setup<N, false, true, false>, nullptr);     \
-      if (err != cudaSuccess) return err;                                                \
-      tc_decode_kernel<N, false, true, false><<<grid, block, smem, stream>>>(p);         \
-    } else {                                                                             \
-      err = dsa_configure_once(BIT, &tc_setup<N, false, false, false>, nullptr);         \
-      if (err != cudaSuccess) return err;                                                \
-      tc_decode_kernel<N, false, false, false><<<grid, block, smem, stream>>>(p);        \
-    }                                                                                    \
-    break;                                                                               \
+#define DSA_TC_CASE(N, BIT)                                                                   \
+  case N: {                                                                                   \
+    const int smem = (int)TcCfg<N>::kSmem;                                                    \
+    if (v32) {                                                                                \
+      err = launch_v32<N>(p, grid, block, stream, BIT + 36);                                  \
+      if (err != cudaSuccess) return err;                                                     \
+    } else if (m1 && ext) {                                                                   \
+      err = dsa_configure_once(BIT + 28, &tc_setup<N, true, false, true>, nullptr);           \
+      if (err != cudaSuccess) return err;                                                     \
+      tc_decode_kernel<N, true, false, true, false><<<grid, block, smem, stream>>>(p);        \
+    } else if (m1) {                                                                          \
+      err = dsa_configure_once(BIT + 32, &tc_setup<N, false, false, true>, nullptr);          \
+      if (err != cudaSuccess) return err;                                                     \
+      tc_decode_kernel<N, false, false, true, false><<<grid, block, smem, stream>>>(p);       \
+    } else if (ext) {                                                                         \
+      err = dsa_configure_once(BIT + 20, &tc_setup<N, true, false, false>, nullptr);          \
+      if (err != cudaSuccess) return err;                                                     \
+      tc_decode_kernel<N, true, false, false, false><<<grid, block, smem, stream>>>(p);       \
+    } else if (strict) {                                                                      \
+      err = dsa_configure_once(BIT + 24, &tc_setup<N, false, true, false>, nullptr);          \
+      if (err != cudaSuccess) return err;                                                     \
+      tc_decode_kernel<N, false, true, false, false><<<grid, block, smem, stream>>>(p);       \
+    } else {                                                                                  \
+      err = dsa_configure_once(BIT, &tc_setup<N, false, false, false>, nullptr);              \
+      if (err != cudaSuccess) return err;                                                     \
+      tc_decode_kernel<N, false, false, false, false><<<grid, block, smem, stream>>>(p);      \
+    }                                                                                         \
+    break;                                                                                    \
   }
     DSA_TC_CASE(16, 0)
     DSA_TC_CASE(32, 1)

@@ -84,7 +84,7 @@ def test_ue8m0_record_format_is_accepted(lib):
     bad_extra = B.CacheDesc(FAKE + 8, 64, 64 * 288, 64, 1)
     assert run_v41(lib, a, out=FAKE, swa_desc=ue, extra_desc=bad_extra) == -3
     assert a.call(lib, swa_desc=ue, extra_desc=bad_extra) == -3
-    assert a.call(lib, swa_desc=B.CacheDesc(FAKE, 64, 64 * 528, 64, 4)) == -2   # no format 4
+    assert a.call(lib, swa_desc=B.CacheDesc(FAKE, 64, 64 * 656, 64, 5)) == -2   # no format 5
 
 
 def test_model1_record_format_is_accepted(lib):
