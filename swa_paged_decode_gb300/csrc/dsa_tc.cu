@@ -515,8 +515,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // kStrict: the plan carries a wait budget (a test knob); only that
 // instantiation compiles the exact-budget waits. kV32: V3.2 records (576-dim
 // keys and Q: a 16 KB tile of the key dims 512..575 and a 9-block Q tile;
-// at most 32 heads per group, no RoPE).
-template <int HPG, bool kExt, bool kStrict, bool kM1, bool kV32>
+// at most 32 heads per group, no RoPE). kShared: several head groups read
+// the same tiles (plain form); only group 0 prefetches records into L2.
+template <int HPG, bool kExt, bool kStrict, bool kM1, bool kV32, bool kShared = false>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   using Cfg = TcCfg<HPG, kV32>;
   constexpr int NH = Cfg::kHalf;
@@ -603,6 +604,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     // up and for fp8 tiles (see below).
     auto prefetch = [&](const Cursor &c, int32_t sid) {
       if (j != 0 || c.u >= u1) return;
+      if constexpr (kShared) {   // the other groups' loads find the records in L2
+        if (hg != 0) return;
+      }
       int32_t lid2, row02;
       cursor_tile(p, c, lid2, row02);
       const ListArgs &L = p.list[lid2];
@@ -1253,14 +1257,14 @@ bool dsa_tc_supports(int hpg) { return hpg == 16 || hpg == 32 || hpg == 64; }
 namespace {
 // Checks that the kernel kept exactly kLaunchRegs registers per thread (the
 // warpgroup register split assumes it) and raises its shared-memory limit.
-template <int N, bool E, bool S, bool M, bool V = false>
+template <int N, bool E, bool S, bool M, bool V = false, bool SH = false>
 cudaError_t tc_setup(void *) {
   using namespace dsa;
   cudaFuncAttributes fa;
-  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E, S, M, V>);
+  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E, S, M, V, SH>);
   if (err != cudaSuccess) return err;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(tc_decode_kernel<N, E, S, M, V>,
+  return cudaFuncSetAttribute(tc_decode_kernel<N, E, S, M, V, SH>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)TcCfg<N, V>::kSmem);
 }
@@ -1316,6 +1320,11 @@ cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
       err = dsa_configure_once(BIT + 24, &tc_setup<N, false, true, false>, nullptr);          \
       if (err != cudaSuccess) return err;                                                     \
       tc_decode_kernel<N, false, true, false, false><<<grid, block, smem, stream>>>(p);       \
+    } else if (p.HG > 1) {                                                                    \
+      err = dsa_configure_once(BIT + 40, &tc_setup<N, false, false, false, false, true>,      \
+                               nullptr);                                                      \
+      if (err != cudaSuccess) return err;                                                     \
+      tc_decode_kernel<N, false, false, false, false, true><<<grid, block, smem, stream>>>(p); \
     } else {                                                                                  \
       err = dsa_configure_once(BIT, &tc_setup<N, false, false, false>, nullptr);              \
       if (err != cudaSuccess) return err;                                                     \
