@@ -173,7 +173,14 @@ typedef struct {
   int64_t d_qk;             /* key / query dims the plan was made for: 512, or
                               576 (V3.2 records); 0 in a zeroed plan reads
                               as 512                                        */
-  int64_t reserved[10];
+  int64_t producer_q;       /* 1: on the plain tensor-core form (fp8-528 /
+                              NVFP4 records, no V4.1 options) the producer
+                              warps stage each token's Q and issue its first
+                              QK; set for 64 heads per group when the
+                              schedule gives fewer than 16 tiles per token
+                              segment. Either value computes the same
+                              result                                        */
+  int64_t reserved[9];
 } dsa_decode_plan_t;
 
 /* Plan one decode call.

@@ -49,8 +49,9 @@ class Plan(ctypes.Structure):
         [(n, ctypes.c_int64) for n in (
             "total_units", "ws_sel_offset", "ws_part_lse_offset", "ws_part_sel_offset",
             "ws_part_o_offset", "workspace_bytes", "ws_bounds_offset", "balance_live",
-            "ws_stage_offset", "workspace_bytes_mx", "wait_budget_cycles", "d_qk")] + \
-        [("reserved", ctypes.c_int64 * 10)]
+            "ws_stage_offset", "workspace_bytes_mx", "wait_budget_cycles", "d_qk",
+            "producer_q")] + \
+        [("reserved", ctypes.c_int64 * 9)]
 
 
 _lib = None

@@ -122,6 +122,7 @@ void fill_schedule(const dsa_decode_plan_t *plan, void *ws, Params &p) {
   p.bounds = reinterpret_cast<int64_t *>(w + plan->ws_bounds_offset);
   p.balance = (int32_t)plan->balance_live;
   p.wait_budget = plan->wait_budget_cycles > 0 ? (long long)plan->wait_budget_cycles : 0;
+  p.pq = plan->producer_q != 0 ? 1 : 0;
 }
 
 dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
@@ -366,6 +367,17 @@ dsa_status dsa_decode_plan_qk(int32_t num_tokens, int32_t num_heads, int32_t swa
   // the tiles per token) splits no token: then there is nothing to combine.
   const bool whole = !plan->balance_live && upc % plan->tiles_per_token == 0;
   plan->split_tokens = (ctas > 1 && !whole) ? (int32_t)(ctas - 1) : 0;
+  // Token boundaries: T tokens over the C CTAs of a head group make about
+  // T + C token segments. With fewer than 16 tiles per segment (the widths'
+  // tile counts stand in for the lengths) and 64 heads per group, the
+  // producer warps stage Q and issue a token's first QK (measured: config 3
+  // +5 %, config 4 +1.3 %, config 5 at T = 64 +4 %; at T = 1024, 29 tiles
+  // per segment, the other form is 1.5 % faster).
+  plan->producer_q =
+      (plan->kernel == dsa::kKernelTc && plan->heads_per_group == 64 && d_qk == 512 &&
+       (int64_t)num_tokens * plan->tiles_per_token < 16 * ((int64_t)num_tokens + ctas))
+          ? 1
+          : 0;
   // Workspace: status | sel[T][2] | part_lse[HG][2C][hpg] | part_sel[2C][2] |
   //            part_o[HG][2C][hpg][512] | bounds[C+1]
   //            (| stage[T][H][512] fp32, for MXFP8 output only)

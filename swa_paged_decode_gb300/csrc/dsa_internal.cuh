@@ -44,6 +44,7 @@ struct Params {
   const __nv_bfloat16 *q;
   int64_t q_st, q_sh;          // element strides
   int32_t dqk;                 // key / query dims: 512, or 576 (V3.2 records)
+  int32_t pq;                  // plan's producer_q: the producers stage Q (plain form)
   ListArgs list[2];
   int32_t nlists;
   const float *sink;           // [H] or null
@@ -299,8 +300,9 @@ __device__ inline float e2m1_to_f32(uint32_t nib) {
 // skip it (they may be captured into a CUDA graph, where no set-up call is
 // wanted). Thread-safe. Bits in use: tensor-core kernels 0-2 (plain), 20-22
 // (V4.1 options), 24-26 (exact-budget waits), 28-30 and 32-34 (MODEL1 records),
-// 36-37 (V3.2 records), 40-42 (head groups sharing tiles),
-// SIMT kernels 8-11, combine 16-18.
+// 36-37 (V3.2 records), 40-42 (head groups sharing tiles), 46 and 50
+// (producers staging Q, with and without shared tiles), SIMT kernels 8-11,
+// combine 16-18.
 cudaError_t dsa_configure_once(int bit, cudaError_t (*f)(void *), void *arg);
 
 // Programmatic dependent launch: the decode kernels let the combine grid be

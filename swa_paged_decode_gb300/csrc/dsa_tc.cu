@@ -88,7 +88,7 @@ struct TcCfg {
   static constexpr uint32_t kM = kHeadF + 256;           // [64] running max (log2)
   static constexpr uint32_t kRed = kM + 256;             // [4][64] f32
   static constexpr uint32_t kMisc = kRed + 1024;         // mbarriers, counters, tmem base
-  static constexpr uint32_t kBytes = kMisc + 256;   // bars 120 B, abort, tmem, counters
+  static constexpr uint32_t kBytes = kMisc + 256;   // bars 72 B, abort, tmem, counters
   static constexpr uint32_t kSmem = kBytes + 1024 > 232448u ? 232448u : kBytes + 1024;
   static constexpr uint32_t kCols = HPG == 16 ? 128 : (HPG == 32 ? 256 : 512);
   static constexpr uint32_t kColS = 0;                   // S block b at b*HPG
@@ -106,11 +106,13 @@ enum Bar : int {
   kBarSFull = 5,    // MMA commit -> softmax: S ready (and every earlier MMA done)
   kBarOFinal = 6,   // MMA commit -> softmax: last PV of a token done
   kBarDrain = 7,    // MMA commit -> issuer: every MMA issued so far done (abort path)
-  kNumBars = 8
+  kBarDrainQK = 8,  // producers' QK commits -> themselves: their MMAs done (abort path)
+  kNumBars = 9
 };
 constexpr uint32_t kMiscAbort = 8 * kNumBars;        // int32
 constexpr uint32_t kMiscTmem = kMiscAbort + 4;       // uint32
 constexpr uint32_t kMiscCnt = kMiscAbort + 8;        // [4][2] uint32: kept rows / checksum
+constexpr uint32_t kMiscQk = kMiscCnt + 32;          // uint32: producer warps done with opening tiles
 // Kept-row records ride in 4 slots indexed by the ordinal of the token among
 // the tokens with work: producers can be at most two such tokens ahead of the
 // softmax warps that read (and clear) a slot.
@@ -509,6 +511,36 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
                : "memory");
 }
 
+// S = K . Q^T over the whole tile into TMEM (columns kColS..): the 32 MMAs
+// (36 with the V3.2 tail tile) go out back to back from one thread, then a
+// commit to `sfull`. The issue loop holds no waits or warp syncs: an
+// mbarrier access of the issuing thread stalls its issue while earlier MMAs
+// stream operands.
+template <int HPG, bool kV32>
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t kv_base, uint32_t q_base,
+                                         uint32_t kr_base, uint64_t *sfull) {
+  using Cfg = TcCfg<HPG, kV32>;
+  const uint64_t dA = tc::sdesc(kv_base, 16, 1024, tc::kSwz128);
+  const uint64_t dB = tc::sdesc(q_base, 16, 1024, tc::kSwz128);
+#pragma unroll
+  for (int kb = 0; kb < 8; ++kb) {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t ad = dA + (uint64_t)((kb * 16384 + ks * 32) >> 4);
+      const uint64_t bd = dB + (uint64_t)((kb * HPG * 128 + ks * 32) >> 4);
+      tc::mma_f16(tmem + Cfg::kColS, ad, bd, Cfg::kIdQK, (kb | ks) ? 1u : 0u);
+    }
+  }
+  if constexpr (kV32) {   // key dims 512..575: the tail tile against Q's k-block 8
+    const uint64_t dA_kr = tc::sdesc(kr_base, 16, 1024, tc::kSwz128);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      tc::mma_f16(tmem + Cfg::kColS, dA_kr + (uint64_t)((ks * 32) >> 4),
+                  dB + (uint64_t)((8 * HPG * 128 + ks * 32) >> 4), Cfg::kIdQK, 1u);
+  }
+  tc::mma_commit(sfull);
+}
+
 // kExt: the V4.1 options (fp8 records with ue8m0 scales, GPT-J RoPE, MXFP8
 // output); the plain instantiation compiles none of their code. kM1: MODEL1
 // records as well, in instantiations of their own (with or without kExt).
@@ -517,7 +549,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // keys and Q: a 16 KB tile of the key dims 512..575 and a 9-block Q tile;
 // at most 32 heads per group, no RoPE). kShared: several head groups read
 // the same tiles (plain form); only group 0 prefetches records into L2.
-template <int HPG, bool kExt, bool kStrict, bool kM1, bool kV32, bool kShared = false>
+// kPQ (plain form, for schedules with few tiles per token): the producers,
+// idle at a token boundary once the next tile is written, stage the next
+// token's Q and issue its first QK, which then overlap the softmax warps'
+// finalize of the previous token. With many tiles per token the form
+// without it is faster (its steady state measured about 1.5 % shorter).
+template <int HPG, bool kExt, bool kStrict, bool kM1, bool kV32, bool kShared = false,
+          bool kPQ = false>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   using Cfg = TcCfg<HPG, kV32>;
   constexpr int NH = Cfg::kHalf;
@@ -543,6 +581,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   volatile int32_t *abort_s = reinterpret_cast<volatile int32_t *>(smem + Cfg::kMisc + kMiscAbort);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kMisc + kMiscTmem);
   uint32_t *cnt_s = reinterpret_cast<uint32_t *>(smem + Cfg::kMisc + kMiscCnt);
+  uint32_t *qk_cnt = reinterpret_cast<uint32_t *>(smem + Cfg::kMisc + kMiscQk);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hg = blockIdx.x % p.HG;
@@ -558,10 +597,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
   }
   if (tid == 0) {
     for (int b = 0; b < kNumBars; ++b)
-      tc::mbar_init(&bars[b], b == kBarKvFull ? kPrWarps : 1u);
+      tc::mbar_init(&bars[b], (b == kBarKvFull || b == kBarDrainQK) ? kPrWarps : 1u);
     tc::fence_mbar_init();
     *abort_s = 0;
     for (int i = 0; i < 8; ++i) cnt_s[i] = 0;
+    *qk_cnt = 0;
+  }
+  if constexpr (kPQ) {   // the running max of the first token (finalize resets it after)
+    if (tid < HPG) m_s[tid] = kMaxInit;
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -595,8 +638,136 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     const int pw = warp - kSmWarps;
     // the two lanes of a row hold its two halves (j), so they can trade data
     const int row = 16 * pw + (lane >> 1), j = lane & 1;
+    // kPQ: Q of token t -> f16 K-major SW128 tile, staged here once the
+    // token's first tile is written (the previous token's last QK has read the old
+    // Q by then: its PV blocks are free). RoPE in fp32 (NeoX or GPT-J), then
+    // a power-of-two prescale per head so its max |q| lies in [1, 2): exact
+    // for bf16 inputs whose exponents fit f16's range after scaling; the
+    // factor goes to headf_s. Warp pw stages heads pw, pw + 8, ..., kQB at a
+    // time (their loads issued together: one round trip per batch), each
+    // rotated, reduced and stored without any cross-warp step.
+    static_assert(HPG % kPrWarps == 0, "heads per producer warp");
+    constexpr int kQH = HPG / kPrWarps;
+    constexpr int kQB = kQH < 4 ? kQH : 4;
+    auto stage_q_pr = [&](int32_t t) {
+      int64_t pos = p.positions ? __ldg(p.positions + t) : 0;
+      if (pos < 0 || (p.cos_sin && pos >= p.cs_rows)) {   // outside the table: flag, row 0
+        if (pw == 0 && lane == 0) report_status(p.status, DSA_ERR_INVALID_ARG);
+        pos = 0;
+      }
+      // Lane -> dims: lanes 0..27 hold 8-dim chunks 2 lane and 2 lane + 1
+      // (dims 16 lane .. 16 lane + 15); lanes 28..31 (the RoPE dims
+      // 448..511) hold chunks 56 + r and 60 + r, r = lane - 28 (dims
+      // 448 + 8r .. +7 and 480 + 8r .. +7), so that both NeoX pairs
+      // (448 + i, 480 + i) and GPT-J pairs (448 + 2i, 449 + 2i) lie inside
+      // one lane and the rotation needs no shuffles.
+      const bool rl = lane >= 28;
+      const int ca = rl ? 56 + (lane - 28) : 2 * lane, cb = rl ? 60 + (lane - 28) : 2 * lane + 1;
+      const bool rope = p.cos_sin != nullptr;
+      const bool gptj = kExt && p.rope_gptj != 0;
+      const bool rot = rope && rl && dbg_ok(p.status, pos >= 0 && pos < p.cs_rows, kDbgTable);
+      // This lane's cos / sin from the token's table row: NeoX pairs
+      // 8r .. 8r + 7; GPT-J pairs 4r .. 4r + 3 (chunk 56 + r) and
+      // 16 + 4r .. 16 + 4r + 3 (chunk 60 + r). Entry i is cos, i + 32 sin.
+      // Re-read (from L1) for every head rather than held in registers.
+      const float4 *cs_row = rot ? reinterpret_cast<const float4 *>(p.cos_sin + pos * 64) : nullptr;
+      const int f0 = gptj ? lane - 28 : 2 * (lane - 28), f1 = gptj ? lane - 24 : 2 * (lane - 28) + 1;
+#pragma unroll 1
+      for (int i0 = 0; i0 < kQH; i0 += kQB) {
+        uint4 qa[kQB], qb[kQB];
+        uint4 qc[kV32 ? kQB : 1];   // V3.2: lanes 0..7 also hold chunk 64 + lane (dims 512..575)
+#pragma unroll
+        for (int i = 0; i < kQB; ++i) {
+          const int hq = h0 + pw + kPrWarps * (i0 + i);
+          const __nv_bfloat16 *qh = p.q + (int64_t)t * p.q_st + (int64_t)hq * p.q_sh;
+          if (dbg_ok(p.status, t >= 0 && t < p.T && hq < p.H, kDbgQ)) {
+            qa[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + ca);
+            qb[i] = __ldg(reinterpret_cast<const uint4 *>(qh) + cb);
+            if constexpr (kV32)
+              qc[i] = lane < 8 ? __ldg(reinterpret_cast<const uint4 *>(qh) + 64 + lane)
+                               : make_uint4(0, 0, 0, 0);
+          } else {
+            qa[i] = qb[i] = make_uint4(0, 0, 0, 0);
+            if constexpr (kV32) qc[i] = make_uint4(0, 0, 0, 0);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kQB; ++i) {
+          const int h = pw + kPrWarps * (i0 + i);
+          const uint32_t w[8] = {qa[i].x, qa[i].y, qa[i].z, qa[i].w, qb[i].x, qb[i].y, qb[i].z, qb[i].w};
+          float v[16];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            v[2 * k] = bf16_bits_to_f32(w[k] & 0xFFFFu);
+            v[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
+          }
+          if (rot) {
+            const float4 ca0 = tc::ldg_f4_here(cs_row + f0), ca1 = tc::ldg_f4_here(cs_row + f1);
+            const float4 sa0 = tc::ldg_f4_here(cs_row + 8 + f0), sa1 = tc::ldg_f4_here(cs_row + 8 + f1);
+            const float c8[8] = {ca0.x, ca0.y, ca0.z, ca0.w, ca1.x, ca1.y, ca1.z, ca1.w};
+            const float s8[8] = {sa0.x, sa0.y, sa0.z, sa0.w, sa1.x, sa1.y, sa1.z, sa1.w};
+            if (gptj) {   // (v[2m], v[2m+1]) pair 4r + m; (v[8+2m], v[9+2m]) pair 16 + 4r + m
+#pragma unroll
+              for (int m = 0; m < 8; ++m) {
+                const int a = 2 * m;   // m < 4: chunk A, else chunk B (c8/s8 index m)
+                const float x1 = v[a], x2 = v[a + 1];
+                v[a] = fmaf(x1, c8[m], -(x2 * s8[m]));
+                v[a + 1] = fmaf(x2, c8[m], x1 * s8[m]);
+              }
+            } else {      // (v[k], v[8+k]) pair 8r + k
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float x1 = v[k], x2 = v[8 + k];
+                v[k] = fmaf(x1, c8[k], -(x2 * s8[k]));
+                v[8 + k] = fmaf(x2, c8[k], x1 * s8[k]);
+              }
+            }
+          }
+          float mx = 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(v[k]));
+          float vc[8];   // V3.2: the lane's dims of chunk 64 + lane (zeros past lane 7)
+          if constexpr (kV32) {
+            const uint32_t wc[4] = {qc[i].x, qc[i].y, qc[i].z, qc[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              vc[2 * k] = bf16_bits_to_f32(wc[k] & 0xFFFFu);
+              vc[2 * k + 1] = bf16_bits_to_f32(wc[k] >> 16);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx = fmaxf(mx, fabsf(vc[k]));
+          }
+          // max |q| of the head: non-negative floats order as their bits
+          const uint32_t mbits = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+          int e = mbits ? (int)((mbits >> 23) & 0xFF) - 127 : 0;
+          e = e < -126 ? -126 : (e > 126 ? 126 : e);
+          const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+          if (lane == 0) headf_s[h] = p.scale_log2 * __uint_as_float((uint32_t)(127 + e) << 23);
+          uint32_t f[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] = tc::pack_f16x2(v[2 * k] * down, v[2 * k + 1] * down);
+          const uint32_t qo = sw128_off(h, ca >> 3, ca & 7, HPG * 128);
+          const uint32_t qo1 = sw128_off(h, cb >> 3, cb & 7, HPG * 128);
+          if (dbg_ok(p.status, qo + 16u <= HPG * 1024u && qo1 + 16u <= HPG * 1024u, kDbgSmemQ)) {
+            tc::st_shared_v4(q_base + qo, f[0], f[1], f[2], f[3]);
+            tc::st_shared_v4(q_base + qo1, f[4], f[5], f[6], f[7]);
+          }
+          if constexpr (kV32) {   // chunk 64 + lane into k-block 8
+            if (lane < 8) {
+              uint32_t fc[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) fc[k] = tc::pack_f16x2(vc[2 * k] * down, vc[2 * k + 1] * down);
+              const uint32_t qo2 = sw128_off(h, 8, lane, HPG * 128);
+              if (dbg_ok(p.status, qo2 + 16u <= HPG * 1152u, kDbgSmemQ))
+                tc::st_shared_v4(q_base + qo2, fc[0], fc[1], fc[2], fc[3]);
+            }
+          }
+        }
+      }
+    };
     uint32_t ph_free[4] = {0, 0, 0, 0};
     bool first = true;
+    bool new_tok = true;   // kPQ: the tile opens a token, Q is staged with it
     int warm = 0;
     uint32_t kept = 0, chk = 0, pord = 0;
     // Tile records are loaded into registers one tile ahead, and prefetched
@@ -737,12 +908,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
           if (mb == 0) dequant_tail_v32(g, rnorm, row, j, kr_base, p.status);
         }
       }
+      const bool opens = kPQ && new_tok;   // the token's first tile in this CTA
+      if constexpr (kPQ) {
+        if (opens) {
+          // The next tile's loads rewrite only part of g (by format and
+          // lane): clearing it here keeps the rest from being held in
+          // registers through the staging.
+          g = Gather{};
+          stage_q_pr(t);
+        }
+        new_tok = last_of_token;
+      }
       // One hand-off per tile: the QK MMAs are issued once the whole tile is
       // in place, so per-block fences and arrives would only lengthen the
       // dequant chain.
       tc::fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarKvFull]);
+      if constexpr (kPQ) {
+        if (lane == 0) {
+          mbar_arrive(&bars[kBarKvFull]);
+          // A token's first QK goes out from here, so that it runs while the
+          // softmax warps finalize the previous token: from lane 0 of the
+          // producer warp that lands its rows last (an acquire-release count
+          // of the warps done tells it, with no wait).
+          if (opens && (tc::atom_add_acq_rel_shared(qk_cnt, 1u) & (kPrWarps - 1)) == kPrWarps - 1 &&
+              !*abort_s) {
+            tc::tc_fence_after();
+            issue_qk<HPG, kV32>(tmem, kv_base, q_base, kr_base, &bars[kBarSFull]);
+          }
+        }
+      } else {
+        if (lane == 0) mbar_arrive(&bars[kBarKvFull]);
+      }
       first = false;
       // L2 prefetch two tiles ahead: while the CTA warms up, and always for
       // fp8 tiles, whose 17 sector loads per row otherwise keep the load
@@ -943,6 +1140,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         const int h = tid;
         const float l = red_s[h] + red_s[64 + h] + red_s[128 + h] + red_s[192 + h];
         const float m = seg_worked ? m_s[h] : -INFINITY;
+        if constexpr (kPQ) m_s[h] = kMaxInit;   // the next token's (ordered by the barrier below)
         float iv = 0.f;
         if (l > 0.f) {
           float den = l;
@@ -1031,10 +1229,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         first_pv = true;
 #pragma unroll
         for (int j = 0; j < NH; ++j) l_reg[j] = 0.f;
-        // Q is staged only for tokens with a live tile in this range.
-        Cursor cv = cu;
-        cursor_first_live(p, cv, seg.u_end);
-        if (cv.u < seg.u_end) stage_q(t);
+        if constexpr (!kPQ) {   // (kPQ: the producers stage it)
+          // Q is staged only for tokens with a live tile in this range.
+          Cursor cv = cu;
+          cursor_first_live(p, cv, seg.u_end);
+          if (cv.u < seg.u_end) stage_q(t);
+        }
       }
       if (!cursor_live(p, cu)) continue;
       seg_worked = true;
@@ -1042,10 +1242,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       // once the producers have landed all of it, which keeps the issue
       // loop free of waits and warp syncs (an mbarrier access of the issuing
       // thread stalls its issue while earlier MMAs stream operands).
+      // (kPQ: a token's first QK comes from the producers.)
       if (warp == 0) {
         wait(kBarKvFull, ph_kv);
         tc::tc_fence_after();
-        if (issuer && !*abort_s) {
+        if (issuer && !(kPQ && first_pv) && !*abort_s) {
 #pragma unroll
           for (int kb = 0; kb < 8; ++kb) {
             const uint32_t d_tmem = tmem + Cfg::kColS;
@@ -1242,6 +1443,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     tc::mma_commit(&bars[kBarDrain]);
     tc::mbar_wait(&bars[kBarDrain], 0u, kWaitBudget);
   }
+  if constexpr (kPQ) {   // the producers' lane 0 threads likewise (each may have issued QKs)
+    if (warp >= kSmWarps && lane == 0 && *abort_s) {
+      tc::mma_commit(&bars[kBarDrainQK]);
+      tc::mbar_wait(&bars[kBarDrainQK], 0u, kWaitBudget);
+    }
+  }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -1257,14 +1464,14 @@ bool dsa_tc_supports(int hpg) { return hpg == 16 || hpg == 32 || hpg == 64; }
 namespace {
 // Checks that the kernel kept exactly kLaunchRegs registers per thread (the
 // warpgroup register split assumes it) and raises its shared-memory limit.
-template <int N, bool E, bool S, bool M, bool V = false, bool SH = false>
+template <int N, bool E, bool S, bool M, bool V = false, bool SH = false, bool PQ = false>
 cudaError_t tc_setup(void *) {
   using namespace dsa;
   cudaFuncAttributes fa;
-  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E, S, M, V, SH>);
+  cudaError_t err = cudaFuncGetAttributes(&fa, tc_decode_kernel<N, E, S, M, V, SH, PQ>);
   if (err != cudaSuccess) return err;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(tc_decode_kernel<N, E, S, M, V, SH>,
+  return cudaFuncSetAttribute(tc_decode_kernel<N, E, S, M, V, SH, PQ>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)TcCfg<N, V>::kSmem);
 }
@@ -1283,6 +1490,29 @@ cudaError_t launch_v32(const dsa::Params &p, dim3 grid, dim3 block, cudaStream_t
     return cudaSuccess;
   }
 }
+
+// The plain form: head groups sharing tiles or not (SH), and at 64 heads per
+// group with `pq` the form whose producers stage Q (kPQ).
+template <int N, bool SH>
+cudaError_t launch_plain(const dsa::Params &p, bool pq, dim3 grid, dim3 block,
+                         cudaStream_t stream, int bit, int bit_pq) {
+  using namespace dsa;
+  const int smem = (int)TcCfg<N>::kSmem;
+  if constexpr (N == 64) {
+    if (pq) {
+      const cudaError_t err =
+          dsa_configure_once(bit_pq, &tc_setup<N, false, false, false, false, SH, true>, nullptr);
+      if (err != cudaSuccess) return err;
+      tc_decode_kernel<N, false, false, false, false, SH, true><<<grid, block, smem, stream>>>(p);
+      return cudaSuccess;
+    }
+  }
+  const cudaError_t err =
+      dsa_configure_once(bit, &tc_setup<N, false, false, false, false, SH>, nullptr);
+  if (err != cudaSuccess) return err;
+  tc_decode_kernel<N, false, false, false, false, SH><<<grid, block, smem, stream>>>(p);
+  return cudaSuccess;
+}
 }  // namespace
 
 cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
@@ -1296,6 +1526,8 @@ cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
   const bool ext = p.rope_gptj || p.mx_on || has_fmt(DSA_REC_FP8_528_UE8M0);
   // exact-budget waits (a plan with a wait budget) exist for the plain form
   const bool strict = !ext && p.wait_budget > 0;
+  // the plan's choice of the form whose producers stage Q (kPQ)
+  const bool pq = p.pq != 0;
   cudaError_t err = cudaSuccess;
   switch (p.hpg) {
 #define DSA_TC_CASE(N, BIT)                                                                   \
@@ -1321,14 +1553,11 @@ cudaError_t dsa_launch_tc(const dsa::Params &p, cudaStream_t stream) {
       if (err != cudaSuccess) return err;                                                     \
       tc_decode_kernel<N, false, true, false, false><<<grid, block, smem, stream>>>(p);       \
     } else if (p.HG > 1) {                                                                    \
-      err = dsa_configure_once(BIT + 40, &tc_setup<N, false, false, false, false, true>,      \
-                               nullptr);                                                      \
+      err = launch_plain<N, true>(p, pq, grid, block, stream, BIT + 40, BIT + 44);            \
       if (err != cudaSuccess) return err;                                                     \
-      tc_decode_kernel<N, false, false, false, false, true><<<grid, block, smem, stream>>>(p); \
     } else {                                                                                  \
-      err = dsa_configure_once(BIT, &tc_setup<N, false, false, false>, nullptr);              \
+      err = launch_plain<N, false>(p, pq, grid, block, stream, BIT, BIT + 48);                \
       if (err != cudaSuccess) return err;                                                     \
-      tc_decode_kernel<N, false, false, false, false><<<grid, block, smem, stream>>>(p);      \
     }                                                                                         \
     break;                                                                                    \
   }

@@ -77,6 +77,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long l
   return true;
 }
 
+// Shared-memory add with acquire-release order at CTA scope (the writes
+// that precede it in this thread are visible to the thread that observes
+// its result, and vice versa); returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_shared(uint32_t *a, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(smem_u32(a)), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -300,6 +312,16 @@ __device__ __forceinline__ uint2 ldg_nc_v2(const void *p) {
   return v;
 }
 
+// Read-only 16-byte load kept in L1, issued where it stands (volatile: not
+// merged with or hoisted above another load of the same address, so the
+// value need not stay in registers between uses).
+__device__ __forceinline__ float4 ldg_f4_here(const float4 *p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
 __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"

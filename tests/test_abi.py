@@ -255,3 +255,23 @@ def test_split_tokens_zero_only_when_every_token_is_whole(lib):
     assert p.balance_live == 1 and p.split_tokens == p.ctas_per_group - 1
     p, _ = B.dsa_decode_plan(400, 16, 128, 0, num_sms=152)     # 3 whole tokens per CTA
     assert p.units_per_cta == 3 and p.split_tokens == 0
+
+
+@pytest.mark.parametrize("T,H,ws,we,expect", [
+    (1024, 64, 128, 4096, 0),    # config 5: 33 tiles per token, ~29 per segment
+    (256, 64, 128, 4096, 0),     # ~21 per segment
+    (64, 64, 128, 4096, 1),      # ~10 per segment (tokens split over CTAs)
+    (128, 64, 128, 2048, 1),     # config 3 widths
+    (256, 128, 128, 2048, 1),    # config 4: two 64-head groups
+    (4096, 32, 128, 512, 0),     # 32 heads per group: the softmax warps stage Q
+])
+def test_plan_producer_q(lib, T, H, ws, we, expect):
+    """The form whose producers stage Q is planned for 64 heads per group and
+    fewer than 16 tiles per token segment (T tokens over C CTAs of a group:
+    T + C segments)."""
+    plan, _ = B.dsa_decode_plan(T, H, ws, we, 152)
+    C, tpt = plan.ctas_per_group, plan.tiles_per_token
+    rule = plan.heads_per_group == 64 and T * tpt < 16 * (T + C)
+    assert plan.producer_q == int(rule) == expect
+    p576, _ = B.dsa_decode_plan_qk(T, min(H, 64), ws, we, 152, 576)
+    assert p576.producer_q == 0                      # V3.2 records: groups of at most 32

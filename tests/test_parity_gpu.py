@@ -117,6 +117,25 @@ def test_forced_split_schedules(num_sms):
     compare(out, lse, kept, chk, oracle_ref(w), what=f"num_sms={num_sms}")
 
 
+@pytest.mark.parametrize("long_lists", [False, True])
+def test_q_staging_forms_at_64_heads(long_lists):
+    """Both forms of the 64-head kernel on the same kind of inputs: the
+    producers stage Q and issue a token's first QK when the schedule gives
+    few tiles per token segment (short lists), the softmax warps do with
+    many (long lists on few CTAs)."""
+    if long_lists:
+        w = small(45, T=8, H=64, swa_w=128, extra_w=4096, extra_lens=(3000, 4096),
+                  extra_slots=1 << 16)
+        dec, out, lse, kept, chk = run_gpu(w, num_sms=2)
+        assert dec.plan.producer_q == 0
+    else:
+        w = small(46, T=8, H=64, extra_lens=(1, 256))
+        dec, out, lse, kept, chk = run_gpu(w, num_sms=3)
+        assert dec.plan.producer_q == 1 and dec.plan.ctas_per_group > 1
+    assert dec.plan.heads_per_group == 64
+    compare(out, lse, kept, chk, oracle_ref(w), what=f"64 heads, long lists {long_lists}")
+
+
 def test_split_with_empty_partials():
     # Lengths so short that most split parts see no row at all.
     w = small(42, T=3, H=16, swa_lens=(0, 3), extra_lens=(0, 2))
