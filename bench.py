@@ -185,7 +185,7 @@ class Step:
         self.B = B
         self.mx = mx
         self.dec = B.Decoder(w, mx_group=MX_GROUP if mx else None)
-        self.has_combine = self.dec.plan.split_tokens > 0
+        self.has_combine = self.dec.plan.split_tokens > 0 and not self.dec.plan.merge_in_run
 
     def __call__(self, ev_k0=None, ev_k1=None):
         w, B, d = self.w, self.B, self.dec

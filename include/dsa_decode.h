@@ -180,7 +180,16 @@ typedef struct {
                               schedule gives fewer than 16 tiles per token
                               segment. Either value computes the same
                               result                                        */
-  int64_t reserved[9];
+  int64_t merge_in_run;     /* 1: the tensor-core run kernel merges every split
+                              token itself (the CTA that completes a token's
+                              units merges its parts), so dsa_decode_combine
+                              launches no merge; set when tokens have few
+                              parts (ctas_per_group <= 4 T) and a token
+                              spans at most 64 CTAs (min(ctas_per_group,
+                              tiles_per_token) <= 64)                       */
+  int64_t ws_count_offset;  /* int32 [head_groups][T] units done per token,
+                              zeroed by each run with the status word       */
+  int64_t reserved[7];
 } dsa_decode_plan_t;
 
 /* Plan one decode call.

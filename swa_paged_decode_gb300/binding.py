@@ -50,8 +50,8 @@ class Plan(ctypes.Structure):
             "total_units", "ws_sel_offset", "ws_part_lse_offset", "ws_part_sel_offset",
             "ws_part_o_offset", "workspace_bytes", "ws_bounds_offset", "balance_live",
             "ws_stage_offset", "workspace_bytes_mx", "wait_budget_cycles", "d_qk",
-            "producer_q")] + \
-        [("reserved", ctypes.c_int64 * 9)]
+            "producer_q", "merge_in_run", "ws_count_offset")] + \
+        [("reserved", ctypes.c_int64 * 7)]
 
 
 _lib = None

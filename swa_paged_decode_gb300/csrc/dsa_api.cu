@@ -123,6 +123,8 @@ void fill_schedule(const dsa_decode_plan_t *plan, void *ws, Params &p) {
   p.balance = (int32_t)plan->balance_live;
   p.wait_budget = plan->wait_budget_cycles > 0 ? (long long)plan->wait_budget_cycles : 0;
   p.pq = plan->producer_q != 0 ? 1 : 0;
+  p.merge = plan->merge_in_run != 0 ? 1 : 0;
+  p.tok_cnt = reinterpret_cast<int32_t *>(w + plan->ws_count_offset);
 }
 
 dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
@@ -221,7 +223,8 @@ dsa_status run_impl(const dsa_decode_plan_t *plan, void *workspace, size_t works
   fill_schedule(plan, workspace, p);
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, st);
+  // status word and the per-token unit counts of the in-run merge: one memset
+  cudaError_t e = cudaMemsetAsync(workspace, 0, (size_t)plan->ws_sel_offset, st);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   return cuda_status(plan->kernel == dsa::kKernelTc ? dsa_launch_tc(p, st)
                                                     : dsa_launch_simt(p, st));
@@ -253,7 +256,8 @@ dsa_status combine_impl(const dsa_decode_plan_t *plan, void *workspace, size_t w
   p.lse = lse;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (p.mx_on) p.stage = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan->ws_stage_offset);
-  cudaError_t e = dsa_launch_combine(p, st);
+  // (a plan whose run kernel merged the split tokens launches no merge here)
+  cudaError_t e = plan->merge_in_run ? cudaSuccess : dsa_launch_combine(p, st);
   if (e == cudaSuccess && p.mx_on) e = dsa_launch_mx_epilogue(p, st);
   return cuda_status(e);
 }
@@ -378,11 +382,28 @@ dsa_status dsa_decode_plan_qk(int32_t num_tokens, int32_t num_heads, int32_t swa
        (int64_t)num_tokens * plan->tiles_per_token < 16 * ((int64_t)num_tokens + ctas))
           ? 1
           : 0;
-  // Workspace: status | sel[T][2] | part_lse[HG][2C][hpg] | part_sel[2C][2] |
-  //            part_o[HG][2C][hpg][512] | bounds[C+1]
-  //            (| stage[T][H][512] fp32, for MXFP8 output only)
+  // Split tokens merged by the run kernel itself (tensor-core kernel): the
+  // CTA that completes a token's units merges its parts, at most 64 of them
+  // (their weights sit in a shared-memory buffer of 64 x heads-per-group
+  // floats; a token spans at most min(C, tiles per token) CTAs). One CTA
+  // reads every part of the token, so this pays only while tokens have few
+  // parts: about C / T + 1 on average, here at most 5 (C <= 4 T). Measured
+  // against the separate merge kernel: config 3 +5 %, config 4 +2 %,
+  // config 5 T = 256 +2.6 %, T = 1024 +1.2 %; at T = 8 (about 10 parts) it
+  // was 11 % slower and at T = 1 (33 parts) 37 % slower.
+  const int64_t span = ctas < plan->tiles_per_token ? ctas : (int64_t)plan->tiles_per_token;
+  plan->merge_in_run = (plan->kernel == dsa::kKernelTc && plan->split_tokens > 0 && span <= 64 &&
+                        ctas <= 4 * (int64_t)num_tokens)
+                           ? 1
+                           : 0;
+  // Workspace: status | count[HG][T] | sel[T][2] | part_lse[HG][2C][hpg] |
+  //            part_sel[2C][2] | part_o[HG][2C][hpg][512] | bounds[C+1]
+  //            (| stage[T][H][512] fp32, for MXFP8 output only); each run
+  //            zeroes everything before sel
   const int64_t slots = 2 * ctas;
   int64_t off = kStatusBytes;
+  plan->ws_count_offset = off;
+  off = align_up(off + 4 * (int64_t)plan->head_groups * num_tokens, kAlignWs);
   plan->ws_sel_offset = off;
   off = align_up(off + 8 * (int64_t)num_tokens, kAlignWs);
   plan->ws_part_lse_offset = off;

@@ -45,6 +45,8 @@ struct Params {
   int64_t q_st, q_sh;          // element strides
   int32_t dqk;                 // key / query dims: 512, or 576 (V3.2 records)
   int32_t pq;                  // plan's producer_q: the producers stage Q (plain form)
+  int32_t merge;               // plan's merge_in_run: the run kernel merges split tokens
+  int32_t *tok_cnt;            // [HG][T] units of each token done (zeroed per run)
   ListArgs list[2];
   int32_t nlists;
   const float *sink;           // [H] or null
@@ -120,7 +122,8 @@ __device__ inline int64_t token_cost(int64_t live) {
 // Unit range [u0, u1) of CTA c. Called by every thread of the block (it
 // synchronizes the block; blockDim.x a multiple of 32, at most 1024); scr:
 // shared scratch of blockDim.x + 2 + blockDim.x / 32 int64. Also publishes
-// the range to p.bounds for the combine kernel.
+// the range to p.bounds (both ends, so that a CTA merging a split token
+// finds every part's range written by that part) for the merge.
 __device__ inline void cta_range(const Params &p, int32_t c, int64_t *scr, int64_t &u0,
                                  int64_t &u1) {
   const int n = blockDim.x, tid = threadIdx.x;
@@ -130,7 +133,7 @@ __device__ inline void cta_range(const Params &p, int32_t c, int64_t *scr, int64
     u1 = u0 + p.upc < p.U ? u0 + p.upc : p.U;
     if (tid == 0) {
       p.bounds[c] = u0;
-      if (c == p.C - 1) p.bounds[p.C] = p.U;
+      p.bounds[c + 1] = u1;   // also written by CTA c + 1 (same value)
     }
     return;
   }
@@ -208,7 +211,7 @@ __device__ inline void cta_range(const Params &p, int32_t c, int64_t *scr, int64
   __syncthreads();   // scratch free again
   if (tid == 0) {
     p.bounds[c] = u0;
-    if (c == p.C - 1) p.bounds[p.C] = p.U;
+    p.bounds[c + 1] = u1;   // also written by CTA c + 1 (same value)
   }
 }
 

@@ -1112,6 +1112,134 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       sm_bar();   // Q (async proxy), head factors and m_s visible
     };
 
+    // Split token t, merged in the run by the CTA that completed its units
+    // (the combine kernel's arithmetic, parts in CTA order, so the result
+    // does not depend on which CTA merges): parts are the CTAs c0..c1 whose
+    // ranges meet the token's units [ts, te) -- every one of them has
+    // arrived, and each wrote both ends of its range to p.bounds before its
+    // partial. M = max_i lse_i, w_i = e^{lse_i - M}, out = sum_i w_i O_i /
+    // (sum_i w_i + e^{sink - M}), lse = M + log sum_i w_i. The weights sit
+    // in the P buffer (free between a token's last PV and the next
+    // token's first softmax): at most 64 parts (the plan's condition).
+    auto merge_token = [&](int32_t t) {
+      const int64_t ts = (int64_t)t * p.tpt, te = ts + p.tpt;
+      int32_t c0 = cta, c1 = cta;
+      while (c0 > 0 && __ldcg(reinterpret_cast<const long long *>(p.bounds) + c0) > ts) --c0;
+      while (c1 + 1 < p.C && __ldcg(reinterpret_cast<const long long *>(p.bounds) + c1 + 1) < te) ++c1;
+      const bool c0_late = __ldcg(reinterpret_cast<const long long *>(p.bounds) + c0) < ts;
+      // partial slot of part c: 2c when t is the CTA's first token, else 2c + 1
+      auto slot_of = [&](int32_t c) -> int64_t {
+        return 2 * (int64_t)c + ((c == c0 && c0_late) ? 1 : 0);
+      };
+      int np = c1 - c0 + 1;   // >= 1; at most 64 by the plan, held here in every build
+      if (np > 64) {
+        if (tid == 0) report_status(p.status, DSA_ERR_UNSUPPORTED);
+        np = 0;
+      }
+      const int64_t sb = (int64_t)hg * 2 * p.C;
+      const int64_t part_n = (int64_t)p.HG * 2 * p.C * HPG;
+      float *w_s = reinterpret_cast<float *>(smem + Cfg::kP);   // [np][HPG]
+      if (tid < HPG) {
+        const int h = tid;
+        float mx = -INFINITY;
+        for (int q = 0; q < np; ++q) {
+          const int64_t ip = (sb + slot_of(c0 + q)) * HPG + h;
+          const float li = dbg_ok(p.status, ip >= 0 && ip < part_n, kDbgPartial)
+                               ? __ldcg(p.part_lse + ip) : -INFINITY;
+          w_s[q * HPG + h] = li;
+          mx = fmaxf(mx, li);
+        }
+        float z = 0.f;
+        for (int q = 0; q < np; ++q) {
+          const float li = w_s[q * HPG + h];
+          const float w = (li == -INFINITY) ? 0.f : expf(li - mx);
+          w_s[q * HPG + h] = w;
+          z += w;
+        }
+        float inv = 0.f;
+        if (z > 0.f) {
+          float den = z;
+          if (p.sink) den = (sink_h == INFINITY) ? INFINITY : z + expf(sink_h - mx);
+          inv = 1.f / den;
+        }
+        red_s[h] = inv;
+        const int64_t il = (int64_t)t * p.H + h0 + h;
+        if (dbg_ok(p.status, il >= 0 && il < (int64_t)p.T * p.H, kDbgOut))
+          p.lse[il] = (z > 0.f) ? mx + logf(z) : -INFINITY;
+      }
+      if (tid == 64 && hg == 0) {   // row-selection record: sum over the parts
+        uint32_t k = 0, s2 = 0;
+        for (int q = 0; q < np; ++q) {
+          const int64_t sl = slot_of(c0 + q);
+          if (!dbg_ok(p.status, sl >= 0 && sl < 2 * p.C, kDbgSel)) continue;
+          k += (uint32_t)__ldcg(p.part_sel + 2 * sl);
+          s2 += (uint32_t)__ldcg(p.part_sel + 2 * sl + 1);
+        }
+        if (dbg_ok(p.status, t >= 0 && t < p.T, kDbgSel)) {
+          p.sel[2 * (int64_t)t] = (int32_t)k;
+          p.sel[2 * (int64_t)t + 1] = (int32_t)s2;
+        }
+      }
+      sm_bar();
+      // out = sum_i w_i O_i * inv: thread items e = tid + 256 k, head
+      // e / 128, float4 e % 128 of it; 8 items at a time, two parts' loads
+      // in flight together.
+      constexpr int kItems = HPG * (kD / 4) / 256;
+      static_assert(kItems % 8 == 0, "merge items per thread");
+      const float4 *po = reinterpret_cast<const float4 *>(p.part_o);
+      float *const stage = kExt ? p.stage : nullptr;
+#pragma unroll 1
+      for (int k0 = 0; k0 < kItems; k0 += 8) {
+        float4 acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int q = 0; q < np; q += 2) {
+          const bool two = q + 1 < np;
+          const int64_t s0 = (sb + slot_of(c0 + q)) * HPG;
+          const int64_t s1 = two ? (sb + slot_of(c0 + q + 1)) * HPG : s0;
+          float4 o0[8], o1[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int e = tid + 256 * (k0 + i), h = e >> 7, d4 = e & 127;
+            const bool ok0 = dbg_ok(p.status, s0 + h >= 0 && s0 + h < part_n, kDbgPartial);
+            const bool ok1 = dbg_ok(p.status, s1 + h >= 0 && s1 + h < part_n, kDbgPartial);
+            o0[i] = ok0 ? __ldcg(po + (s0 + h) * (kD / 4) + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            o1[i] = (two && ok1) ? __ldcg(po + (s1 + h) * (kD / 4) + d4)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int h = (tid + 256 * (k0 + i)) >> 7;
+            const float w0 = w_s[q * HPG + h], w1 = two ? w_s[(q + 1) * HPG + h] : 0.f;
+            acc[i].x = fmaf(w1, o1[i].x, fmaf(w0, o0[i].x, acc[i].x));
+            acc[i].y = fmaf(w1, o1[i].y, fmaf(w0, o0[i].y, acc[i].y));
+            acc[i].z = fmaf(w1, o1[i].z, fmaf(w0, o0[i].z, acc[i].z));
+            acc[i].w = fmaf(w1, o1[i].w, fmaf(w0, o0[i].w, acc[i].w));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = tid + 256 * (k0 + i), h = e >> 7, d4 = e & 127;
+          const float inv = red_s[h];
+          const int64_t io = ((int64_t)t * p.H + h0 + h) * kD + 4 * d4;
+          if (!dbg_ok(p.status, io >= 0 && io + 4 <= (int64_t)p.T * p.H * kD, kDbgOut)) continue;
+          if (stage != nullptr) {   // MXFP8 output: fp32 to the staging area, cast later
+            *reinterpret_cast<float4 *>(stage + io) =
+                make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
+            continue;
+          }
+          const __nv_bfloat162 a = __floats2bfloat162_rn(acc[i].x * inv, acc[i].y * inv);
+          const __nv_bfloat162 b = __floats2bfloat162_rn(acc[i].z * inv, acc[i].w * inv);
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t *>(&a);
+          pk.y = *reinterpret_cast<const uint32_t *>(&b);
+          *reinterpret_cast<uint2 *>(p.out + io) = pk;
+        }
+      }
+      sm_bar();   // weights and red_s free again
+    };
+
     // Token finished: sums over rows, sink, out / lse (or partial), selection.
     auto finalize = [&](const Segment &seg) {
       if (seg_worked) wait(kBarOFinal, ph_of);
@@ -1213,6 +1341,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       }
       tc::tc_fence_before();
       sm_bar();   // O read out (next PV may overwrite it); red_s free again
+      if (p.merge && !seg.whole) {
+        // Split token: count this part's units; the part that completes the
+        // token merges it. Every thread's partial stores are fenced before
+        // the count, the merging CTA fences again before reading the parts.
+        __threadfence();
+        int last = 0;
+        if (tid == 0) {
+          const int32_t units = (int32_t)(seg.u_end - seg.u_begin);
+          const int64_t ic = (int64_t)hg * p.T + seg.t;
+          if (dbg_ok(p.status, ic >= 0 && ic < (int64_t)p.HG * p.T, kDbgPartial))
+            last = atomicAdd(p.tok_cnt + ic, units) + units == p.tpt;
+        }
+        if (sm_bar_or(last)) {
+          __threadfence();
+          merge_token(seg.t);
+        }
+      }
     };
 
     Segment seg;

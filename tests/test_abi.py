@@ -275,3 +275,19 @@ def test_plan_producer_q(lib, T, H, ws, we, expect):
     assert plan.producer_q == int(rule) == expect
     p576, _ = B.dsa_decode_plan_qk(T, min(H, 64), ws, we, 152, 576)
     assert p576.producer_q == 0                      # V3.2 records: groups of at most 32
+
+
+@pytest.mark.parametrize("T,H,ws,we,sms", [(1024, 64, 128, 4096, 152), (1, 64, 128, 4096, 152),
+                                           (2, 64, 128, 9000, 1000), (4, 16, 128, 0, 152)])
+def test_plan_merge_in_run_and_count_block(lib, T, H, ws, we, sms):
+    """Split tokens are merged by the run kernel when tokens have few parts
+    (C <= 4 T) and a token spans at most 64 CTAs; the per-token unit counts it uses ([head_groups][T] int32) sit
+    between the status word and the selection records, inside the block each
+    run zeroes."""
+    plan, nbytes = B.dsa_decode_plan(T, H, ws, we, sms)
+    span = min(plan.ctas_per_group, plan.tiles_per_token)
+    expect = int(plan.split_tokens > 0 and span <= 64 and plan.ctas_per_group <= 4 * T)
+    assert plan.merge_in_run == expect
+    assert plan.ws_count_offset >= 4
+    assert plan.ws_count_offset + 4 * plan.head_groups * T <= plan.ws_sel_offset
+    assert plan.ws_sel_offset % 256 == 0 and plan.ws_sel_offset <= nbytes

@@ -136,6 +136,18 @@ def test_q_staging_forms_at_64_heads(long_lists):
     compare(out, lse, kept, chk, oracle_ref(w), what=f"64 heads, long lists {long_lists}")
 
 
+@pytest.mark.parametrize("num_sms", [16, 1000])
+def test_split_tokens_merged_in_run_or_by_combine(num_sms):
+    """Tokens of 72 tiles split over CTAs: on 16 SMs each spans a few CTAs and
+    the run kernel merges it (the CTA that completes its units); on 1000 a
+    token spans more than 64 CTAs and the combine kernel merges it."""
+    w = small(47, T=8, H=64, extra_w=9000, extra_lens=(8000, 9000), extra_slots=1 << 16)
+    dec, out, lse, kept, chk = run_gpu(w, num_sms=num_sms)
+    assert dec.plan.split_tokens > 0
+    assert dec.plan.merge_in_run == (1 if num_sms == 16 else 0)
+    compare(out, lse, kept, chk, oracle_ref(w), what=f"merge, num_sms={num_sms}")
+
+
 def test_split_with_empty_partials():
     # Lengths so short that most split parts see no row at all.
     w = small(42, T=3, H=16, swa_lens=(0, 3), extra_lens=(0, 2))
