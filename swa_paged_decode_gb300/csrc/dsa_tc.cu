@@ -971,7 +971,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     const float4 *m_s4 = reinterpret_cast<const float4 *>(m_s) + half * (NH / 4);
     // per head: scale * log2(e) * 2^e, e the exponent of the head's Q prescale
     const float4 *hf_s4 = reinterpret_cast<const float4 *>(headf_s) + half * (NH / 4);
-    int32_t cur_t = -1;
     bool seg_worked = false, first_pv = true;
     // the sink logit of head tid, read once (finalize needs it per token)
     const float sink_h = (tid < HPG && p.sink) ? __ldg(p.sink + h0 + tid) : 0.f;
@@ -1360,224 +1359,221 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       }
     };
 
-    Segment seg;
-    seg.t = -1;
-    for (Cursor cu = cursor_at(p, u0); cu.u < u1; cursor_step(p, cu)) {
+    // One pass per token segment of the range: set-up, its tiles, then
+    // finalize (the per-token work stays outside the tile loop).
+    Cursor cu = cursor_at(p, u0);
+    while (cu.u < u1) {
       const int32_t t = cu.t;
-      int32_t lid, row0;
-      cursor_tile(p, cu, lid, row0);
-      if (t != cur_t) {
-        if (cur_t >= 0) finalize(seg);
-        cur_t = t;
-        seg = make_segment(p, cta, t, u0, u1);
-        seg_worked = false;
-        first_pv = true;
+      const Segment seg = make_segment(p, cta, t, u0, u1);
+      seg_worked = false;
+      first_pv = true;
 #pragma unroll
-        for (int j = 0; j < NH; ++j) l_reg[j] = 0.f;
-        if constexpr (!kPQ) {   // (kPQ: the producers stage it)
-          // Q is staged only for tokens with a live tile in this range.
-          Cursor cv = cu;
-          cursor_first_live(p, cv, seg.u_end);
-          if (cv.u < seg.u_end) stage_q(t);
-        }
+      for (int j = 0; j < NH; ++j) l_reg[j] = 0.f;
+      if constexpr (!kPQ) {   // (kPQ: the producers stage it)
+        // Q is staged only for tokens with a live tile in this range.
+        Cursor cv = cu;
+        cursor_first_live(p, cv, seg.u_end);
+        if (cv.u < seg.u_end) stage_q(t);
       }
-      if (!cursor_live(p, cu)) continue;
-      seg_worked = true;
-      // ---- S = K . Q^T over the whole tile: the MMAs go out back to back
-      // once the producers have landed all of it, which keeps the issue
-      // loop free of waits and warp syncs (an mbarrier access of the issuing
-      // thread stalls its issue while earlier MMAs stream operands).
-      // (kPQ: a token's first QK comes from the producers.)
-      if (warp == 0) {
-        wait(kBarKvFull, ph_kv);
+      for (; cu.u < u1 && cu.t == t; cursor_step(p, cu)) {
+        if (!cursor_live(p, cu)) continue;
+        seg_worked = true;
+        // ---- S = K . Q^T over the whole tile: the MMAs go out back to back
+        // once the producers have landed all of it, which keeps the issue
+        // loop free of waits and warp syncs (an mbarrier access of the issuing
+        // thread stalls its issue while earlier MMAs stream operands).
+        // (kPQ: a token's first QK comes from the producers.)
+        if (warp == 0) {
+          wait(kBarKvFull, ph_kv);
+          tc::tc_fence_after();
+          if (issuer && !(kPQ && first_pv) && !*abort_s) {
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb) {
+              const uint32_t d_tmem = tmem + Cfg::kColS;
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t ad = dA_qk + (uint64_t)((kb * 16384 + ks * 32) >> 4);
+                const uint64_t bd = dB_qk + (uint64_t)((kb * HPG * 128 + ks * 32) >> 4);
+                tc::mma_f16(d_tmem, ad, bd, Cfg::kIdQK, (kb | ks) ? 1u : 0u);
+              }
+            }
+            if constexpr (kV32) {   // key dims 512..575: the tail tile against Q's k-block 8
+              const uint64_t dA_kr = tc::sdesc(kr_base, 16, 1024, tc::kSwz128);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                tc::mma_f16(tmem + Cfg::kColS, dA_kr + (uint64_t)((ks * 32) >> 4),
+                            dB_qk + (uint64_t)((8 * HPG * 128 + ks * 32) >> 4), Cfg::kIdQK, 1u);
+            }
+            tc::mma_commit(&bars[kBarSFull]);
+          }
+          __syncwarp();
+        } else {
+          // the row flags are written with block 0 of the tile
+          wait(kBarKvFull, ph_kv);
+        }
+        // This thread's row: kept or not, and its exponent e (the tile holds
+        // k * 2^-e). In log2 units the row's score is x = S * hf * 2^e; the
+        // running max m and P work on y = x + e, so P = 2^(y - m) carries the
+        // factor 2^e that PV needs to rebuild k from the tile, while the row
+        // sums take P * 2^-e = 2^(x - m): out = O / l and lse = m + log2 l
+        // keep their form. Rows that are not kept get y = -inf (P = 0).
+        const int32_t ei = row_e_s[prow];
+        const bool rv = ei != kRowInvalid;
+        const float er = rv ? (float)ei : -INFINITY;
+        const float rs = rv ? pow2i(ei) : 0.f;
+        const float rinv = rv ? pow2i(-ei) : 0.f;
+        wait(kBarSFull, ph_s);
         tc::tc_fence_after();
-        if (issuer && !(kPQ && first_pv) && !*abort_s) {
+        // S of this thread's row and head half (TMEM -> registers)
+        auto load_s = [&](float (&v)[NH]) {
+          if constexpr (NH % 32 == 0) {
 #pragma unroll
-          for (int kb = 0; kb < 8; ++kb) {
-            const uint32_t d_tmem = tmem + Cfg::kColS;
+            for (int g32 = 0; g32 < NH / 32; ++g32) {
+              const uint32_t c = tl_lane + Cfg::kColS + half * NH + 32 * g32;
+              uint32_t a[16], b[16];
+              tc::tmem_ld16x2(c, c + 16, a, b);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t ad = dA_qk + (uint64_t)((kb * 16384 + ks * 32) >> 4);
-              const uint64_t bd = dB_qk + (uint64_t)((kb * HPG * 128 + ks * 32) >> 4);
-              tc::mma_f16(d_tmem, ad, bd, Cfg::kIdQK, (kb | ks) ? 1u : 0u);
+              for (int i = 0; i < 16; ++i) {
+                v[32 * g32 + i] = __uint_as_float(a[i]);
+                v[32 * g32 + 16 + i] = __uint_as_float(b[i]);
+              }
+            }
+          } else {
+            tc::tmem_ld<NH>(tl_lane + Cfg::kColS + half * NH, v);
+          }
+        };
+        // P as f16, MN-major [128 rows, HPG]
+        auto store_p = [&](const float (&v)[NH]) {
+#pragma unroll
+          for (int k = 0; k < NH / 8; ++k) {
+            uint32_t pw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pw[e] = tc::pack_f16x2(v[8 * k + 2 * e], v[8 * k + 2 * e + 1]);
+            const int ci = half * (NH / 8) + k;
+            const uint32_t po = p_off<HPG>(prow, ci);
+            if (dbg_ok(p.status, po + 16u <= Cfg::kPBytes, kDbgSmemP))
+              tc::st_shared_v4(p_base + po, pw[0], pw[1], pw[2], pw[3]);
+          }
+        };
+        float x[NH];
+        load_s(x);
+        // Scores and, against the current running max, P -- optimistically:
+        // the max moves on only when a score passes it by kRescaleSlack (a few
+        // tiles per token), and then the whole group redoes P below.
+        // (The token's first tile always raises the max from its initial
+        // value: it goes straight to the exact pass.)
+        bool need = first_pv;
+        if (!first_pv) {
+#pragma unroll
+          for (int g4 = 0; g4 < NH / 4; ++g4) {
+            const float4 m4 = m_s4[g4], f4 = hf_s4[g4];
+            const float mm[4] = {m4.x, m4.y, m4.z, m4.w}, hf[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float &xv = x[4 * g4 + i];
+              const float t = fmaf(xv, hf[i] * rs, er - mm[i]);   // y - m (-inf if not kept)
+              need |= t > kRescaleSlack;
+              xv = tc::ex2(t);
             }
           }
-          if constexpr (kV32) {   // key dims 512..575: the tail tile against Q's k-block 8
-            const uint64_t dA_kr = tc::sdesc(kr_base, 16, 1024, tc::kSwz128);
+          store_p(x);
+          tc::fence_async_smem();
+        }
+        tc::tc_fence_before();
+        if (sm_bar_or(need ? 1 : 0)) {
+          // Raise the running max to the tile max; rescale sums and O; redo P.
+          tc::tc_fence_after();
+          load_s(x);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc::mma_f16(tmem + Cfg::kColS, dA_kr + (uint64_t)((ks * 32) >> 4),
-                          dB_qk + (uint64_t)((8 * HPG * 128 + ks * 32) >> 4), Cfg::kIdQK, 1u);
+          for (int j = 0; j < NH; ++j) x[j] = fmaf(x[j], headf_s[half * NH + j] * rs, er);   // y
+          // Per-head max over the warp's 32 rows by recursive halving, in
+          // place (x is reloaded below): at step st a lane keeps the upper
+          // half of its 2 st values when lane bit st is set, else the lower,
+          // and takes the max with the partner's copy of that half; head j
+          // ends in lane j (NH < 32: lanes j, j + NH, ... are folded last).
+#pragma unroll
+          for (int st = NH / 2; st >= 1; st >>= 1) {
+            const bool up = (lane & st) != 0;
+#pragma unroll
+            for (int i = 0; i < st; ++i) {
+              const float send = up ? x[i] : x[i + st];
+              const float keep = up ? x[i + st] : x[i];
+              x[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, st));
+            }
           }
-          tc::mma_commit(&bars[kBarSFull]);
+#pragma unroll
+          for (int off = NH; off < 32; off <<= 1) x[0] = fmaxf(x[0], __shfl_xor_sync(0xffffffffu, x[0], off));
+          if (lane < NH) red_s[q4 * 64 + half * NH + lane] = x[0];
+          sm_bar();
+          if (tid < HPG) {   // new max and rescale factor of head tid (factor -> red_s[tid])
+            const float tm = fmaxf(fmaxf(red_s[tid], red_s[64 + tid]), fmaxf(red_s[128 + tid], red_s[192 + tid]));
+            const float mo = m_s[tid];
+            const float mn = fmaxf(mo, tm);
+            red_s[tid] = tc::ex2(mo - mn);   // 0 when mo is still kMaxInit
+            m_s[tid] = mn;
+          }
+          sm_bar();
+#pragma unroll
+          for (int j = 0; j < NH; ++j) l_reg[j] *= red_s[half * NH + j];
+          if (!first_pv) {
+#pragma unroll 1
+            for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+              for (int g8 = 0; g8 < NH / 8; ++g8) {
+                float o[8];
+                const uint32_t ta = tl_lane + Cfg::kColO + mb * HPG + half * NH + 8 * g8;
+                tc::tmem_ld<8>(ta, o);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] *= red_s[half * NH + 8 * g8 + i];
+                tc::tmem_st<8>(ta, o);
+              }
+            }
+          }
+          load_s(x);
+#pragma unroll
+          for (int j = 0; j < NH; ++j) x[j] = fmaf(x[j], headf_s[half * NH + j] * rs, er);   // y
+#pragma unroll
+          for (int g4 = 0; g4 < NH / 4; ++g4) {
+            const float4 m4 = m_s4[g4];
+            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float &xv = x[4 * g4 + i];
+              xv = tc::ex2(xv - mm[i]);   // y = -inf (row not kept): 0
+            }
+          }
+          store_p(x);
+          tc::fence_async_smem();
+          tc::tc_fence_before();
+          sm_bar();   // P, O and red_s settled before PV
+        }
+#pragma unroll
+        for (int j = 0; j < NH; ++j) l_reg[j] = fmaf(x[j], rinv, l_reg[j]);   // += 2^(x - m)
+        // ---- O^T += K^T . P
+        if (issuer && !*abort_s) {
+          tc::tc_fence_after();
+          // M blocks unrolled with compile-time indices (runtime-indexed
+          // operands slowed the issue loop measurably).
+#pragma unroll
+          for (int mb = 0; mb < 4; ++mb) {
+            const uint64_t ab = dA_pv + (uint64_t)((2 * mb * 16384) >> 4);
+            const uint32_t dt = tmem + Cfg::kColO + mb * HPG;
+            tc::mma_f16(dt, ab, dB_pv, Cfg::kIdPV, first_pv ? 0u : 1u);
+#pragma unroll
+            for (int ks = 1; ks < 8; ++ks)
+              tc::mma_f16(dt, ab + (uint64_t)((ks * 2048) >> 4),
+                          dB_pv + (uint64_t)((ks * 16 * Cfg::kPRow) >> 4), Cfg::kIdPV, 1u);
+            tc::mma_commit(&bars[kBarKvFree + mb]);
+          }
+          Cursor cv = cu;
+          cursor_next_live(p, cv, seg.u_end);
+          if (cv.u >= seg.u_end) tc::mma_commit(&bars[kBarOFinal]);   // last PV of this token
         }
         __syncwarp();
-      } else {
-        // the row flags are written with block 0 of the tile
-        wait(kBarKvFull, ph_kv);
+        first_pv = false;
       }
-      // This thread's row: kept or not, and its exponent e (the tile holds
-      // k * 2^-e). In log2 units the row's score is x = S * hf * 2^e; the
-      // running max m and P work on y = x + e, so P = 2^(y - m) carries the
-      // factor 2^e that PV needs to rebuild k from the tile, while the row
-      // sums take P * 2^-e = 2^(x - m): out = O / l and lse = m + log2 l
-      // keep their form. Rows that are not kept get y = -inf (P = 0).
-      const int32_t ei = row_e_s[prow];
-      const bool rv = ei != kRowInvalid;
-      const float er = rv ? (float)ei : -INFINITY;
-      const float rs = rv ? pow2i(ei) : 0.f;
-      const float rinv = rv ? pow2i(-ei) : 0.f;
-      wait(kBarSFull, ph_s);
-      tc::tc_fence_after();
-      // S of this thread's row and head half (TMEM -> registers)
-      auto load_s = [&](float (&v)[NH]) {
-        if constexpr (NH % 32 == 0) {
-#pragma unroll
-          for (int g32 = 0; g32 < NH / 32; ++g32) {
-            const uint32_t c = tl_lane + Cfg::kColS + half * NH + 32 * g32;
-            uint32_t a[16], b[16];
-            tc::tmem_ld16x2(c, c + 16, a, b);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              v[32 * g32 + i] = __uint_as_float(a[i]);
-              v[32 * g32 + 16 + i] = __uint_as_float(b[i]);
-            }
-          }
-        } else {
-          tc::tmem_ld<NH>(tl_lane + Cfg::kColS + half * NH, v);
-        }
-      };
-      // P as f16, MN-major [128 rows, HPG]
-      auto store_p = [&](const float (&v)[NH]) {
-#pragma unroll
-        for (int k = 0; k < NH / 8; ++k) {
-          uint32_t pw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) pw[e] = tc::pack_f16x2(v[8 * k + 2 * e], v[8 * k + 2 * e + 1]);
-          const int ci = half * (NH / 8) + k;
-          const uint32_t po = p_off<HPG>(prow, ci);
-          if (dbg_ok(p.status, po + 16u <= Cfg::kPBytes, kDbgSmemP))
-            tc::st_shared_v4(p_base + po, pw[0], pw[1], pw[2], pw[3]);
-        }
-      };
-      float x[NH];
-      load_s(x);
-      // Scores and, against the current running max, P -- optimistically:
-      // the max moves on only when a score passes it by kRescaleSlack (a few
-      // tiles per token), and then the whole group redoes P below.
-      // (The token's first tile always raises the max from its initial
-      // value: it goes straight to the exact pass.)
-      bool need = first_pv;
-      if (!first_pv) {
-#pragma unroll
-        for (int g4 = 0; g4 < NH / 4; ++g4) {
-          const float4 m4 = m_s4[g4], f4 = hf_s4[g4];
-          const float mm[4] = {m4.x, m4.y, m4.z, m4.w}, hf[4] = {f4.x, f4.y, f4.z, f4.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float &xv = x[4 * g4 + i];
-            const float t = fmaf(xv, hf[i] * rs, er - mm[i]);   // y - m (-inf if not kept)
-            need |= t > kRescaleSlack;
-            xv = tc::ex2(t);
-          }
-        }
-        store_p(x);
-        tc::fence_async_smem();
-      }
-      tc::tc_fence_before();
-      if (sm_bar_or(need ? 1 : 0)) {
-        // Raise the running max to the tile max; rescale sums and O; redo P.
-        tc::tc_fence_after();
-        load_s(x);
-#pragma unroll
-        for (int j = 0; j < NH; ++j) x[j] = fmaf(x[j], headf_s[half * NH + j] * rs, er);   // y
-        // Per-head max over the warp's 32 rows by recursive halving, in
-        // place (x is reloaded below): at step st a lane keeps the upper
-        // half of its 2 st values when lane bit st is set, else the lower,
-        // and takes the max with the partner's copy of that half; head j
-        // ends in lane j (NH < 32: lanes j, j + NH, ... are folded last).
-#pragma unroll
-        for (int st = NH / 2; st >= 1; st >>= 1) {
-          const bool up = (lane & st) != 0;
-#pragma unroll
-          for (int i = 0; i < st; ++i) {
-            const float send = up ? x[i] : x[i + st];
-            const float keep = up ? x[i + st] : x[i];
-            x[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, st));
-          }
-        }
-#pragma unroll
-        for (int off = NH; off < 32; off <<= 1) x[0] = fmaxf(x[0], __shfl_xor_sync(0xffffffffu, x[0], off));
-        if (lane < NH) red_s[q4 * 64 + half * NH + lane] = x[0];
-        sm_bar();
-        if (tid < HPG) {   // new max and rescale factor of head tid (factor -> red_s[tid])
-          const float tm = fmaxf(fmaxf(red_s[tid], red_s[64 + tid]), fmaxf(red_s[128 + tid], red_s[192 + tid]));
-          const float mo = m_s[tid];
-          const float mn = fmaxf(mo, tm);
-          red_s[tid] = tc::ex2(mo - mn);   // 0 when mo is still kMaxInit
-          m_s[tid] = mn;
-        }
-        sm_bar();
-#pragma unroll
-        for (int j = 0; j < NH; ++j) l_reg[j] *= red_s[half * NH + j];
-        if (!first_pv) {
-#pragma unroll 1
-          for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll
-            for (int g8 = 0; g8 < NH / 8; ++g8) {
-              float o[8];
-              const uint32_t ta = tl_lane + Cfg::kColO + mb * HPG + half * NH + 8 * g8;
-              tc::tmem_ld<8>(ta, o);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) o[i] *= red_s[half * NH + 8 * g8 + i];
-              tc::tmem_st<8>(ta, o);
-            }
-          }
-        }
-        load_s(x);
-#pragma unroll
-        for (int j = 0; j < NH; ++j) x[j] = fmaf(x[j], headf_s[half * NH + j] * rs, er);   // y
-#pragma unroll
-        for (int g4 = 0; g4 < NH / 4; ++g4) {
-          const float4 m4 = m_s4[g4];
-          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float &xv = x[4 * g4 + i];
-            xv = tc::ex2(xv - mm[i]);   // y = -inf (row not kept): 0
-          }
-        }
-        store_p(x);
-        tc::fence_async_smem();
-        tc::tc_fence_before();
-        sm_bar();   // P, O and red_s settled before PV
-      }
-#pragma unroll
-      for (int j = 0; j < NH; ++j) l_reg[j] = fmaf(x[j], rinv, l_reg[j]);   // += 2^(x - m)
-      // ---- O^T += K^T . P
-      if (issuer && !*abort_s) {
-        tc::tc_fence_after();
-        // M blocks unrolled with compile-time indices (runtime-indexed
-        // operands slowed the issue loop measurably).
-#pragma unroll
-        for (int mb = 0; mb < 4; ++mb) {
-          const uint64_t ab = dA_pv + (uint64_t)((2 * mb * 16384) >> 4);
-          const uint32_t dt = tmem + Cfg::kColO + mb * HPG;
-          tc::mma_f16(dt, ab, dB_pv, Cfg::kIdPV, first_pv ? 0u : 1u);
-#pragma unroll
-          for (int ks = 1; ks < 8; ++ks)
-            tc::mma_f16(dt, ab + (uint64_t)((ks * 2048) >> 4),
-                        dB_pv + (uint64_t)((ks * 16 * Cfg::kPRow) >> 4), Cfg::kIdPV, 1u);
-          tc::mma_commit(&bars[kBarKvFree + mb]);
-        }
-        Cursor cv = cu;
-        cursor_next_live(p, cv, seg.u_end);
-        if (cv.u >= seg.u_end) tc::mma_commit(&bars[kBarOFinal]);   // last PV of this token
-      }
-      __syncwarp();
-      first_pv = false;
+      finalize(seg);
     }
-    if (cur_t >= 0) finalize(seg);
   }
 
   // After a wait gave up, MMAs issued before it may still be running: the
