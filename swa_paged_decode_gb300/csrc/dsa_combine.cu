@@ -222,41 +222,57 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
 // the token's position; pairs lie inside a thread's 4 dims), an ue8m0 scale
 // E = ceil(log2(max(amax, 1e-10) * fp32(1/448))) + 127 and e4m3 codes of
 // x * 2^(127 - E) (round to nearest even, saturating), o-fused layout.
-// Warp = one (token, head, 128-dim quarter); 8 lanes = one 32-dim chunk.
+// A warp takes kMxUnits consecutive (token, head, 128-dim quarter) units;
+// 8 lanes = one 32-dim chunk.
 constexpr int kMxThreads = 256;
+constexpr int kMxUnits = 4;   // units per warp, their loads in flight together
 
 __global__ void __launch_bounds__(kMxThreads) mx_epilogue_kernel(Params p) {
   pdl_wait_primary();   // the staged outputs are complete and visible
-  const int64_t unit = (int64_t)blockIdx.x * (kMxThreads / 32) + (threadIdx.x >> 5);
-  if (unit >= (int64_t)p.T * p.H * 4) return;   // whole warps leave together
-  const int lane = threadIdx.x & 31, quarter = (int)(unit & 3);
-  const int64_t th = unit >> 2;
-  const int64_t t = th / p.H;
-  const int h = (int)(th - t * p.H);
-  const int d0 = 128 * quarter + 4 * lane;
-  const float4 v = __ldg(reinterpret_cast<const float4 *>(p.stage + th * kD + d0));
-  float x[4] = {v.x, v.y, v.z, v.w};
-  const float *cs_row = mx_rope_row(p, t);
-  if (cs_row != nullptr && d0 >= kRopeStart) {
+  const int64_t units = (int64_t)p.T * p.H * 4;
+  const int64_t w0 = ((int64_t)blockIdx.x * (kMxThreads / 32) + (threadIdx.x >> 5)) * kMxUnits;
+  const int lane = threadIdx.x & 31;
+  // the warp's units' 512-byte rows, loaded together (kMxUnits in flight)
+  float4 v[kMxUnits];
 #pragma unroll
-    for (int pr = 0; pr < 2; ++pr) {
-      const int i = (d0 - kRopeStart) / 2 + pr;
-      const float c = __ldg(cs_row + i), sn = __ldg(cs_row + kRopeHalf + i);
-      const float oe = x[2 * pr], oo = x[2 * pr + 1];
-      x[2 * pr] = fmaf(oe, c, sn * oo);
-      x[2 * pr + 1] = fmaf(oo, c, -(sn * oe));
-    }
+  for (int i = 0; i < kMxUnits; ++i) {
+    const int64_t unit = w0 + i;
+    v[i] = unit < units
+               ? __ldg(reinterpret_cast<const float4 *>(p.stage + (unit >> 2) * kD + 128 * (unit & 3)) + lane)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
-  for (int off = 4; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-  const uint32_t E = ue8m0_ceil(fmaxf(a, 1e-10f) * (1.0f / 448.0f));
-  const float sc = ue8m0_inverse(E);
-  const uint32_t codes =
-      e4m3x2_rn_sat(x[0] * sc, x[1] * sc) | (e4m3x2_rn_sat(x[2] * sc, x[3] * sc) << 16);
-  const int c = d0 >> 5;
-  *reinterpret_cast<uint32_t *>(mx_chunk(p, t, h, c) + (d0 & 31)) = codes;
-  if ((d0 & 31) == 0) *mx_scale_byte(p, t, h, c) = (uint8_t)E;
+  for (int i = 0; i < kMxUnits; ++i) {
+    const int64_t unit = w0 + i;
+    if (unit >= units) break;   // whole warps leave together
+    const int quarter = (int)(unit & 3);
+    const int64_t th = unit >> 2;
+    const int64_t t = th / p.H;
+    const int h = (int)(th - t * p.H);
+    const int d0 = 128 * quarter + 4 * lane;
+    float x[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    const float *cs_row = mx_rope_row(p, t);
+    if (cs_row != nullptr && d0 >= kRopeStart) {
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr) {
+        const int k = (d0 - kRopeStart) / 2 + pr;
+        const float c = __ldg(cs_row + k), sn = __ldg(cs_row + kRopeHalf + k);
+        const float oe = x[2 * pr], oo = x[2 * pr + 1];
+        x[2 * pr] = fmaf(oe, c, sn * oo);
+        x[2 * pr + 1] = fmaf(oo, c, -(sn * oe));
+      }
+    }
+    float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    const uint32_t E = ue8m0_ceil(fmaxf(a, 1e-10f) * (1.0f / 448.0f));
+    const float sc = ue8m0_inverse(E);
+    const uint32_t codes =
+        e4m3x2_rn_sat(x[0] * sc, x[1] * sc) | (e4m3x2_rn_sat(x[2] * sc, x[3] * sc) << 16);
+    const int c = d0 >> 5;
+    *reinterpret_cast<uint32_t *>(mx_chunk(p, t, h, c) + (d0 & 31)) = codes;
+    if ((d0 & 31) == 0) *mx_scale_byte(p, t, h, c) = (uint8_t)E;
+  }
 }
 
 }  // namespace dsa
@@ -314,7 +330,8 @@ cudaError_t dsa_launch_mx_epilogue(const dsa::Params &p, cudaStream_t stream) {
   using namespace dsa;
   const int64_t units = (int64_t)p.T * p.H * 4;
   if (units == 0) return cudaSuccess;
-  const int64_t blocks = (units + kMxThreads / 32 - 1) / (kMxThreads / 32);
+  const int64_t per_block = (int64_t)(kMxThreads / 32) * kMxUnits;
+  const int64_t blocks = (units + per_block - 1) / per_block;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
   // Programmatic dependent of the kernel before it (combine, or the decode
   // kernel when nothing was split): it waits for that grid's completion.
