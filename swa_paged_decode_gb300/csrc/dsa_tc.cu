@@ -1122,10 +1122,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
     // token's first softmax): at most 64 parts (the plan's condition).
     auto merge_token = [&](int32_t t) {
       const int64_t ts = (int64_t)t * p.tpt, te = ts + p.tpt;
-      int32_t c0 = cta, c1 = cta;
-      while (c0 > 0 && __ldcg(reinterpret_cast<const long long *>(p.bounds) + c0) > ts) --c0;
-      while (c1 + 1 < p.C && __ldcg(reinterpret_cast<const long long *>(p.bounds) + c1 + 1) < te) ++c1;
-      const bool c0_late = __ldcg(reinterpret_cast<const long long *>(p.bounds) + c0) < ts;
+      const long long *bnd = reinterpret_cast<const long long *>(p.bounds);
+      int32_t *info = reinterpret_cast<int32_t *>(red_s + 128);   // c0, c1, c0 late
+      if (warp == 0) {
+        // The range starts around this CTA in one round trip (lane: CTA
+        // cta - 16 + lane): c0 = the last CTA at or before this one whose
+        // range starts at or before ts, c1 + 1 = the first after it whose
+        // range starts at or past te. Lanes beyond the parts may read ends
+        // that CTAs not involved have not written yet; the ballots take
+        // the bit nearest this CTA, which lies among the parts. A token
+        // spanning beyond the window walks on from its edge.
+        const int cb = cta - 16 + lane;
+        const long long bv = (cb >= 0 && cb <= p.C) ? __ldcg(bnd + cb) : 0;
+        const unsigned le = __ballot_sync(0xffffffffu, cb >= 0 && cb <= cta && bv <= ts);
+        const unsigned ge = __ballot_sync(0xffffffffu, cb > cta && cb <= p.C && bv >= te);
+        if (lane == 0) {
+          int32_t c0 = le ? cta - 16 + (31 - __clz(le)) : cta - 16;
+          int32_t c1 = ge ? cta - 16 + (__ffs(ge) - 1) - 1 : cta + 15;
+          if (!le)
+            while (c0 > 0 && __ldcg(bnd + c0) > ts) --c0;
+          if (!ge)
+            while (c1 + 1 < p.C && __ldcg(bnd + c1 + 1) < te) ++c1;
+          c0 = c0 < 0 ? 0 : c0;
+          c1 = c1 > p.C - 1 ? p.C - 1 : c1;
+          info[0] = c0;
+          info[1] = c1;
+          info[2] = __ldcg(bnd + c0) < ts ? 1 : 0;
+        }
+      }
+      sm_bar();
+      const int32_t c0 = info[0], c1 = info[1];
+      const bool c0_late = info[2] != 0;
       // partial slot of part c: 2c when t is the CTA's first token, else 2c + 1
       auto slot_of = [&](int32_t c) -> int64_t {
         return 2 * (int64_t)c + ((c == c0 && c0_late) ? 1 : 0);
@@ -1138,16 +1165,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
       const int64_t sb = (int64_t)hg * 2 * p.C;
       const int64_t part_n = (int64_t)p.HG * 2 * p.C * HPG;
       float *w_s = reinterpret_cast<float *>(smem + Cfg::kP);   // [np][HPG]
-      if (tid < HPG) {
+      // the parts' lse, one load per thread and round
+      for (int e = tid; e < np * HPG; e += 256) {
+        const int q = e / HPG, h = e - q * HPG;
+        const int64_t ip = (sb + slot_of(c0 + q)) * HPG + h;
+        w_s[e] = dbg_ok(p.status, ip >= 0 && ip < part_n, kDbgPartial) ? __ldcg(p.part_lse + ip)
+                                                                     : -INFINITY;
+      }
+      if (warp == 2 && hg == 0) {   // row-selection record: lanes over the parts
+        uint32_t k = 0, s2 = 0;
+        for (int q = lane; q < np; q += 32) {
+          const int64_t sl = slot_of(c0 + q);
+          if (!dbg_ok(p.status, sl >= 0 && sl < 2 * p.C, kDbgSel)) continue;
+          k += (uint32_t)__ldcg(p.part_sel + 2 * sl);
+          s2 += (uint32_t)__ldcg(p.part_sel + 2 * sl + 1);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          k += __shfl_xor_sync(0xffffffffu, k, off);
+          s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+        }
+        if (lane == 0 && dbg_ok(p.status, t >= 0 && t < p.T, kDbgSel)) {
+          p.sel[2 * (int64_t)t] = (int32_t)k;
+          p.sel[2 * (int64_t)t + 1] = (int32_t)s2;
+        }
+      }
+      sm_bar();
+      if (tid < HPG) {   // weights of head tid: M = max_q lse_q, w_q = e^{lse_q - M}
         const int h = tid;
         float mx = -INFINITY;
-        for (int q = 0; q < np; ++q) {
-          const int64_t ip = (sb + slot_of(c0 + q)) * HPG + h;
-          const float li = dbg_ok(p.status, ip >= 0 && ip < part_n, kDbgPartial)
-                               ? __ldcg(p.part_lse + ip) : -INFINITY;
-          w_s[q * HPG + h] = li;
-          mx = fmaxf(mx, li);
-        }
+        for (int q = 0; q < np; ++q) mx = fmaxf(mx, w_s[q * HPG + h]);
         float z = 0.f;
         for (int q = 0; q < np; ++q) {
           const float li = w_s[q * HPG + h];
@@ -1165,19 +1212,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(Params p) {
         const int64_t il = (int64_t)t * p.H + h0 + h;
         if (dbg_ok(p.status, il >= 0 && il < (int64_t)p.T * p.H, kDbgOut))
           p.lse[il] = (z > 0.f) ? mx + logf(z) : -INFINITY;
-      }
-      if (tid == 64 && hg == 0) {   // row-selection record: sum over the parts
-        uint32_t k = 0, s2 = 0;
-        for (int q = 0; q < np; ++q) {
-          const int64_t sl = slot_of(c0 + q);
-          if (!dbg_ok(p.status, sl >= 0 && sl < 2 * p.C, kDbgSel)) continue;
-          k += (uint32_t)__ldcg(p.part_sel + 2 * sl);
-          s2 += (uint32_t)__ldcg(p.part_sel + 2 * sl + 1);
-        }
-        if (dbg_ok(p.status, t >= 0 && t < p.T, kDbgSel)) {
-          p.sel[2 * (int64_t)t] = (int32_t)k;
-          p.sel[2 * (int64_t)t + 1] = (int32_t)s2;
-        }
       }
       sm_bar();
       // out = sum_i w_i O_i * inv: thread items e = tid + 256 k, head
