@@ -43,9 +43,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # while the kernel sources hash to `sources`. The capture is summarised under
 # profiles/ with the command that made it.
 NCU_TRAFFIC = {
-    "sources": "de9ce770af925f03",
+    "sources": "0024d884f97371c5",
     "workload": "config5_T256_H64",
-    "bytes_per_launch": 444729600 + 27802624,
+    "bytes_per_launch": 444022784 + 26824192,
     "rows_per_launch": 256 * (128 + 4096),
 }
 KERNEL_SOURCES = ("swa_paged_decode_gb300/csrc/dsa_tc.cu", "swa_paged_decode_gb300/csrc/tc_ptx.cuh",
